@@ -1,0 +1,242 @@
+"""Seeded synthetic inputs for the speculative-decoding verify step.
+
+This module is the only code shared by the CPU oracle's tests and the CUDA
+path.  It draws random numbers and lays them out; it computes none of the
+method's arithmetic (no softmax, no acceptance test, no sampling).  Draft
+tokens are therefore NOT produced here: they come from a draft-sampling
+implementation (the oracle in tests, the CUDA `spec_draft_sample` in the
+benchmark), fed with the uniforms `u_draft` drawn here.
+
+Logit recipe (Zipf-like rows with Gaussian noise, the shape the verify step
+sees from a real target/draft pair):
+
+* target row:  z_t[v] = -a * ln(1 + pi(v)) + N(0, sigma_t^2), with pi a fresh
+  permutation of the vocabulary per row.  pi is a random affine permutation
+  pi(v) = (m*v + c) mod V with gcd(m, V) = 1, which is cheap to draw for
+  thousands of 128K-wide rows and keeps each row's multiset of logits exactly
+  Zipf + noise;
+* draft row i of a sequence: z_d = z_t(target row i of that sequence) +
+  N(0, sigma_d^2);
+* bf16 workloads are generated in fp32 and rounded to bf16 here
+  (round-to-nearest-even on the fp32 bit pattern), so that both sides read
+  identical bits.
+
+Uniforms are fp32 multiples of 2^-24 in [0, 1), drawn from a Philox generator
+in the fixed order u_accept, u_resample, u_draft.
+
+Layout (packed, ragged k per sequence):
+  k_offsets [B+1] int32, exclusive prefix sum of k_b (k_offsets[0] = 0)
+  target_logits [k_offsets[B] + B, V]  rows o_b .. o_b + k_b with o_b = k_offsets[b] + b
+  draft_logits  [k_offsets[B], V]      rows k_offsets[b] .. k_offsets[b+1]-1
+  u_accept [k_offsets[B]], u_resample [k_offsets[B] + B], u_draft [k_offsets[B]]
+  temperature [B] fp32 (0 = greedy)
+bf16 arrays are numpy uint16 holding the bf16 bit patterns.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+F32 = "f32"
+BF16 = "bf16"
+
+# The five workloads: (B, k or None for ragged 1..10, V, dtype, temperature
+# rule, a, sigma_t, sigma_d rule).
+CONFIGS = {
+    1: dict(name="tiny_B4_k4_V1000_f32", B=4, k=4, V=1000, dtype=F32,
+            temperature=1.0, a=1.1, sigma_t=1.0, sigma_d=0.5),
+    2: dict(name="B8_k4_V32000_f32", B=8, k=4, V=32000, dtype=F32,
+            temperature=1.0, a=1.1, sigma_t=1.0, sigma_d=0.5),
+    3: dict(name="B64_k5_V128256_bf16_T0.7", B=64, k=5, V=128256, dtype=BF16,
+            temperature=0.7, a=1.1, sigma_t=1.5, sigma_d=1.0),
+    4: dict(name="B256_k8_V152064_bf16_half_greedy", B=256, k=8, V=152064,
+            dtype=BF16, temperature="odd_greedy", a=1.1, sigma_t=1.0,
+            sigma_d="uniform_0.2_1.5"),
+    5: dict(name="B512_ragged_k1to10_V128256_bf16", B=512, k="ragged_1_10",
+            V=128256, dtype=BF16, temperature=1.0, a=1.1, sigma_t=1.0,
+            sigma_d=0.5),
+}
+
+
+@dataclass
+class Workload:
+    """One batch of verify-step inputs (host numpy arrays)."""
+
+    name: str
+    B: int
+    V: int
+    dtype: str
+    k_offsets: np.ndarray          # int32 [B+1]
+    temperature: np.ndarray        # float32 [B]
+    target_logits: np.ndarray      # float32 or uint16(bf16 bits) [R_t, V]
+    draft_logits: np.ndarray       # same dtype [R_d, V]
+    u_accept: np.ndarray           # float32 [R_d]
+    u_resample: np.ndarray         # float32 [R_t]
+    u_draft: np.ndarray            # float32 [R_d]
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def k(self) -> np.ndarray:
+        return np.diff(self.k_offsets)
+
+    @property
+    def rows_target(self) -> int:
+        return int(self.k_offsets[-1]) + self.B
+
+    @property
+    def rows_draft(self) -> int:
+        return int(self.k_offsets[-1])
+
+    @property
+    def elem_bytes(self) -> int:
+        return 4 if self.dtype == F32 else 2
+
+
+def round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns, round to nearest even (finite inputs)."""
+    bits = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (bits >> np.uint32(16)) & np.uint32(1)
+    rounded = bits + np.uint32(0x7FFF) + lsb
+    return (rounded >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> fp32 values (exact)."""
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def uniforms(rng: np.random.Generator, n: int) -> np.ndarray:
+    """n fp32 uniforms in [0, 1), each an exact multiple of 2^-24."""
+    return (rng.integers(0, 1 << 24, size=n, dtype=np.int64).astype(np.float64)
+            * (1.0 / (1 << 24))).astype(np.float32)
+
+
+def _coprime_multipliers(rng: np.random.Generator, V: int, n: int) -> np.ndarray:
+    out = np.empty(n, dtype=np.int64)
+    filled = 0
+    while filled < n:
+        cand = rng.integers(1, max(V, 2), size=2 * (n - filled) + 8, dtype=np.int64)
+        ok = cand[np.gcd(cand, V) == 1]
+        take = min(len(ok), n - filled)
+        out[filled:filled + take] = ok[:take]
+        filled += take
+    return out
+
+
+def _zipf_noise_rows(rng: np.random.Generator, R: int, V: int, a: float,
+                     sigma: float, block: int = 64) -> np.ndarray:
+    """R rows of -a*ln(1+pi(v)) + N(0, sigma^2), fp32."""
+    base = (-a * np.log1p(np.arange(V, dtype=np.float64))).astype(np.float32)
+    mult = _coprime_multipliers(rng, V, R)
+    shift = rng.integers(0, max(V, 1), size=R, dtype=np.int64)
+    out = np.empty((R, V), dtype=np.float32)
+    ar = np.arange(V, dtype=np.int64)
+    for r0 in range(0, R, block):
+        r1 = min(R, r0 + block)
+        idx = (mult[r0:r1, None] * ar[None, :] + shift[r0:r1, None]) % V
+        out[r0:r1] = base[idx]
+        out[r0:r1] += rng.standard_normal((r1 - r0, V), dtype=np.float32) * np.float32(sigma)
+    return out
+
+
+def make_case(B: int, k, V: int, dtype: str = F32, temperature=1.0, a: float = 1.1,
+              sigma_t: float = 1.0, sigma_d=0.5, seed: int = 1234,
+              uniform_seed: int = 0, name: str | None = None) -> Workload:
+    """Build a workload.
+
+    k: int (uniform), a sequence of per-sequence k_b, or "ragged_1_10".
+    temperature: float (all sequences), a sequence, or "odd_greedy" (odd
+      sequences T=0, even sequences T=1).
+    sigma_d: float, or "uniform_0.2_1.5" (one sigma per draft row).
+    """
+    rng = np.random.Generator(np.random.Philox(seed))
+    if isinstance(k, str):
+        assert k == "ragged_1_10"
+        ks = rng.integers(1, 11, size=B, dtype=np.int64)
+    elif np.isscalar(k):
+        ks = np.full(B, int(k), dtype=np.int64)
+    else:
+        ks = np.asarray(k, dtype=np.int64)
+        assert ks.shape == (B,)
+    k_offsets = np.zeros(B + 1, dtype=np.int32)
+    k_offsets[1:] = np.cumsum(ks)
+    R_d = int(k_offsets[-1])
+    R_t = R_d + B
+
+    if isinstance(temperature, str):
+        assert temperature == "odd_greedy"
+        temp = np.where(np.arange(B) % 2 == 1, 0.0, 1.0).astype(np.float32)
+    elif np.isscalar(temperature):
+        temp = np.full(B, float(temperature), dtype=np.float32)
+    else:
+        temp = np.asarray(temperature, dtype=np.float32)
+        assert temp.shape == (B,)
+
+    zt = _zipf_noise_rows(rng, R_t, V, a, sigma_t)
+    # target row paired with draft row d of sequence b is d + b
+    seq_of_draft = np.repeat(np.arange(B, dtype=np.int64), ks)
+    pair_row = np.arange(R_d, dtype=np.int64) + seq_of_draft
+    if isinstance(sigma_d, str):
+        assert sigma_d == "uniform_0.2_1.5"
+        sig = rng.uniform(0.2, 1.5, size=R_d).astype(np.float32)
+    else:
+        sig = np.full(R_d, float(sigma_d), dtype=np.float32)
+    zd = np.empty((R_d, V), dtype=np.float32)
+    block = 64
+    for r0 in range(0, R_d, block):
+        r1 = min(R_d, r0 + block)
+        zd[r0:r1] = zt[pair_row[r0:r1]]
+        zd[r0:r1] += rng.standard_normal((r1 - r0, V), dtype=np.float32) * sig[r0:r1, None]
+
+    if dtype == BF16:
+        zt = round_to_bf16_bits(zt)
+        zd = round_to_bf16_bits(zd)
+    else:
+        assert dtype == F32
+
+    urng = np.random.Generator(np.random.Philox(uniform_seed))
+    u_accept = uniforms(urng, R_d)
+    u_resample = uniforms(urng, R_t)
+    u_draft = uniforms(urng, R_d)
+    return Workload(name=name or f"B{B}_V{V}_{dtype}", B=B, V=V, dtype=dtype,
+                    k_offsets=k_offsets, temperature=temp, target_logits=zt,
+                    draft_logits=zd, u_accept=u_accept, u_resample=u_resample,
+                    u_draft=u_draft,
+                    meta=dict(a=a, sigma_t=sigma_t, sigma_d=sigma_d, seed=seed,
+                              uniform_seed=uniform_seed))
+
+
+def make_config(cfg: int) -> Workload:
+    """Workload number cfg (1..5) with its fixed seeds (logits: 1000+cfg,
+    uniforms: 0)."""
+    c = CONFIGS[cfg]
+    return make_case(B=c["B"], k=c["k"], V=c["V"], dtype=c["dtype"],
+                     temperature=c["temperature"], a=c["a"], sigma_t=c["sigma_t"],
+                     sigma_d=c["sigma_d"], seed=1000 + cfg, uniform_seed=0,
+                     name=c["name"])
+
+
+def algorithmic_bytes(w: Workload, n_sampled: int | None = None) -> dict:
+    """Bytes the verify step must move at minimum, by the accounting rule:
+    every needed logit row read once (target rows; draft rows of sampled
+    sequences only) plus one row-equivalent per sampled sequence for the
+    resample.  Also the draft-sampling pass (every draft row once)."""
+    s = w.elem_bytes
+    sampled = w.temperature > 0
+    ks = w.k
+    rows_needed = w.rows_target + int(ks[sampled].sum())
+    n_s = int(sampled.sum()) if n_sampled is None else n_sampled
+    small = (w.B + 1) * 4 + w.B * 4 + w.rows_draft * 4 * 2 + w.rows_target * 4 * 2 + w.B * 4
+    verify = s * w.V * (rows_needed + n_s) + small
+    draft = s * w.V * w.rows_draft + w.rows_draft * 4 * 2 + (w.B + 1) * 4 + w.B * 4
+    return dict(verify=int(verify), draft_sample=int(draft),
+                rows_verified=int(w.rows_target + w.rows_draft),
+                rows_needed=int(rows_needed), sampled_sequences=n_s)
+
+
+def seq_rows(w: Workload, b: int):
+    """(target row range, draft row range) of sequence b."""
+    k0, k1 = int(w.k_offsets[b]), int(w.k_offsets[b + 1])
+    return range(k0 + b, k1 + b + 1), range(k0, k1)
