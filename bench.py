@@ -1,0 +1,386 @@
+#!/usr/bin/env python
+"""Benchmark of the speculative-decoding sampling round on one GB300.
+
+One step = spec_draft_sample (draft-side softmax + multinomial over every
+draft row) + spec_verify (softmax of every target/draft row, accept test,
+first rejection, residual or bonus draw) on the ragged adaptive-k batch
+(B = 512 sequences, k_b uniform in 1..10, V = 128256, bf16 logits, T = 1).
+Inputs are resident in HBM and larger than L2 (no flush needed).
+
+metric: verified logit rows/s (R_t + R_d rows per step) and achieved HBM
+GB/s of algorithmic bytes (every needed row once, plus one row-equivalent
+per sampled sequence for the resample, plus the draft-sampling pass).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the batch (the
+path shards by sequence with no collective: weak scaling); timing is the
+max over ranks.  --impl reference times the fp64 CPU oracle on the host
+cores (rank 0 only) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified logit rows/sec and achieved HBM GB/s (fraction of 8 TB/s), 1xGB300"
+UNIT = "rows/s"
+MAIN_CONFIG = 5
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=MAIN_CONFIG)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--extra-configs", default="3,4",
+                    help="other workloads measured kernel-only (comma list, '' for none)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, enabled: bool = True):
+        self.enabled = enabled
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        if not self.enabled:
+            return self
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.enabled or self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def to_device(w, torch, dev):
+    import numpy as np
+
+    def t(a):
+        x = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            x = x.view(torch.bfloat16)
+        return x.to(dev)
+    return dict(tl=t(w.target_logits), dl=t(w.draft_logits), ua=t(w.u_accept), ur=t(w.u_resample),
+                ud=t(w.u_draft), T=t(w.temperature), ko=t(w.k_offsets))
+
+
+def measure(w, steps, warmup, torch, sv, dev, sampler=None, barrier=None):
+    """Device-resident timing of draft sample + verify with CUDA events on
+    the launching stream.  Returns per-step, per-call times (ms)."""
+    d = to_device(w, torch, dev)
+    toks = torch.empty(w.rows_draft, dtype=torch.int32, device=dev)
+    out_t = torch.empty(w.rows_target, dtype=torch.int32, device=dev)
+    out_n = torch.empty(w.B, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        sv.spec_draft_sample(d["dl"], d["T"], d["ud"], d["ko"], out_draft_tokens=toks)
+        sv.spec_verify(d["tl"], d["dl"], toks, d["ua"], d["ur"], d["T"], d["ko"], out_tokens=out_t,
+                       out_num_accepted=out_n)
+
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    ctx = sampler if sampler is not None else _Null()
+    with ctx:
+        t0.record(stream)
+        for i in range(steps):
+            e = ev[i]
+            e[0].record(stream)
+            sv.spec_draft_sample(d["dl"], d["T"], d["ud"], d["ko"], out_draft_tokens=toks)
+            e[1].record(stream)
+            sv.spec_verify(d["tl"], d["dl"], toks, d["ua"], d["ur"], d["T"], d["ko"], out_tokens=out_t,
+                           out_num_accepted=out_n)
+            e[2].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    total = t0.elapsed_time(t1)
+    draft = [e[0].elapsed_time(e[1]) for e in ev]
+    ver = [e[1].elapsed_time(e[2]) for e in ev]
+    n_acc = out_n.float().mean().item()
+    del d
+    return dict(step_ms=total / steps, draft_ms=statistics.mean(draft), verify_ms=statistics.mean(ver),
+                verify_ms_median=statistics.median(ver), mean_accepted=n_acc)
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def e2e(w, steps, torch, sv):
+    """Through the public host-buffer entry point: H2D of the step's inputs
+    from pinned memory, draft sample + verify, D2H of the results."""
+    import numpy as np
+
+    def h(a):
+        x = torch.from_numpy(np.ascontiguousarray(a))
+        return (x.view(torch.bfloat16) if a.dtype == np.uint16 else x).pin_memory()
+    hs = dict(tl=h(w.target_logits), dl=h(w.draft_logits), ud=h(w.u_draft), ua=h(w.u_accept),
+              ur=h(w.u_resample), T=h(w.temperature), ko=h(w.k_offsets))
+    outs = (torch.empty(w.rows_draft, dtype=torch.int32).pin_memory(),
+            torch.empty(w.rows_target, dtype=torch.int32).pin_memory(),
+            torch.empty(w.B, dtype=torch.int32).pin_memory())
+
+    def call():
+        sv.spec_round_host(hs["tl"], hs["dl"], hs["ud"], hs["ua"], hs["ur"], hs["T"], hs["ko"],
+                           out_draft_tokens=outs[0], out_tokens=outs[1], out_num_accepted=outs[2])
+    call()
+    call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        call()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    h2d = sum(v.numel() * v.element_size() for v in hs.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs)
+    return ms, h2d, d2h
+
+
+def cpu_baseline(w, seconds, nthreads):
+    """The oracle as it stands, on host cores, on the first n sequences of
+    the workload (n sized for about `seconds` of CPU time)."""
+    import oracle
+    import workloads
+
+    def sub(n):
+        ko = w.k_offsets[:n + 1].copy()
+        R_d, R_t = int(ko[-1]), int(ko[-1]) + n
+        return workloads.Workload(name=w.name, B=n, V=w.V, dtype=w.dtype, k_offsets=ko,
+                                  temperature=w.temperature[:n].copy(),
+                                  target_logits=w.target_logits[:R_t], draft_logits=w.draft_logits[:R_d],
+                                  u_accept=w.u_accept[:R_d], u_resample=w.u_resample[:R_t],
+                                  u_draft=w.u_draft[:R_d])
+
+    def run(s):
+        t = time.perf_counter()
+        ds = oracle.draft_sample(s.draft_logits, s.temperature, s.u_draft, s.k_offsets, nthreads=nthreads)
+        oracle.verify(s.target_logits, s.draft_logits, ds.tokens, s.u_accept, s.u_resample, s.temperature,
+                      s.k_offsets, nthreads=nthreads)
+        return time.perf_counter() - t
+
+    n = min(w.B, max(nthreads, 4))
+    t = run(sub(n))
+    n = int(min(w.B, max(1, n * seconds / max(t, 1e-3))))
+    s = sub(n)
+    t = run(s)
+    rows = s.rows_target + s.rows_draft
+    return dict(value=rows / t, unit=UNIT, cores=nthreads, kind="oracle",
+                sample=f"first {n} of {w.B} sequences of {w.name} ({rows} rows), draft sample + verify, "
+                       f"fp64 C oracle, OpenMP over sequences, {t:.1f} s")
+
+
+# ------------------------------------------------------------------ main
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    import workloads
+    w = workloads.make_config(args.config)
+    nthreads = oracle.cores()
+    per_step = max(1.0, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(w, per_step / 4, nthreads)
+    vals = [cpu_baseline(w, per_step, nthreads) for _ in range(args.steps)]
+    v = statistics.median(x["value"] for x in vals)
+    rows_step = w.rows_target + w.rows_draft
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * rows_step / v,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded Zipf-like logits)",
+            "config": {"workload": w.name, "B": w.B, "V": w.V, "k": "uniform 1..10", "logits": w.dtype},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+                             "sample": vals[-1]["sample"]},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    import workloads
+    import speculative_decoding_verification_61_gb300 as sv
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(dev))
+        barrier = dist.barrier
+    sv.lib()
+    peak, peak_kind = peaks()
+
+    w = workloads.make_config(args.config)
+    ab = workloads.algorithmic_bytes(w)
+    sampler = ClockSampler(local, enabled=(rank == 0 and not args.no_clocks))
+    m = measure(w, args.steps, args.warmup, torch, sv, dev, sampler=sampler, barrier=barrier)
+    step_ms = m["step_ms"]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    rows = w.rows_target + w.rows_draft
+    value = world * rows / (step_ms * 1e-3)
+    step_bytes = ab["verify"] + ab["draft_sample"]
+    verify_gbs = ab["verify"] / (m["verify_ms"] * 1e-3) / 1e9
+    draft_gbs = ab["draft_sample"] / (m["draft_ms"] * 1e-3) / 1e9
+
+    extra = {}
+    for c in [int(x) for x in args.extra_configs.split(",") if x.strip()] if rank == 0 else []:
+        wc = workloads.make_config(c)
+        abc = workloads.algorithmic_bytes(wc)
+        mc = measure(wc, max(50, args.steps // 4), args.warmup, torch, sv, dev)
+        extra[wc.name] = {
+            "verify_ms": round(mc["verify_ms"], 5), "draft_sample_ms": round(mc["draft_ms"], 5),
+            "verify_rows_per_s": (wc.rows_target + wc.rows_draft) / (mc["verify_ms"] * 1e-3),
+            "verify_gbs": abc["verify"] / (mc["verify_ms"] * 1e-3) / 1e9,
+            "verify_frac_of_8tbs": abc["verify"] / (mc["verify_ms"] * 1e-3) / 8e12,
+            "verify_bytes": abc["verify"], "mean_accepted": mc["mean_accepted"]}
+        del wc
+
+    e2e_line = None
+    if rank == 0 and args.e2e_steps > 0:
+        ms, h2d, d2h = e2e(w, args.e2e_steps, torch, sv)
+        e2e_line = {"value": rows / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": args.e2e_steps,
+                    "api": "spec_round_host (pinned host buffers)"}
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+    import oracle
+    cpu = cpu_baseline(w, args.cpu_seconds, oracle.cores()) if world == 1 or rank == 0 else None
+    clocks = sampler.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Zipf-like logits + Gaussian noise)",
+        "config": {"workload": w.name, "B": w.B, "V": w.V, "k": "uniform 1..10 per sequence",
+                   "temperature": 1.0, "rows_target": w.rows_target, "rows_draft": w.rows_draft,
+                   "step": "spec_draft_sample + spec_verify", "l2": "inputs > L2 (no flush)",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_gbs": step_bytes / (step_ms * 1e-3) / 1e9,
+        "frac_of_8tbs": step_bytes / (step_ms * 1e-3) / 8e12,
+        "bytes_per_step": step_bytes,
+        "kernels": {"spec_verify_ms": m["verify_ms"], "spec_verify_gbs": verify_gbs,
+                    "spec_verify_frac_of_8tbs": verify_gbs / 8000.0,
+                    "spec_draft_sample_ms": m["draft_ms"], "spec_draft_sample_gbs": draft_gbs,
+                    "mean_accepted": m["mean_accepted"]},
+        "roofline": {"bound": "hbm", "kernel": "spec_verify (all its launches)",
+                     "achieved": verify_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": verify_gbs / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": None, "algorithmic_bytes_per_launch": ab["verify"]},
+        "gpu_launches": 6 * args.steps,
+        "cpu_baseline": cpu,
+        "e2e": e2e_line,
+        "clocks": clocks,
+        "other_workloads": extra,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,189 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) speculative-decoding
+ * verify-and-resample library.
+ *
+ * The operation (three web pages on the method, cited by title and section):
+ *   docs.ifdog.com "投机解码", section 投机解码的三步流程 (three-step procedure)
+ *     step 3, and section 动手实践 (speculative_decode: sampling and greedy
+ *     branches);
+ *   bbs.huaweicloud.com "大模型推理无损加速:投机采样(Speculative Decoding)数学原理与
+ *     工业级落地实践", section 二.1 (acceptance probability
+ *     alpha = min(1, p/q)), section 二.2 (residual distribution
+ *     norm(max(0, p - q))), section 三 (speculative_sampling_step);
+ *   sxl-space.tk "【大模型】- 推测解码", section 批量推测解码
+ *     (BatchSpeculativeDecoder: one verify per sequence of a batch).
+ *
+ * For each of B sequences with k_b drafted tokens x_0..x_{k_b-1}:
+ *   (a) temperature-scaled softmax of every target row (k_b + 1 of them) and
+ *       every draft row (k_b), p_i = softmax(z_t,i / T_b), q_i = softmax(z_d,i / T_b);
+ *   (b) alpha_i = min(1, p_i(x_i) / q_i(x_i)); x_i is accepted iff
+ *       u_accept_i < alpha_i; n_b = index of the first rejection (k_b if none);
+ *   (c) if n_b < k_b: one token drawn from norm(max(0, p_j - q_j)) at j = n_b
+ *       by inverse CDF (smallest v with C_v > u * Z, ascending vocabulary
+ *       order, u = u_resample at position j); else the bonus token drawn from
+ *       p_{k_b} the same way;
+ *   (d) T_b = 0 (greedy): accept while x_i == argmax p_i (lowest index on
+ *       ties); the first mismatch emits argmax p_i, full acceptance emits
+ *       argmax p_{k_b}.
+ *
+ * Common conventions for every entry point below
+ *   - Pointers are DEVICE pointers unless the name ends in _host.  The
+ *     caller owns every buffer; the library keeps no pointer after a call.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  The return value reports only what the host can
+ *     check: argument errors and launch failures.
+ *   - Layout, with R_d = k_offsets[B] and R_t = R_d + B (k_offsets is read
+ *     on the device, so the host never needs R_d):
+ *       k_offsets     int32 [B+1]   k_offsets[0] = 0, 0 <= k_b <= SPEC_MAX_K
+ *       target_logits [R_t, V]      row-major; sequence b owns rows
+ *                                   o_b .. o_b + k_b with o_b = k_offsets[b] + b
+ *                                   (row o_b + i predicts draft position i,
+ *                                   row o_b + k_b is the bonus position)
+ *       draft_logits  [R_d, V]      sequence b owns rows k_offsets[b] .. +k_b-1
+ *       draft_tokens  int32 [R_d]
+ *       u_accept      float [R_d]   in [0,1); position i of b uses u_accept[k_offsets[b]+i]
+ *       u_resample    float [R_t]   in [0,1); the resample/bonus at position j
+ *                                   uses u_resample[o_b + j]; unused ones are ignored
+ *       temperature   float [B]     0 = greedy, > 0 sampled
+ *       out_tokens    int32 [R_t]   slots o_b .. o_b + k_b: the n_b accepted
+ *                                   tokens, the resampled/bonus token, then -1
+ *       out_num_accepted int32 [B]  n_b, or -1 for a data error in sequence b
+ *   - dtype: SPEC_F32 or SPEC_BF16, for both logit tensors.  Both logit
+ *     pointers must be 16-byte aligned and V * sizeof(element) a multiple of
+ *     16 (V % 4 == 0 for fp32, V % 8 == 0 for bf16); otherwise
+ *     SPEC_ERR_ALIGNMENT.
+ *   - Data errors found on the device mark only their sequence
+ *     (out_num_accepted[b] = -1, its token slots -1): a draft token outside
+ *     [0, V), a temperature < 0 / NaN / inf, a needed logit row holding NaN
+ *     or +inf or entirely -inf (a greedy row: holding NaN).  An invalid
+ *     k_offsets array (k_offsets[0] != 0, or some k_b outside
+ *     [0, SPEC_MAX_K]) fails the whole call on the device: every
+ *     out_num_accepted = -1, out_tokens untouched, and the workspace status
+ *     word set to SPEC_ERR_INVALID_ARG.
+ *   - Temperature: every row of sequence b, target and draft, is divided by
+ *     T_b before the softmax.
+ *   - Randomness is never drawn inside the library: all uniforms are inputs,
+ *     so results are reproducible bit for bit.
+ *   - Workspace: the entry points without a workspace argument use one
+ *     library-owned device workspace per GPU, allocated (cudaMalloc,
+ *     synchronous) on the first call that needs a larger one; that first
+ *     call therefore must not happen during stream capture.  Concurrent
+ *     calls that share a workspace (the library-owned one included) must be
+ *     ordered on one stream; calls on independent streams need their own
+ *     workspace through the *_ex entry points.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPEC_VERIFY_ABI_VERSION 1
+#define SPEC_MAX_K 32        /* drafted positions per sequence */
+#define SPEC_MAX_B 4096      /* sequences per call */
+#define SPEC_MAX_V (1 << 24) /* vocabulary size */
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = -1,  /* null pointer, B/V/dtype out of range, bad k_offsets (device) */
+    SPEC_ERR_ALIGNMENT = -2,    /* logit pointer or row stride not 16-byte aligned */
+    SPEC_ERR_CUDA = -3,         /* a CUDA call failed (launch, allocation, copy) */
+    SPEC_ERR_TIMEOUT = -4,      /* a bounded device-side wait gave up (device status only) */
+    SPEC_ERR_WORKSPACE = -5     /* caller workspace smaller than spec_workspace_bytes() */
+} spec_status_t;
+
+/* Optional parity/diagnostic outputs of spec_verify_ex; any field may be NULL.
+ * Values are undefined (NaN) where the quantity does not exist. */
+typedef struct {
+    float *accept_prob;   /* [R_d] alpha_i of every drafted position of a sampled sequence */
+    float *residual_mass; /* [B]  Z = sum max(0, p_j - q_j) at the resampled position */
+    float *lse_target;    /* [R_t] log-sum-exp of z/T (natural log) per target row */
+    float *lse_draft;     /* [R_d] log-sum-exp of z/T per draft row */
+} spec_verify_aux_t;
+
+/*
+ * Verify-and-resample for B sequences (operations (a)-(d) above).
+ * Returns SPEC_OK, or an error code for host-detectable argument errors
+ * (nothing is launched then).  B = 0 is a valid no-op.
+ */
+int spec_verify(const void *target_logits, const void *draft_logits,
+                const int32_t *draft_tokens, const float *u_accept,
+                const float *u_resample, const float *temperature, int B,
+                const int32_t *k_offsets, int V, int dtype, int32_t *out_tokens,
+                int32_t *out_num_accepted, void *stream);
+
+/*
+ * spec_verify with optional aux outputs and a caller-owned device workspace
+ * of at least spec_workspace_bytes(B, V, dtype) bytes (256-byte aligned).
+ * workspace == NULL selects the library-owned one.  The workspace needs no
+ * initialisation beyond being zero-filled once before its first use.
+ */
+int spec_verify_ex(const void *target_logits, const void *draft_logits,
+                   const int32_t *draft_tokens, const float *u_accept,
+                   const float *u_resample, const float *temperature, int B,
+                   const int32_t *k_offsets, int V, int dtype, int32_t *out_tokens,
+                   int32_t *out_num_accepted, const spec_verify_aux_t *aux,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Draft-side softmax + multinomial (docs.ifdog.com "投机解码", section 动手实践,
+ * drafting loop; sxl-space.tk "【大模型】- 推测解码", draft_generate): for every
+ * draft row r of sequence b, out_draft_tokens[r] = argmax z (lowest index)
+ * if T_b = 0, else the inverse-CDF draw from softmax(z / T_b) at u_draft[r].
+ * A row with NaN (or, when sampled, +inf / entirely -inf) or a bad T_b
+ * gives -1.  draft_logits [R_d, V], u_draft float [R_d], out int32 [R_d].
+ */
+int spec_draft_sample(const void *draft_logits, const float *temperature,
+                      const float *u_draft, int B, const int32_t *k_offsets, int V,
+                      int dtype, int32_t *out_draft_tokens, void *stream);
+
+int spec_draft_sample_ex(const void *draft_logits, const float *temperature,
+                         const float *u_draft, int B, const int32_t *k_offsets, int V,
+                         int dtype, int32_t *out_draft_tokens, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/*
+ * One sampling round from HOST memory: copies the inputs to the device,
+ * runs spec_draft_sample (which fills the draft tokens) and then
+ * spec_verify, copies the draft tokens and the verify outputs back, and
+ * returns after the stream has finished.  All pointers are host pointers
+ * (pinned memory gives full copy bandwidth); k_offsets [B+1] is read on the
+ * host to size the copies.  Uses a library-owned device staging area that
+ * grows on demand (synchronous cudaMalloc).
+ */
+int spec_round_host(const void *target_logits_host, const void *draft_logits_host,
+                    const float *u_draft_host, const float *u_accept_host,
+                    const float *u_resample_host, const float *temperature_host, int B,
+                    const int32_t *k_offsets_host, int V, int dtype,
+                    int32_t *out_draft_tokens_host, int32_t *out_tokens_host,
+                    int32_t *out_num_accepted_host, void *stream);
+
+/* Bytes of device workspace needed by spec_verify_ex / spec_draft_sample_ex
+ * for a call with B sequences over vocabulary V (0 for invalid arguments). */
+size_t spec_workspace_bytes(int B, int V, int dtype);
+
+/*
+ * Device status word of a workspace (NULL: the library-owned one of the
+ * current device): SPEC_OK or the first device-side error (SPEC_ERR_TIMEOUT,
+ * SPEC_ERR_INVALID_ARG) since it was last cleared.  Synchronous (it waits
+ * for the device).  clear != 0 resets it to SPEC_OK.
+ */
+int spec_workspace_status(const void *workspace, int *status_out, int clear);
+
+/* Human-readable name of a status code (static string). */
+const char *spec_status_string(int status);
+
+/* SPEC_VERIFY_ABI_VERSION of the loaded library. */
+int spec_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

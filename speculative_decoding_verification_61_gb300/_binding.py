@@ -1,0 +1,227 @@
+"""ctypes marshalling for libspecverify.so (argument marshalling only)."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(PKG, "_build", "libspecverify.so")
+
+F32, BF16 = 0, 1
+MAX_K, MAX_B, MAX_V = 32, 4096, 1 << 24
+ABI_VERSION = 1
+SPEC_ERRORS = {0: "SPEC_OK", -1: "SPEC_ERR_INVALID_ARG", -2: "SPEC_ERR_ALIGNMENT",
+               -3: "SPEC_ERR_CUDA", -4: "SPEC_ERR_TIMEOUT", -5: "SPEC_ERR_WORKSPACE"}
+
+# every symbol include/spec_verify.h declares
+EXPORTS = ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",
+           "spec_round_host", "spec_workspace_bytes", "spec_workspace_status",
+           "spec_status_string", "spec_abi_version")
+
+
+class SpecError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {SPEC_ERRORS.get(code, code)}")
+        self.code = code
+
+
+class _Aux(ctypes.Structure):
+    _fields_ = [("accept_prob", ctypes.c_void_p), ("residual_mass", ctypes.c_void_p),
+                ("lse_target", ctypes.c_void_p), ("lse_draft", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"CUDA library not built: {_LIB_PATH} is missing "
+                           "(run __graft_entry__.build() or python -m "
+                           "speculative_decoding_verification_61_gb300.build)")
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, ip, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.spec_verify.argtypes = [vp, vp, vp, vp, vp, vp, ip, vp, ip, ip, vp, vp, vp]
+    L.spec_verify_ex.argtypes = [vp, vp, vp, vp, vp, vp, ip, vp, ip, ip, vp, vp,
+                                 ctypes.POINTER(_Aux), vp, sz, vp]
+    L.spec_draft_sample.argtypes = [vp, vp, vp, ip, vp, ip, ip, vp, vp]
+    L.spec_draft_sample_ex.argtypes = [vp, vp, vp, ip, vp, ip, ip, vp, vp, sz, vp]
+    L.spec_round_host.argtypes = [vp, vp, vp, vp, vp, vp, ip, vp, ip, ip, vp, vp, vp, vp]
+    L.spec_workspace_bytes.argtypes = [ip, ip, ip]
+    L.spec_workspace_bytes.restype = sz
+    L.spec_workspace_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int), ip]
+    L.spec_status_string.argtypes = [ip]
+    L.spec_status_string.restype = ctypes.c_char_p
+    L.spec_abi_version.argtypes = []
+    for name in ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",
+                 "spec_round_host", "spec_workspace_status", "spec_abi_version"):
+        getattr(L, name).restype = ip
+    _lib = L
+    return L
+
+
+def exported_symbols():
+    L = lib()
+    return {name: hasattr(L, name) for name in EXPORTS}
+
+
+# ----------------------------------------------------------------- helpers
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_dev(name, t, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _raise(rc, what):
+    if rc != 0:
+        raise SpecError(rc, what)
+
+
+# ----------------------------------------------------------------- API
+def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_resample,
+                temperature, k_offsets, out_tokens=None, out_num_accepted=None,
+                aux: bool = False, workspace=None, stream=None):
+    """Verify-and-resample (device tensors).  Returns (out_tokens [R_t] int32,
+    out_num_accepted [B] int32) and, with aux=True, a dict of accept_prob,
+    residual_mass, lse_target, lse_draft (float32)."""
+    import torch
+    B = temperature.numel()
+    V = target_logits.shape[-1]
+    dt = _dtype_code(target_logits)
+    for name, t in (("target_logits", target_logits), ("draft_logits", draft_logits)):
+        _check_dev(name, t, target_logits.dtype)
+    _check_dev("draft_tokens", draft_tokens, torch.int32)
+    _check_dev("u_accept", u_accept, torch.float32)
+    _check_dev("u_resample", u_resample, torch.float32)
+    _check_dev("temperature", temperature, torch.float32)
+    _check_dev("k_offsets", k_offsets, torch.int32)
+    if k_offsets.numel() != B + 1:
+        raise ValueError("k_offsets must have B + 1 entries")
+    R_t = u_resample.numel()
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty(R_t, dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    L = lib()
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_p(workspace), workspace.numel() * workspace.element_size())
+    ax = None
+    aux_out = None
+    if aux:
+        R_d = draft_tokens.numel()
+        aux_out = dict(accept_prob=torch.full((R_d,), float("nan"), device=dev),
+                       residual_mass=torch.full((B,), float("nan"), device=dev),
+                       lse_target=torch.full((R_t,), float("nan"), device=dev),
+                       lse_draft=torch.full((R_d,), float("nan"), device=dev))
+        ax = _Aux(*(ctypes.c_void_p(aux_out[k].data_ptr()) for k in
+                    ("accept_prob", "residual_mass", "lse_target", "lse_draft")))
+    if ax is None and workspace is None:
+        rc = L.spec_verify(_p(target_logits), _p(draft_logits), _p(draft_tokens), _p(u_accept),
+                           _p(u_resample), _p(temperature), B, _p(k_offsets), V, dt,
+                           _p(out_tokens), _p(out_num_accepted), _stream(stream))
+    else:
+        rc = L.spec_verify_ex(_p(target_logits), _p(draft_logits), _p(draft_tokens), _p(u_accept),
+                              _p(u_resample), _p(temperature), B, _p(k_offsets), V, dt,
+                              _p(out_tokens), _p(out_num_accepted),
+                              ctypes.byref(ax) if ax is not None else None, ws_ptr, ws_bytes,
+                              _stream(stream))
+    _raise(rc, "spec_verify")
+    if aux:
+        return out_tokens, out_num_accepted, aux_out
+    return out_tokens, out_num_accepted
+
+
+def spec_draft_sample(draft_logits, temperature, u_draft, k_offsets, out_draft_tokens=None,
+                      workspace=None, stream=None):
+    """Draft-side softmax + multinomial (argmax for T = 0).  Returns int32 [R_d]."""
+    import torch
+    B = temperature.numel()
+    V = draft_logits.shape[-1]
+    dt = _dtype_code(draft_logits)
+    _check_dev("draft_logits", draft_logits)
+    _check_dev("temperature", temperature, torch.float32)
+    _check_dev("u_draft", u_draft, torch.float32)
+    _check_dev("k_offsets", k_offsets, torch.int32)
+    if out_draft_tokens is None:
+        out_draft_tokens = torch.empty(u_draft.numel(), dtype=torch.int32, device=draft_logits.device)
+    L = lib()
+    if workspace is None:
+        rc = L.spec_draft_sample(_p(draft_logits), _p(temperature), _p(u_draft), B, _p(k_offsets), V,
+                                 dt, _p(out_draft_tokens), _stream(stream))
+    else:
+        rc = L.spec_draft_sample_ex(_p(draft_logits), _p(temperature), _p(u_draft), B, _p(k_offsets),
+                                    V, dt, _p(out_draft_tokens), _p(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream))
+    _raise(rc, "spec_draft_sample")
+    return out_draft_tokens
+
+
+def spec_round_host(target_logits, draft_logits, u_draft, u_accept, u_resample, temperature,
+                    k_offsets, out_draft_tokens=None, out_tokens=None, out_num_accepted=None,
+                    stream=None):
+    """One sampling round from host (CPU, ideally pinned) tensors: draft
+    sampling then verify on the GPU, results copied back to host tensors."""
+    import torch
+    B = temperature.numel()
+    V = target_logits.shape[-1]
+    dt = _dtype_code(target_logits)
+    for name, t in (("target_logits", target_logits), ("draft_logits", draft_logits),
+                    ("u_draft", u_draft), ("u_accept", u_accept), ("u_resample", u_resample),
+                    ("temperature", temperature), ("k_offsets", k_offsets)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    R_d, R_t = u_accept.numel(), u_resample.numel()
+    if out_draft_tokens is None:
+        out_draft_tokens = torch.empty(R_d, dtype=torch.int32)
+    if out_tokens is None:
+        out_tokens = torch.empty(R_t, dtype=torch.int32)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty(B, dtype=torch.int32)
+    rc = lib().spec_round_host(_p(target_logits), _p(draft_logits), _p(u_draft), _p(u_accept),
+                               _p(u_resample), _p(temperature), B, _p(k_offsets), V, dt,
+                               _p(out_draft_tokens), _p(out_tokens), _p(out_num_accepted),
+                               _stream(stream))
+    _raise(rc, "spec_round_host")
+    return out_draft_tokens, out_tokens, out_num_accepted
+
+
+def workspace_bytes(B: int, V: int, dtype: int) -> int:
+    return int(lib().spec_workspace_bytes(B, V, dtype))
+
+
+def workspace_status(workspace=None, clear: bool = False) -> int:
+    """Device status word of a workspace tensor (None: the library-owned one)."""
+    v = ctypes.c_int(0)
+    rc = lib().spec_workspace_status(None if workspace is None else _p(workspace), ctypes.byref(v),
+                                     1 if clear else 0)
+    _raise(rc, "spec_workspace_status")
+    return v.value

@@ -1,0 +1,237 @@
+// device_utils.cuh -- sm_103a building blocks for the verify kernels:
+// mbarrier + 1-D bulk-copy (TMA engine) staging, bounded waits, the MUFU
+// base-2 exponential, and element traits for fp32 / bf16 logit rows.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "spec_verify.h"
+
+namespace specv {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr double kLog2eD = 1.4426950408889634073599246810019;
+constexpr double kLn2D = 0.69314718055994530941723212145818;
+constexpr int kMaxK = SPEC_MAX_K;
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+// Make initialised barriers visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of `bar` with the given parity to complete, giving up
+// after ~2 s of wall time.  Returns false on time-out.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// 1-D bulk copy global -> shared (TMA engine, no tensor map), completing
+// `bytes` of transaction count on `bar`.  dst, src 16-B aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(smem_u32(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Hardware base-2 exponential (MUFU.EX2): ~2 ulp, subnormal results flushed
+// to zero, ex2(-inf) = 0, ex2(NaN) = NaN.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// NaN-propagating max.
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ void set_status(int *status, int code) {
+    atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------- elements
+template <int DT>
+struct Elem;
+
+template <>
+struct Elem<SPEC_F32> {
+    static constexpr int kBytes = 4;
+    static constexpr int kPerVec = 4;  // elements per 16-byte vector
+    __device__ static __forceinline__ void unpack(const uint4 &v, float (&x)[4]) {
+        x[0] = __uint_as_float(v.x);
+        x[1] = __uint_as_float(v.y);
+        x[2] = __uint_as_float(v.z);
+        x[3] = __uint_as_float(v.w);
+    }
+    __device__ static __forceinline__ float vmax_nan(const uint4 &v) {
+        return fmax_nan(fmax_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                        fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+    }
+    __device__ static __forceinline__ float load1(const void *base, int64_t idx) {
+        return __ldg(reinterpret_cast<const float *>(base) + idx);
+    }
+};
+
+template <>
+struct Elem<SPEC_BF16> {
+    static constexpr int kBytes = 2;
+    static constexpr int kPerVec = 8;
+    __device__ static __forceinline__ void unpack(const uint4 &v, float (&x)[8]) {
+        x[0] = __uint_as_float(v.x << 16);
+        x[1] = __uint_as_float(v.x & 0xffff0000u);
+        x[2] = __uint_as_float(v.y << 16);
+        x[3] = __uint_as_float(v.y & 0xffff0000u);
+        x[4] = __uint_as_float(v.z << 16);
+        x[5] = __uint_as_float(v.z & 0xffff0000u);
+        x[6] = __uint_as_float(v.w << 16);
+        x[7] = __uint_as_float(v.w & 0xffff0000u);
+    }
+    __device__ static __forceinline__ float vmax_nan(const uint4 &v) {
+        // packed bf16x2 NaN-propagating max, then the two halves
+        __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&v.x);
+        __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&v.y);
+        __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162 *>(&v.z);
+        __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162 *>(&v.w);
+        __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+        uint32_t u = *reinterpret_cast<uint32_t *>(&m);
+        return fmax_nan(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+    }
+    __device__ static __forceinline__ float load1(const void *base, int64_t idx) {
+        const unsigned short h = __ldg(reinterpret_cast<const unsigned short *>(base) + idx);
+        return __uint_as_float(static_cast<uint32_t>(h) << 16);
+    }
+};
+
+// ---------------------------------------------------------------- partials
+// Online-softmax partial over a chunk: s = sum 2^(x*c - m).  NaN in s marks
+// an invalid row (NaN / +inf logit).  m = -inf, s = 0 means no mass.
+struct SoftPart {
+    float m, s;
+};
+
+__device__ __forceinline__ SoftPart soft_merge(SoftPart a, SoftPart b) {
+    if (a.m < b.m) {
+        SoftPart t = a;
+        a = b;
+        b = t;
+    }
+    if (b.m == -INFINITY) {
+        if (b.s != b.s) a.s = b.s;  // keep a NaN marker
+        return a;
+    }
+    a.s = a.s + b.s * ex2(b.m - a.m);
+    return a;
+}
+
+// Arg-max partial: largest value, lowest index among equals; idx = -1 marks
+// a NaN; idx = INT_MAX marks "no element".
+struct ArgPart {
+    float v;
+    int i;
+};
+
+__device__ __forceinline__ ArgPart arg_merge(ArgPart a, ArgPart b) {
+    if (a.i == -1 || b.i == -1) return ArgPart{a.v, -1};
+    if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
+    return a;
+}
+
+__device__ __forceinline__ SoftPart shfl_soft(SoftPart p, int off) {
+    return SoftPart{__shfl_xor_sync(0xffffffffu, p.m, off), __shfl_xor_sync(0xffffffffu, p.s, off)};
+}
+
+__device__ __forceinline__ ArgPart shfl_arg(ArgPart p, int off) {
+    return ArgPart{__shfl_xor_sync(0xffffffffu, p.v, off), __shfl_xor_sync(0xffffffffu, p.i, off)};
+}
+
+__device__ __forceinline__ SoftPart warp_soft(SoftPart p) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) p = soft_merge(p, shfl_soft(p, off));
+    return p;
+}
+
+__device__ __forceinline__ ArgPart warp_arg(ArgPart p) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) p = arg_merge(p, shfl_arg(p, off));
+    return p;
+}
+
+// c = log2(e) / T rounded to fp32 (T > 0), 0 for greedy (T == 0), NaN for an
+// invalid temperature.  Every kernel derives the scale the same way.
+__device__ __forceinline__ float temp_scale(float T) {
+    if (T == 0.0f) return 0.0f;
+    if (!(T > 0.0f) || !isfinite(T)) return __int_as_float(0x7fc00000);
+    const float c = static_cast<float>(kLog2eD / static_cast<double>(T));
+    return isfinite(c) ? c : __int_as_float(0x7fc00000);
+}
+
+// Residual weight max(0, p_v - q_v) with p_v = 2^(z_t*c - Lt), q_v likewise;
+// L is passed as an fp32 hi/lo pair.  Operations are pinned (no contraction
+// choices left to the compiler) so that every kernel computes identical
+// bits for the same inputs.
+__device__ __forceinline__ float resid_weight(float zt, float zd, float c, float lth, float ltl,
+                                              float ldh, float ldl) {
+    const float at = __fsub_rn(__fmaf_rn(zt, c, -lth), ltl);
+    const float ad = __fsub_rn(__fmaf_rn(zd, c, -ldh), ldl);
+    return fmaxf(__fsub_rn(ex2(at), ex2(ad)), 0.0f);
+}
+
+// Target/draft probability weight 2^(z*c - M) relative to the row max M.
+__device__ __forceinline__ float prob_weight(float z, float c, float M) {
+    return ex2(__fmaf_rn(z, c, -M));
+}
+
+}  // namespace specv

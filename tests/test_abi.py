@@ -1,0 +1,85 @@
+"""CPU checks of the C-ABI library: it builds for sm_103a, loads without a
+GPU, exports every symbol include/spec_verify.h declares, and rejects bad
+arguments on the host (no compute call needs a GPU for these)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_61_gb300 import build
+    build.build()
+    import speculative_decoding_verification_61_gb300 as sv
+    return sv.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    for n in ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",
+              "spec_round_host", "spec_workspace_bytes", "spec_workspace_status",
+              "spec_status_string", "spec_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in spec_verify.h but not exported"
+
+
+def test_binding_covers_every_declared_symbol():
+    from speculative_decoding_verification_61_gb300 import _binding
+    assert set(declared_functions()) <= set(_binding.EXPORTS)
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.spec_abi_version() == 1
+    assert lib.spec_status_string(0) == b"SPEC_OK"
+    assert lib.spec_status_string(-2) == b"SPEC_ERR_ALIGNMENT"
+    assert lib.spec_status_string(12345) == b"SPEC_ERR_UNKNOWN"
+
+
+def test_workspace_bytes_host_only(lib):
+    import speculative_decoding_verification_61_gb300 as sv
+    a = sv.workspace_bytes(512, 128256, sv.BF16)
+    b = sv.workspace_bytes(64, 128256, sv.BF16)
+    assert a > b > 0 and a % 256 == 0
+    assert sv.workspace_bytes(4, 1001, sv.BF16) == 0      # V * 2 not a multiple of 16
+    assert sv.workspace_bytes(-1, 1000, sv.F32) == 0
+    assert sv.workspace_bytes(4, 1000, 7) == 0
+    assert sv.workspace_bytes(sv.MAX_B + 1, 1000, sv.F32) == 0
+
+
+def test_host_argument_errors_launch_nothing(lib):
+    """Errors the host can see are returned before any CUDA call."""
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)  # never dereferenced: validation fails first
+    # bad dtype
+    assert lib.spec_verify(fake, fake, fake, fake, fake, fake, 4, fake, 1000, 9, fake, fake, None) == -1
+    # negative B, oversized B
+    assert lib.spec_verify(fake, fake, fake, fake, fake, fake, -1, fake, 1000, 0, fake, fake, None) == -1
+    assert lib.spec_verify(fake, fake, fake, fake, fake, fake, 5000, fake, 1000, 0, fake, fake, None) == -1
+    # V not a multiple of 16 bytes
+    assert lib.spec_verify(fake, fake, fake, fake, fake, fake, 4, fake, 1001, 1, fake, fake, None) == -2
+    # null pointer
+    assert lib.spec_verify(None, fake, fake, fake, fake, fake, 4, fake, 1000, 0, fake, fake, None) == -1
+    # misaligned logits pointer
+    assert lib.spec_verify(vp((1 << 20) + 4), fake, fake, fake, fake, fake, 4, fake, 1000, 0, fake,
+                           fake, None) == -2
+    # B == 0 is a no-op
+    assert lib.spec_verify(None, None, None, None, None, None, 0, None, 1000, 0, None, None, None) == 0
+    assert lib.spec_draft_sample(None, None, None, 0, None, 1000, 0, None, None) == 0
+    assert lib.spec_draft_sample(fake, fake, fake, 4, fake, 1000, 3, fake, None) == -1

@@ -1,0 +1,211 @@
+"""GPU parity of the CUDA path (through the C ABI) against the fp64 oracle,
+on seeded inputs: small cases that span several chunks with ragged tails,
+the five workloads at full size, edge cases and a statistical check."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from parity import FLAG_MARGIN, compare_verify, gpu_draft_sample, gpu_verify, run_and_compare, to_device
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import speculative_decoding_verification_61_gb300 as sv
+    sv.lib()  # raises if the library is missing: no fallback
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_small_workloads_exact(cfg):
+    rep = run_and_compare(workloads.make_config(cfg))
+    assert rep["verify_flagged"] <= 1
+
+
+CASES = [
+    # several chunks with a ragged last chunk, mixed k including 0 and 32
+    dict(B=12, k=[0, 1, 2, 3, 5, 8, 13, 21, 32, 4, 7, 1], V=20000, dtype="bf16", temperature=1.0),
+    dict(B=12, k=[0, 1, 2, 3, 5, 8, 13, 21, 32, 4, 7, 1], V=20000, dtype="f32", temperature=0.8),
+    dict(B=16, k="ragged_1_10", V=40008, dtype="bf16", temperature="odd_greedy",
+         sigma_d="uniform_0.2_1.5"),
+    dict(B=9, k=4, V=8, dtype="f32", temperature=1.0),            # tiny vocabulary
+    dict(B=9, k=3, V=16, dtype="bf16", temperature=0.5),
+    dict(B=5, k=6, V=131072, dtype="bf16", temperature=0.05),      # sharp distributions
+    dict(B=5, k=6, V=65536, dtype="f32", temperature=4.0),         # flat distributions
+    dict(B=40, k=2, V=2056, dtype="bf16", temperature=1.0, sigma_d=3.0),  # low acceptance
+    dict(B=40, k=6, V=3000, dtype="f32", temperature=1.0, sigma_d=0.05),  # high acceptance
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_parity_cases(case):
+    w = workloads.make_case(seed=100 + case, **CASES[case])
+    rep = run_and_compare(w)
+    assert rep["verify_flagged"] <= max(1, w.B // 50)
+
+
+@pytest.mark.parametrize("cfg", [3, 4, 5])
+def test_full_size_workloads(cfg):
+    """The benchmark's workloads at full size, every sequence checked."""
+    w = workloads.make_config(cfg)
+    rep = run_and_compare(w)
+    assert rep["verify_flagged"] <= max(2, w.B // 100), rep
+    assert rep.get("draft_flagged", 0) <= max(2, w.rows_draft // 100), rep
+
+
+def test_repeated_calls_and_caller_workspace():
+    import speculative_decoding_verification_61_gb300 as sv
+    w = workloads.make_case(B=20, k="ragged_1_10", V=24000, dtype="bf16", seed=7,
+                            temperature="odd_greedy")
+    d = to_device(w)
+    toks = gpu_draft_sample(d)
+    a = gpu_verify(d, toks, aux=False)
+    b = gpu_verify(d, toks, aux=False)
+    ws = torch.zeros(sv.workspace_bytes(w.B, w.V, sv.BF16), dtype=torch.uint8, device="cuda")
+    c = sv.spec_verify(d["target_logits"], d["draft_logits"], toks, d["u_accept"], d["u_resample"],
+                       d["temperature"], d["k_offsets"], workspace=ws)
+    c2 = sv.spec_verify(d["target_logits"], d["draft_logits"], toks, d["u_accept"], d["u_resample"],
+                        d["temperature"], d["k_offsets"], workspace=ws)
+    for x in (b, c, c2):
+        assert torch.equal(a[0], x[0]) and torch.equal(a[1], x[1])
+    t2 = sv.spec_draft_sample(d["draft_logits"], d["temperature"], d["u_draft"], d["k_offsets"],
+                              workspace=ws)
+    assert torch.equal(toks, t2)
+    assert sv.workspace_status(ws) == 0 and sv.workspace_status() == 0
+
+
+def test_unused_uniforms_do_not_matter_gpu():
+    w = workloads.make_case(B=32, k=6, V=12000, dtype="bf16", seed=3)
+    d = to_device(w)
+    toks = gpu_draft_sample(d)
+    t0, n0 = gpu_verify(d, toks, aux=False)
+    n0h = n0.cpu().numpy()
+    ua, ur = w.u_accept.copy(), w.u_resample.copy()
+    rng = np.random.default_rng(1)
+    for b in range(w.B):
+        k0, k = int(w.k_offsets[b]), int(w.k[b])
+        n = n0h[b]
+        ua[k0 + n + 1:k0 + k] = rng.random(max(0, k - n - 1)).astype(np.float32)
+        for j in range(k + 1):
+            if j != n:
+                ur[k0 + b + j] = np.float32(rng.random())
+    d["u_accept"] = torch.from_numpy(ua).cuda()
+    d["u_resample"] = torch.from_numpy(ur).cuda()
+    t1, n1 = gpu_verify(d, toks, aux=False)
+    assert torch.equal(t0, t1) and torch.equal(n0, n1)
+
+
+def test_data_errors_mark_only_their_sequence():
+    w = workloads.make_case(B=8, k=3, V=4096, dtype="f32", seed=9, temperature="odd_greedy")
+    tl, dl = w.target_logits.copy(), w.draft_logits.copy()
+    temp = w.temperature.copy()
+    ods = oracle.draft_sample(w.draft_logits, w.temperature, w.u_draft, w.k_offsets)
+    toks = ods.tokens.copy()
+    tl[1 * 4 + 2, 7] = np.nan          # greedy sequence 1: NaN in a target row
+    dl[2 * 3 + 0, 3] = np.inf          # sampled sequence 2: +inf in a draft row
+    toks[4 * 3 + 1] = 4096             # sequence 4: token out of range
+    temp[6] = -1.0                     # sequence 6: bad temperature
+    tl[0 * 4 + 3, :] = -np.inf         # sequence 0: bonus row entirely -inf
+    tl[3 * 4 + 1, 100] = np.inf        # greedy sequence 3: +inf is a valid greedy logit
+    w2 = workloads.Workload(**{**w.__dict__, "target_logits": tl, "draft_logits": dl,
+                               "temperature": temp})
+    d = to_device(w2)
+    gt, gn, ga = gpu_verify(d, torch.from_numpy(toks).cuda(), aux=True)
+    ora = oracle.verify(tl, dl, toks, w.u_accept, w.u_resample, temp, w.k_offsets)
+    gn = gn.cpu().numpy()
+    for b in (0, 1, 2, 4, 6):
+        assert ora.num_accepted[b] == -1 and gn[b] == -1, b
+    assert gn[3] == ora.num_accepted[3] >= 0
+    compare_verify(w2, gt.cpu().numpy(), gn, {k: v.cpu().numpy() for k, v in ga.items()}, ora)
+
+
+def test_invalid_k_offsets_fail_the_call_on_device():
+    import speculative_decoding_verification_61_gb300 as sv
+    w = workloads.make_case(B=4, k=2, V=1000, seed=2)
+    d = to_device(w)
+    bad = w.k_offsets.copy()
+    bad[2] = bad[1] + 40  # k_1 = 40 > 32
+    d["k_offsets"] = torch.from_numpy(bad).cuda()
+    ws = torch.zeros(sv.workspace_bytes(w.B, w.V, sv.F32), dtype=torch.uint8, device="cuda")
+    out_t = torch.full((w.rows_target,), 77, dtype=torch.int32, device="cuda")
+    t, n = sv.spec_verify(d["target_logits"], d["draft_logits"],
+                          torch.zeros(w.rows_draft, dtype=torch.int32, device="cuda"),
+                          d["u_accept"], d["u_resample"], d["temperature"], d["k_offsets"],
+                          out_tokens=out_t, workspace=ws)
+    torch.cuda.synchronize()
+    assert (n.cpu().numpy() == -1).all()
+    assert (out_t.cpu().numpy() == 77).all()  # buffers of unknown size untouched
+    assert sv.workspace_status(ws, clear=True) == -1  # SPEC_ERR_INVALID_ARG
+    assert sv.workspace_status(ws) == 0
+
+
+def test_round_host_matches_device_path():
+    import speculative_decoding_verification_61_gb300 as sv
+    w = workloads.make_case(B=16, k="ragged_1_10", V=16000, dtype="bf16", seed=21)
+    d = to_device(w)
+    toks = gpu_draft_sample(d)
+    t, n = gpu_verify(d, toks, aux=False)
+
+    def h(a):
+        x = torch.from_numpy(np.ascontiguousarray(a))
+        return (x.view(torch.bfloat16) if a.dtype == np.uint16 else x).pin_memory()
+
+    hd, ht, hn = sv.spec_round_host(h(w.target_logits), h(w.draft_logits), h(w.u_draft),
+                                    h(w.u_accept), h(w.u_resample), h(w.temperature),
+                                    h(w.k_offsets))
+    assert torch.equal(hd, toks.cpu()) and torch.equal(ht, t.cpu()) and torch.equal(hn, n.cpu())
+
+
+def test_alignment_errors():
+    import speculative_decoding_verification_61_gb300 as sv
+    w = workloads.make_case(B=2, k=2, V=1000, seed=2)
+    d = to_device(w)
+    toks = torch.zeros(w.rows_draft, dtype=torch.int32, device="cuda")
+    flat = d["target_logits"].reshape(-1)
+    shifted = flat[1:1 + w.rows_target * w.V].reshape(w.rows_target, w.V)  # 4-byte offset
+    with pytest.raises(sv.SpecError) as e:
+        sv.spec_verify(shifted, d["draft_logits"], toks, d["u_accept"], d["u_resample"],
+                       d["temperature"], d["k_offsets"])
+    assert e.value.code == -2
+
+
+def test_statistical_marginal_on_gpu():
+    """2^16 sequences sharing one (p, q) pair, V = 1000: the first emitted
+    token follows p_0 (chi-square), and the acceptance rate of position 0 is
+    1 - Z_0."""
+    from scipy.special import softmax
+    from scipy.stats import chisquare
+    N, V, k = 1 << 16, 1000, 2
+    rng = np.random.default_rng(5)
+    t = (-1.1 * np.log1p(rng.permutation(V)) + rng.standard_normal(V)).astype(np.float32)
+    tr = np.stack([t, np.roll(t, 3), np.roll(t, 7)])
+    dr = (tr[:k] + rng.standard_normal((k, V)) * 0.5).astype(np.float32)
+    urng = np.random.Generator(np.random.Philox(11))
+    w = workloads.Workload(name="shared_pq", B=N, V=V, dtype="f32",
+                           k_offsets=(np.arange(N + 1) * k).astype(np.int32),
+                           temperature=np.ones(N, np.float32),
+                           target_logits=np.tile(tr, (N, 1)), draft_logits=np.tile(dr, (N, 1)),
+                           u_accept=workloads.uniforms(urng, N * k),
+                           u_resample=workloads.uniforms(urng, N * (k + 1)),
+                           u_draft=workloads.uniforms(urng, N * k))
+    d = to_device(w)
+    toks = gpu_draft_sample(d)
+    gt, gn = gpu_verify(d, toks, aux=False)
+    slots = gt.cpu().numpy().reshape(N, k + 1)
+    gn = gn.cpu().numpy()
+    p0, q0 = softmax(tr[0].astype(np.float64)), softmax(dr[0].astype(np.float64))
+    counts = np.bincount(slots[:, 0], minlength=V)
+    e = p0 * N
+    keep = e > 5
+    c2 = np.append(counts[keep], counts[~keep].sum()).astype(np.float64)
+    e2 = np.append(e[keep], e[~keep].sum())
+    _, pval = chisquare(c2, e2 * c2.sum() / e2.sum())
+    assert pval > 1e-4
+    Z0 = np.maximum(0, p0 - q0).sum()
+    assert abs((gn >= 1).mean() - (1 - Z0)) < 5 * np.sqrt(Z0 * (1 - Z0) / N)

@@ -10,19 +10,23 @@ benchmark), fed with the uniforms `u_draft` drawn here.
 Logit recipe (Zipf-like rows with Gaussian noise, the shape the verify step
 sees from a real target/draft pair):
 
-* target row:  z_t[v] = -a * ln(1 + pi(v)) + N(0, sigma_t^2), with pi a fresh
-  permutation of the vocabulary per row.  pi is a random affine permutation
-  pi(v) = (m*v + c) mod V with gcd(m, V) = 1, which is cheap to draw for
-  thousands of 128K-wide rows and keeps each row's multiset of logits exactly
-  Zipf + noise;
+* target row:  z_t[v] = -a * ln(1 + pi_r(v)) + N(0, sigma_t^2), with pi_r a
+  permutation of the vocabulary drawn per row: one random arrangement P of
+  the vocabulary per workload, rotated by a random offset per row,
+  pi_r(v) = P[(v + c_r) mod V].  Each row keeps its multiset of logits
+  exactly Zipf + noise and puts its large logits at different token ids;
+  rotations make 128K-wide rows cheap to draw;
 * draft row i of a sequence: z_d = z_t(target row i of that sequence) +
   N(0, sigma_d^2);
 * bf16 workloads are generated in fp32 and rounded to bf16 here
   (round-to-nearest-even on the fp32 bit pattern), so that both sides read
   identical bits.
 
-Uniforms are fp32 multiples of 2^-24 in [0, 1), drawn from a Philox generator
-in the fixed order u_accept, u_resample, u_draft.
+Random streams: k_b (ragged batches) from the workload seed; then one
+independent PCG64 stream per sequence (SeedSequence spawn), so a sequence's
+logits do not depend on how many threads generate the batch.  Uniforms are
+fp32 multiples of 2^-24 in [0, 1), drawn from a Philox generator in the
+fixed order u_accept, u_resample, u_draft.
 
 Layout (packed, ragged k per sequence):
   k_offsets [B+1] int32, exclusive prefix sum of k_b (k_offsets[0] = 0)
@@ -34,7 +38,8 @@ bf16 arrays are numpy uint16 holding the bf16 bit patterns.
 """
 from __future__ import annotations
 
-import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -113,34 +118,6 @@ def uniforms(rng: np.random.Generator, n: int) -> np.ndarray:
             * (1.0 / (1 << 24))).astype(np.float32)
 
 
-def _coprime_multipliers(rng: np.random.Generator, V: int, n: int) -> np.ndarray:
-    out = np.empty(n, dtype=np.int64)
-    filled = 0
-    while filled < n:
-        cand = rng.integers(1, max(V, 2), size=2 * (n - filled) + 8, dtype=np.int64)
-        ok = cand[np.gcd(cand, V) == 1]
-        take = min(len(ok), n - filled)
-        out[filled:filled + take] = ok[:take]
-        filled += take
-    return out
-
-
-def _zipf_noise_rows(rng: np.random.Generator, R: int, V: int, a: float,
-                     sigma: float, block: int = 64) -> np.ndarray:
-    """R rows of -a*ln(1+pi(v)) + N(0, sigma^2), fp32."""
-    base = (-a * np.log1p(np.arange(V, dtype=np.float64))).astype(np.float32)
-    mult = _coprime_multipliers(rng, V, R)
-    shift = rng.integers(0, max(V, 1), size=R, dtype=np.int64)
-    out = np.empty((R, V), dtype=np.float32)
-    ar = np.arange(V, dtype=np.int64)
-    for r0 in range(0, R, block):
-        r1 = min(R, r0 + block)
-        idx = (mult[r0:r1, None] * ar[None, :] + shift[r0:r1, None]) % V
-        out[r0:r1] = base[idx]
-        out[r0:r1] += rng.standard_normal((r1 - r0, V), dtype=np.float32) * np.float32(sigma)
-    return out
-
-
 def make_case(B: int, k, V: int, dtype: str = F32, temperature=1.0, a: float = 1.1,
               sigma_t: float = 1.0, sigma_d=0.5, seed: int = 1234,
               uniform_seed: int = 0, name: str | None = None) -> Workload:
@@ -151,10 +128,11 @@ def make_case(B: int, k, V: int, dtype: str = F32, temperature=1.0, a: float = 1
       sequences T=0, even sequences T=1).
     sigma_d: float, or "uniform_0.2_1.5" (one sigma per draft row).
     """
-    rng = np.random.Generator(np.random.Philox(seed))
+    ss = np.random.SeedSequence(seed)
+    ss_k, ss_layout, ss_seq = ss.spawn(3)
     if isinstance(k, str):
         assert k == "ragged_1_10"
-        ks = rng.integers(1, 11, size=B, dtype=np.int64)
+        ks = np.random.default_rng(ss_k).integers(1, 11, size=B, dtype=np.int64)
     elif np.isscalar(k):
         ks = np.full(B, int(k), dtype=np.int64)
     else:
@@ -174,27 +152,46 @@ def make_case(B: int, k, V: int, dtype: str = F32, temperature=1.0, a: float = 1
         temp = np.asarray(temperature, dtype=np.float32)
         assert temp.shape == (B,)
 
-    zt = _zipf_noise_rows(rng, R_t, V, a, sigma_t)
-    # target row paired with draft row d of sequence b is d + b
-    seq_of_draft = np.repeat(np.arange(B, dtype=np.int64), ks)
-    pair_row = np.arange(R_d, dtype=np.int64) + seq_of_draft
-    if isinstance(sigma_d, str):
-        assert sigma_d == "uniform_0.2_1.5"
-        sig = rng.uniform(0.2, 1.5, size=R_d).astype(np.float32)
-    else:
-        sig = np.full(R_d, float(sigma_d), dtype=np.float32)
-    zd = np.empty((R_d, V), dtype=np.float32)
-    block = 64
-    for r0 in range(0, R_d, block):
-        r1 = min(R_d, r0 + block)
-        zd[r0:r1] = zt[pair_row[r0:r1]]
-        zd[r0:r1] += rng.standard_normal((r1 - r0, V), dtype=np.float32) * sig[r0:r1, None]
+    base = (-a * np.log1p(np.arange(V, dtype=np.float64))).astype(np.float32)
+    arranged = base[np.random.default_rng(ss_layout).permutation(V)]
+    odt = np.uint16 if dtype == BF16 else np.float32
+    assert dtype in (BF16, F32)
+    zt_out = np.empty((R_t, V), dtype=odt)
+    zd_out = np.empty((R_d, V), dtype=odt)
+    seq_seeds = ss_seq.spawn(B)
 
-    if dtype == BF16:
-        zt = round_to_bf16_bits(zt)
-        zd = round_to_bf16_bits(zd)
+    def store(dst, row):
+        dst[:] = round_to_bf16_bits(row) if dtype == BF16 else row
+
+    def one_sequence(b):
+        rng = np.random.default_rng(seq_seeds[b])
+        k_b = int(ks[b])
+        t0, d0 = int(k_offsets[b]) + b, int(k_offsets[b])
+        shifts = rng.integers(0, V, size=k_b + 1)
+        if isinstance(sigma_d, str):
+            assert sigma_d == "uniform_0.2_1.5"
+            sig = rng.uniform(0.2, 1.5, size=k_b)
+        else:
+            sig = np.full(k_b, float(sigma_d))
+        row = np.empty(V, dtype=np.float32)
+        for i in range(k_b + 1):
+            c = int(shifts[i])
+            row[:V - c] = arranged[c:]
+            row[V - c:] = arranged[:c]
+            row += rng.standard_normal(V, dtype=np.float32) * np.float32(sigma_t)
+            store(zt_out[t0 + i], row)
+            if i < k_b:
+                d = row + rng.standard_normal(V, dtype=np.float32) * np.float32(sig[i])
+                store(zd_out[d0 + i], d)
+
+    workers = max(1, min(32, os.cpu_count() or 1))
+    if B > 1 and workers > 1:
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(one_sequence, range(B)))
     else:
-        assert dtype == F32
+        for b in range(B):
+            one_sequence(b)
+    zt, zd = zt_out, zd_out
 
     urng = np.random.Generator(np.random.Philox(uniform_seed))
     u_accept = uniforms(urng, R_d)
