@@ -182,6 +182,10 @@ const char *spec_status_string(int status);
 /* SPEC_VERIFY_ABI_VERSION of the loaded library. */
 int spec_abi_version(void);
 
+/* Description of the last CUDA failure (the call and the CUDA error name)
+ * seen by the calling thread, or "" if none.  Static per-thread storage. */
+const char *spec_last_error(void);
+
 #ifdef __cplusplus
 }
 #endif

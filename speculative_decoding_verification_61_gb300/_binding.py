@@ -16,7 +16,7 @@ SPEC_ERRORS = {0: "SPEC_OK", -1: "SPEC_ERR_INVALID_ARG", -2: "SPEC_ERR_ALIGNMENT
 # every symbol include/spec_verify.h declares
 EXPORTS = ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",
            "spec_round_host", "spec_workspace_bytes", "spec_workspace_status",
-           "spec_status_string", "spec_abi_version")
+           "spec_status_string", "spec_abi_version", "spec_last_error")
 
 
 class SpecError(RuntimeError):
@@ -60,6 +60,8 @@ def lib():
     L.spec_status_string.argtypes = [ip]
     L.spec_status_string.restype = ctypes.c_char_p
     L.spec_abi_version.argtypes = []
+    L.spec_last_error.argtypes = []
+    L.spec_last_error.restype = ctypes.c_char_p
     for name in ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",
                  "spec_round_host", "spec_workspace_status", "spec_abi_version"):
         getattr(L, name).restype = ip
@@ -103,7 +105,8 @@ def _stream(stream):
 
 def _raise(rc, what):
     if rc != 0:
-        raise SpecError(rc, what)
+        detail = lib().spec_last_error().decode() if rc == -3 else ""
+        raise SpecError(rc, f"{what} [{detail}]" if detail else what)
 
 
 # ----------------------------------------------------------------- API

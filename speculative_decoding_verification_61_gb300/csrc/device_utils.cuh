@@ -91,6 +91,33 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Packed fp32 pair arithmetic (two IEEE fp32 operations per instruction,
+// each rounded to nearest like the scalar forms).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 // NaN-propagating max.
 __device__ __forceinline__ float fmax_nan(float a, float b) {
     float r;
@@ -110,6 +137,7 @@ template <>
 struct Elem<SPEC_F32> {
     static constexpr int kBytes = 4;
     static constexpr int kPerVec = 4;  // elements per 16-byte vector
+    static constexpr int kPairs = 2;   // element pairs per vector
     __device__ static __forceinline__ void unpack(const uint4 &v, float (&x)[4]) {
         x[0] = __uint_as_float(v.x);
         x[1] = __uint_as_float(v.y);
@@ -123,12 +151,26 @@ struct Elem<SPEC_F32> {
     __device__ static __forceinline__ float load1(const void *base, int64_t idx) {
         return __ldg(reinterpret_cast<const float *>(base) + idx);
     }
+    // element pairs of a 16-byte vector
+    __device__ static __forceinline__ float2 pair(const uint4 &v, int p) {
+        return p == 0 ? make_float2(__uint_as_float(v.x), __uint_as_float(v.y))
+                      : make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+    }
+    static constexpr uint32_t kNegInfWord = 0xff800000u;
+    // NaN-propagating max over four vectors
+    __device__ static __forceinline__ float vmax4_nan(const uint4 (&v)[4]) {
+        float m = vmax_nan(v[0]);
+        m = fmax_nan(m, vmax_nan(v[1]));
+        m = fmax_nan(m, vmax_nan(v[2]));
+        return fmax_nan(m, vmax_nan(v[3]));
+    }
 };
 
 template <>
 struct Elem<SPEC_BF16> {
     static constexpr int kBytes = 2;
     static constexpr int kPerVec = 8;
+    static constexpr int kPairs = 4;  // element pairs per vector
     __device__ static __forceinline__ void unpack(const uint4 &v, float (&x)[8]) {
         x[0] = __uint_as_float(v.x << 16);
         x[1] = __uint_as_float(v.x & 0xffff0000u);
@@ -152,6 +194,30 @@ struct Elem<SPEC_BF16> {
     __device__ static __forceinline__ float load1(const void *base, int64_t idx) {
         const unsigned short h = __ldg(reinterpret_cast<const unsigned short *>(base) + idx);
         return __uint_as_float(static_cast<uint32_t>(h) << 16);
+    }
+    __device__ static __forceinline__ float2 word_pair(uint32_t w) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+    // element pairs of a 16-byte vector (p = 0..3: one 32-bit word each)
+    __device__ static __forceinline__ float2 pair(const uint4 &v, int p) {
+        return word_pair(p == 0 ? v.x : p == 1 ? v.y : p == 2 ? v.z : v.w);
+    }
+    static constexpr uint32_t kNegInfWord = 0xff80ff80u;
+    // NaN-propagating max over four vectors: one packed bf16x2 tree over the
+    // 16 words, then the two halves
+    __device__ static __forceinline__ float vmax4_nan(const uint4 (&v)[4]) {
+        __nv_bfloat162 m[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&v[j].x);
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&v[j].y);
+            const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162 *>(&v[j].z);
+            const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162 *>(&v[j].w);
+            m[j] = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+        }
+        const __nv_bfloat162 t = __hmax2_nan(__hmax2_nan(m[0], m[1]), __hmax2_nan(m[2], m[3]));
+        const uint32_t u = *reinterpret_cast<const uint32_t *>(&t);
+        return fmax_nan(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
     }
 };
 

