@@ -164,6 +164,41 @@ int spec_round_host(const void *target_logits_host, const void *draft_logits_hos
                     int32_t *out_draft_tokens_host, int32_t *out_tokens_host,
                     int32_t *out_num_accepted_host, void *stream);
 
+/*
+ * Allocation-free spec_verify (no counterpart on the pages: a deployment
+ * convenience of this library).
+ *
+ * For callers that cannot allocate device memory when they verify: code
+ * running under CUDA stream capture, serving loops that forbid allocation on
+ * the hot path to keep latency predictable, and runtimes whose memory pool
+ * owns all device memory.  Arguments, layout, outputs and data-error
+ * behaviour are those of spec_verify; the caller still provides every input
+ * and output buffer.  The scratch memory the kernels need comes from a
+ * fixed array inside the library (SPEC_NOALLOC_SCRATCH_BYTES, held on every
+ * GPU that loads the library until the process exits), so the call performs
+ * no cudaMalloc, cudaFree or other allocation.
+ *   - A call whose scratch need, spec_workspace_bytes(B, V, dtype), exceeds
+ *     SPEC_NOALLOC_SCRATCH_BYTES is rejected with SPEC_ERR_WORKSPACE before
+ *     anything is launched (spec_last_error() names the sizes).  The limit
+ *     covers, e.g., B = 512 at V = 152064 in bf16.
+ *   - The first call on each device looks up the array's device address
+ *     (once per device, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls share the one array: calls that may overlap on the GPU (on
+ *     different streams without ordering) race and give wrong results.
+ *     Order them on one stream.
+ *   - The array keeps the previous call's contents; the call clears the
+ *     parts that must start at zero.  Device-side status (time-outs) is not
+ *     reported by this entry point; data errors still mark sequences with
+ *     out_num_accepted = -1.
+ */
+#define SPEC_NOALLOC_SCRATCH_BYTES ((size_t)48 << 20)
+int spec_verify_noalloc(const void *target_logits, const void *draft_logits,
+                        const int32_t *draft_tokens, const float *u_accept,
+                        const float *u_resample, const float *temperature, int B,
+                        const int32_t *k_offsets, int V, int dtype, int32_t *out_tokens,
+                        int32_t *out_num_accepted, void *stream);
+
 /* Bytes of device workspace needed by spec_verify_ex / spec_draft_sample_ex
  * for a call with B sequences over vocabulary V (0 for invalid arguments). */
 size_t spec_workspace_bytes(int B, int V, int dtype);

@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     spec_draft_sample,
     spec_round_host,
     spec_verify,
+    spec_verify_noalloc,
     workspace_bytes,
     workspace_status,
 )

@@ -16,7 +16,7 @@ SPEC_ERRORS = {0: "SPEC_OK", -1: "SPEC_ERR_INVALID_ARG", -2: "SPEC_ERR_ALIGNMENT
 # every symbol include/spec_verify.h declares
 EXPORTS = ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",
            "spec_round_host", "spec_workspace_bytes", "spec_workspace_status",
-           "spec_status_string", "spec_abi_version", "spec_last_error")
+           "spec_status_string", "spec_abi_version", "spec_last_error", "spec_verify_noalloc")
 
 
 class SpecError(RuntimeError):
@@ -60,6 +60,8 @@ def lib():
     L.spec_status_string.argtypes = [ip]
     L.spec_status_string.restype = ctypes.c_char_p
     L.spec_abi_version.argtypes = []
+    L.spec_verify_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, ip, vp, ip, ip, vp, vp, vp]
+    L.spec_verify_noalloc.restype = ip
     L.spec_last_error.argtypes = []
     L.spec_last_error.restype = ctypes.c_char_p
     for name in ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",
@@ -228,3 +230,30 @@ def workspace_status(workspace=None, clear: bool = False) -> int:
                                      1 if clear else 0)
     _raise(rc, "spec_workspace_status")
     return v.value
+
+
+def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, u_accept, u_resample,
+                        temperature, k_offsets, out_tokens=None, out_num_accepted=None,
+                        stream=None):
+    """spec_verify without any device allocation inside the call: for callers
+    that cannot allocate while verifying (stream capture, allocation-free
+    serving loops, externally managed memory pools).  Scratch comes from a
+    fixed array in the library (48 MiB); larger batches raise SpecError
+    (SPEC_ERR_WORKSPACE).  Calls share that array, so keep them ordered on
+    one stream.  Output buffers may be passed in to avoid allocating them
+    here as well."""
+    import torch
+    B = temperature.numel()
+    V = target_logits.shape[-1]
+    dt = _dtype_code(target_logits)
+    R_t = u_resample.numel()
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty(R_t, dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    rc = lib().spec_verify_noalloc(_p(target_logits), _p(draft_logits), _p(draft_tokens), _p(u_accept),
+                                   _p(u_resample), _p(temperature), B, _p(k_offsets), V, dt,
+                                   _p(out_tokens), _p(out_num_accepted), _stream(stream))
+    _raise(rc, "spec_verify_noalloc")
+    return out_tokens, out_num_accepted

@@ -1405,3 +1405,77 @@ int spec_abi_version(void) { return SPEC_VERIFY_ABI_VERSION; }
 const char *spec_last_error(void) { return g_last_error; }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------
+// Allocation-free verify.
+//
+// Some callers cannot allocate device memory at the moment they need a
+// verify step: code running inside a CUDA stream capture (a cudaMalloc
+// there breaks the capture), serving loops that forbid allocation on the
+// hot path so that latency stays predictable, and memory pools or embedded
+// runtimes that own all device memory themselves.  spec_verify_noalloc
+// serves them: it runs the same kernels as spec_verify, but its scratch
+// memory is a fixed array compiled into this library, so the call itself
+// never allocates.
+//
+// The array below is a file-scope device variable.  Every GPU on which the
+// library is loaded holds kNoAllocScratchBytes of it until the process
+// exits.  Its name in host code only stands in for the device object, so
+// the host looks its device address up with cudaGetSymbolAddress, once per
+// device, with that device current.
+constexpr size_t kNoAllocScratchBytes = SPEC_NOALLOC_SCRATCH_BYTES;  // 48 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+void *g_noalloc_addr[kMaxDevices] = {};
+
+extern "C" {
+
+int spec_verify_noalloc(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
+                        const float *u_accept, const float *u_resample, const float *temperature, int B,
+                        const int32_t *k_offsets, int V, int dtype, int32_t *out_tokens,
+                        int32_t *out_num_accepted, void *stream) {
+    int rc = check_common(B, V, dtype);
+    if (rc != SPEC_OK) return rc;
+    if (B == 0) return SPEC_OK;
+    if (!target_logits || !draft_logits || !draft_tokens || !u_accept || !u_resample || !temperature ||
+        !k_offsets || !out_tokens || !out_num_accepted)
+        return SPEC_ERR_INVALID_ARG;
+    if (!aligned16(target_logits) || !aligned16(draft_logits)) return SPEC_ERR_ALIGNMENT;
+    Geometry g;
+    make_geometry(V, dtype, &g);
+    const WsLayout l = ws_layout(B, g);
+    if (l.total > kNoAllocScratchBytes) {
+        snprintf(g_last_error, sizeof g_last_error,
+                 "spec_verify_noalloc: B=%d, V=%d needs %zu bytes of scratch, the fixed array holds %zu", B, V,
+                 l.total, kNoAllocScratchBytes);
+        return SPEC_ERR_WORKSPACE;
+    }
+    int dev;
+    DeviceState *st = device_state(&dev);
+    if (!st) return SPEC_ERR_CUDA;
+    void *ws;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_noalloc_addr[dev]) {
+            // first call on this device: resolve the array's device address
+            void *p = nullptr;
+            if (!cuda_ok(cudaGetSymbolAddress(&p, g_noalloc_scratch), "cudaGetSymbolAddress(g_noalloc_scratch)"))
+                return SPEC_ERR_CUDA;
+            g_noalloc_addr[dev] = p;
+        }
+        ws = g_noalloc_addr[dev];
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the array keeps the previous call's contents: the status word is the
+    // only field that must start at zero (the kernels reset their counters)
+    if (!cuda_ok(cudaMemsetAsync(static_cast<unsigned char *>(ws) + kStatusOffset, 0, sizeof(int), s),
+                 "cudaMemsetAsync(noalloc status)"))
+        return SPEC_ERR_CUDA;
+    const spec_verify_aux_t a{};
+    if (dtype == SPEC_F32)
+        return launch_verify<SPEC_F32>(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature,
+                                       B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st, s);
+    return launch_verify<SPEC_BF16>(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature,
+                                    B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st, s);
+}
+
+}  // extern "C"
