@@ -436,8 +436,49 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(
 }
 
 // ================================================================== warp tools
-// Row combine of the n sub-chunk partials of one row by a whole warp.
-__device__ bool warp_combine_soft(const float2 *p, int n, float *M_out, double *S_out) {
+// GB300's fp64 pipe is a small fraction of its fp32 rate, so every loop
+// below (over partials, weights or elements) runs in fp32; fp64 appears only
+// in a few per-call scalars (cumulative masses, thresholds, log-sum-exps).
+
+// Two-sum accumulation: (hi, lo) carries the rounding error of each add.
+struct Acc2 {
+    float hi = 0.0f, lo = 0.0f;
+    __device__ __forceinline__ void add(float b) {
+        const float s = hi + b;
+        const float bb = s - hi;
+        lo += (hi - (s - bb)) + (b - bb);
+        hi = s;
+    }
+    __device__ __forceinline__ float value() const { return hi + lo; }
+};
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+__device__ __forceinline__ float warp_incl_scan_f(float v) {
+    const int lane = lane_id();
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float n = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += n;
+    }
+    return v;
+}
+
+// log2-domain log-sum-exp M + log2(S) for S >= 1: the exponent of S is
+// split off so that log2f works on the mantissa (absolute error ~1e-7).
+__device__ __forceinline__ double lse2(float M, float S) {
+    int e;
+    const float m = frexpf(S, &e);
+    return static_cast<double>(M) + static_cast<double>(e) + static_cast<double>(log2f(m));
+}
+
+// Row combine of the n sub-chunk partials of one row by a whole warp:
+// M = max of the partial maxima, S = sum s_i 2^(m_i - M) (>= 1).
+__device__ bool warp_combine_soft(const float2 *p, int n, float *M_out, float *S_out) {
     const int lane = lane_id();
     float M = -INFINITY;
     bool nan = false;
@@ -450,14 +491,13 @@ __device__ bool warp_combine_soft(const float2 *p, int n, float *M_out, double *
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     nan = __any_sync(0xffffffffu, nan);
     if (nan || !(M > -INFINITY) || !(M < INFINITY)) return false;
-    double S = 0.0;
+    Acc2 acc;
     for (int i = lane; i < n; i += 32) {
         const float2 v = __ldcg(p + i);
-        if (v.x > -INFINITY) S += static_cast<double>(v.y) * static_cast<double>(ex2(v.x - M));
+        if (v.x > -INFINITY) acc.add(v.y * ex2(v.x - M));
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
-    if (!(S > 0.0) || !(S < INFINITY)) return false;
+    const float S = warp_sum_f(acc.value());
+    if (!(S > 0.0f) || !(S < INFINITY)) return false;
     *M_out = M;
     *S_out = S;
     return true;
@@ -474,16 +514,6 @@ __device__ int warp_combine_arg(const float2 *p, int n) {
     return a.i == INT_MAX ? -1 : a.i;
 }
 
-__device__ __forceinline__ double warp_incl_scan_d(double v) {
-    const int lane = lane_id();
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const double n = __shfl_up_sync(0xffffffffu, v, off);
-        if (lane >= off) v += n;
-    }
-    return v;
-}
-
 // Warp-level locate over n non-negative weights wsub(i) (sub-chunk masses):
 // total Z, target = u * Z, and the first i whose cumulative mass exceeds the
 // target, with the mass before it.  If rounding leaves no such i, the last
@@ -498,17 +528,11 @@ __device__ int warp_locate(int n, WS wsub, float u, double *before, double *tota
         const int i = lane + 32 * j;
         cache[j] = (i < n) ? wsub(i) : 0.0f;
     }
-    double tot = 0.0;
-    for (int j = 0; 32 * j < n; ++j) {
-        float w = 0.0f;
+    Acc2 acc;
 #pragma unroll
-        for (int q = 0; q < kCache; ++q)
-            if (q == j) w = cache[q];
-        if (j >= kCache) w = (lane + 32 * j < n) ? wsub(lane + 32 * j) : 0.0f;
-        tot += static_cast<double>(w);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+    for (int j = 0; j < kCache; ++j) acc.add(cache[j]);
+    for (int j = kCache; 32 * j < n; ++j) acc.add((lane + 32 * j < n) ? wsub(lane + 32 * j) : 0.0f);
+    const double tot = static_cast<double>(warp_sum_f(acc.hi)) + static_cast<double>(warp_sum_f(acc.lo));
     const double target = static_cast<double>(u) * tot;
     *total = tot;
     *target_out = target;
@@ -520,19 +544,20 @@ __device__ int warp_locate(int n, WS wsub, float u, double *before, double *tota
         for (int q = 0; q < kCache; ++q)
             if (q == j) w = cache[q];
         if (j >= kCache) w = (lane + 32 * j < n) ? wsub(lane + 32 * j) : 0.0f;
-        const double incl = warp_incl_scan_d(static_cast<double>(w));
-        const double cum = carry + incl;
+        const float incl = warp_incl_scan_f(w);
+        const double cum = carry + static_cast<double>(incl);
         const unsigned hit = __ballot_sync(0xffffffffu, w > 0.0f && cum > target);
         if (hit) {
             const int src = __ffs(hit) - 1;
-            *before = __shfl_sync(0xffffffffu, cum - static_cast<double>(w), src);
+            const double bef = carry + static_cast<double>(incl - w);
+            *before = __shfl_sync(0xffffffffu, bef, src);
             return 32 * j + src;
         }
         const unsigned pos = __ballot_sync(0xffffffffu, w > 0.0f);
         if (pos) {
             const int src = 31 - __clz(pos);
             last = 32 * j + src;
-            last_before = __shfl_sync(0xffffffffu, cum - static_cast<double>(w), src);
+            last_before = __shfl_sync(0xffffffffu, carry + static_cast<double>(incl - w), src);
         }
         carry = __shfl_sync(0xffffffffu, cum, 31);
     }
@@ -586,8 +611,8 @@ __device__ int warp_scan_elems(const void *row1, const void *row2, int a, int b,
 #pragma unroll
         for (int q = 0; q < PV; ++q) lsum += W(x1[q], x2[q]);
     }
-    const double incl = warp_incl_scan_d(static_cast<double>(lsum));
-    const double start = before + incl - static_cast<double>(lsum);
+    const float incl = warp_incl_scan_f(lsum);
+    const double start = before + static_cast<double>(incl - lsum);
     const float rem = __double2float_rd(target - start);  // acc > rem  <=>  start + acc > target
     float acc = 0.0f;
     int found = -1, lastpos = -1;
@@ -643,7 +668,7 @@ __device__ int warp_draw_row(const void *logits, int64_t row, const float2 *part
 // draw for select_kernel.
 struct DecideSmem {
     float M[2 * kMaxK + 1];
-    double S[2 * kMaxK + 1];
+    float S[2 * kMaxK + 1];
     int arg[2 * kMaxK + 1];
     int ok[2 * kMaxK + 1];
 };
@@ -709,8 +734,7 @@ __global__ void __launch_bounds__(256) decide_kernel(
                     sm.ok[si] = am >= 0;
                 }
             } else {
-                float M;
-                double S;
+                float M, S;
                 const bool ok = warp_combine_soft(p, g.n_sub, &M, &S);
                 if (lane == 0) {
                     sm.M[si] = M;
@@ -741,32 +765,33 @@ __global__ void __launch_bounds__(256) decide_kernel(
         n = mism ? (__ffs(mism) - 1) : k;
         tok = sm.arg[n];
     } else if (!err) {
-        // alpha_i = min(1, p_i(x_i) / q_i(x_i)) in the log domain (fp64)
+        // alpha_i = min(1, p_i(x_i) / q_i(x_i)) in the log domain: log-ratio
+        // in fp64 scalars, the exponential in fp32 (alpha abs. error ~1e-7)
         bool acc = false;
         if (lane < k) {
-            Lt = static_cast<double>(sm.M[lane]) + log2(sm.S[lane]);
-            Ld = static_cast<double>(sm.M[kMaxK + 1 + lane]) + log2(sm.S[kMaxK + 1 + lane]);
-            double alpha;
+            Lt = lse2(sm.M[lane], sm.S[lane]);
+            Ld = lse2(sm.M[kMaxK + 1 + lane], sm.S[kMaxK + 1 + lane]);
+            float alpha;
             if (zt == -INFINITY) {
-                alpha = 0.0;
+                alpha = 0.0f;
             } else if (zd == -INFINITY) {
-                alpha = 1.0;
+                alpha = 1.0f;
             } else {
                 const double cd = static_cast<double>(c);
                 const double lr = (static_cast<double>(zt) * cd - Lt) - (static_cast<double>(zd) * cd - Ld);
-                alpha = lr >= 0.0 ? 1.0 : exp2(lr);
+                alpha = lr >= 0.0 ? 1.0f : exp2f(static_cast<float>(lr));
             }
-            alpha_out = static_cast<float>(alpha);
-            acc = static_cast<double>(u_accept[od + lane]) < alpha;
+            alpha_out = alpha;
+            acc = u_accept[od + lane] < alpha;
         } else if (lane == k) {
-            Lt = static_cast<double>(sm.M[k]) + log2(sm.S[k]);
+            Lt = lse2(sm.M[k], sm.S[k]);
         }
         const unsigned rej = __ballot_sync(0xffffffffu, lane < k && !acc);
         n = rej ? (__ffs(rej) - 1) : k;
         if (lane == 0) {
             if (n < k) {
-                const double Ltn = static_cast<double>(sm.M[n]) + log2(sm.S[n]);
-                const double Ldn = static_cast<double>(sm.M[kMaxK + 1 + n]) + log2(sm.S[kMaxK + 1 + n]);
+                const double Ltn = lse2(sm.M[n], sm.S[n]);
+                const double Ldn = lse2(sm.M[kMaxK + 1 + n], sm.S[kMaxK + 1 + n]);
                 const int e = atomicAdd(ws.counters + 0, 1);
                 RJob r;
                 r.trow = ot + n;
@@ -809,7 +834,7 @@ __global__ void __launch_bounds__(256) decide_kernel(
     if (aux.lse_target)
         for (int i = lane; i <= k; i += 32) {
             float v = NAN;
-            if (n >= 0 && !greedy) v = static_cast<float>((static_cast<double>(sm.M[i]) + log2(sm.S[i])) * kLn2D);
+            if (n >= 0 && !greedy) v = static_cast<float>(lse2(sm.M[i], sm.S[i]) * kLn2D);
             aux.lse_target[ot + i] = v;
         }
     if (aux.lse_draft && lane < k)
@@ -862,9 +887,8 @@ __global__ void __launch_bounds__(256) resid_kernel(const void *__restrict__ tar
 #pragma unroll
             for (int q = 0; q < E::kPerVec; ++q) sum += resid_weight(xt[q], xd[q], r.c, r.lth, r.ltl, r.ldh, r.ldl);
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-        if (lane == 0) ws.resid_part[static_cast<int64_t>(e) * g.n_sub + sc] = sum;
+        sum = warp_sum_f(sum);
+        if (lane == 0) ws.resid_part[u] = sum;  // u = e * n_sub + sc
     }
 }
 
@@ -948,8 +972,7 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
         if (c == 0.0f) {
             token = warp_combine_arg(pr, g.n_sub);
         } else if (c == c) {
-            float M;
-            double S;
+            float M, S;
             if (warp_combine_soft(pr, g.n_sub, &M, &S)) token = warp_draw_row<DT>(draft, r, pr, g, c, M, u_draft[r]);
         }
         if (lane == 0) out[r] = token;
