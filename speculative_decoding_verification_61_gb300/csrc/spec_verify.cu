@@ -1019,13 +1019,14 @@ struct WsLayout {
 // Workspace layout.  The counters block comes first so that the status word
 // has a fixed offset (kStatusOffset) whatever B and V are.
 constexpr size_t kStatusOffset = sizeof(int);  // counters[1]
+constexpr size_t kCountersBytes = 256;
 
 WsLayout ws_layout(int B, const Geometry &g) {
     WsLayout l;
     size_t off = 0;
     const size_t rows_cap = static_cast<size_t>(2 * kMaxK + 1) * B;
     l.counters = off;
-    off = align_up(off + 64, 256);
+    off = align_up(off + kCountersBytes, 256);
     l.part = off;
     off = align_up(off + rows_cap * g.n_sub * sizeof(float2), 256);
     l.jobs = off;
@@ -1101,14 +1102,21 @@ size_t stats_smem(int ns, int B) {
     return align_up(s, 128);
 }
 
-// Ring depth and CTAs per SM: three CTAs per SM with four slots each if they
-// fit (more warps to hide latency), else two CTAs with up to kMaxSlots, else
-// one.
+// Ring depth and CTAs per SM of stats_kernel: the preferred shape
+// (SPEC_STATS_CTAS_PER_SM CTAs with SPEC_STATS_SLOTS slots each; three CTAs
+// of four 16 KB slots give 24 consumer warps and 192 KB in flight per SM)
+// if the tables fit beside it, else two CTAs with up to kMaxSlots, else one.
+#ifndef SPEC_STATS_CTAS_PER_SM
+#define SPEC_STATS_CTAS_PER_SM 3
+#endif
+#ifndef SPEC_STATS_SLOTS
+#define SPEC_STATS_SLOTS 4
+#endif
 void pick_ring(const DeviceState &st, int B, int *ns, size_t *smem, int *ctas_per_sm) {
     struct Opt {
         int per_sm, min_ns, max_ns;
     };
-    const Opt opts[] = {{3, 4, 4}, {2, 3, kMaxSlots}, {1, 2, kMaxSlots}};
+    const Opt opts[] = {{SPEC_STATS_CTAS_PER_SM, SPEC_STATS_SLOTS, SPEC_STATS_SLOTS}, {2, 3, kMaxSlots}, {1, 2, kMaxSlots}};
     for (const Opt &o : opts) {
         const size_t budget = static_cast<size_t>(st.smem_per_sm) / o.per_sm - 1024;
         for (int n = o.max_ns; n >= o.min_ns; --n) {
