@@ -83,6 +83,21 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
         : "memory");
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 by the TMA engine, without
+// registers or shared memory (src and bytes multiples of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Atomic add with acquire-release semantics at GPU scope: the caller's
+// earlier writes are visible to whoever later acquires the counter, and
+// the caller sees the writes released by earlier adders.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // Hardware base-2 exponential (MUFU.EX2): ~2 ulp, subnormal results flushed
 // to zero, ex2(-inf) = 0, ex2(NaN) = NaN.
 __device__ __forceinline__ float ex2(float x) {
@@ -293,6 +308,17 @@ __device__ __forceinline__ float resid_weight(float zt, float zd, float c, float
     const float at = __fsub_rn(__fmaf_rn(zt, c, -lth), ltl);
     const float ad = __fsub_rn(__fmaf_rn(zd, c, -ldh), ldl);
     return fmaxf(__fsub_rn(ex2(at), ex2(ad)), 0.0f);
+}
+
+// Two residual weights at once in packed fp32.  Lane for lane these are the
+// operations of resid_weight (x - y is rounded exactly as x + (-y)), so the
+// bits are the same; nl* are the negated hi/lo parts of L.
+__device__ __forceinline__ float2 resid_weight2(float2 zt, float2 zd, float2 c2, float2 nlth2, float2 nltl2,
+                                                float2 nldh2, float2 nldl2) {
+    const float2 at = fadd2(ffma2(zt, c2, nlth2), nltl2);
+    const float2 ad = fadd2(ffma2(zd, c2, nldh2), nldl2);
+    const float2 d = fadd2(make_float2(ex2(at.x), ex2(at.y)), make_float2(-ex2(ad.x), -ex2(ad.y)));
+    return make_float2(fmaxf(d.x, 0.0f), fmaxf(d.y, 0.0f));
 }
 
 // Target/draft probability weight 2^(z*c - M) relative to the row max M.

@@ -11,22 +11,21 @@
 //     of a batch, different accepted lengths).
 //
 // Pipeline of one spec_verify call (all on the caller's stream, no host sync):
-//   1. stats_kernel   persistent; streams every needed logit row through a
-//                     shared-memory ring filled by 1-D bulk copies (TMA
-//                     engine) and reduces each 16 KB chunk to an online
-//                     softmax partial (max m, sum 2^(x c - m)) or, for greedy
-//                     rows, an arg-max partial.  Each row is read from HBM
-//                     once.
-//   2. decide_kernel  one warp per sequence: combines the chunk partials of
-//                     its rows in fp64, forms alpha_i, finds the first
-//                     rejection with a warp ballot, writes the accepted
-//                     prefix, and queues the residual or bonus draw.
-//   3. resid_kernel   for every rejected sequence, sum of max(0, p - q) over
-//                     each half-chunk of the two rows at the rejected position.
-//   4. select_kernel  one block per sequence: locates the half-chunk (residual)
-//                     or chunk (bonus) where the cumulative mass crosses u * Z,
-//                     re-reads only that piece and finds the token with a
-//                     block-wide prefix scan.
+//   1. stats_kernel    persistent; streams every needed logit row through a
+//                      shared-memory ring filled by 1-D bulk copies (TMA
+//                      engine) and reduces each 2 KB sub-chunk to an online
+//                      softmax partial (max m, sum 2^(x c - m)) or, for
+//                      greedy rows, an arg-max partial.  Each row is read
+//                      from HBM once.
+//   2. resolve_kernel  kSub blocks per sequence: each combines the partials
+//                      of the sequence's rows, forms alpha_i and finds the
+//                      first rejection with a warp ballot; on a rejection the
+//                      blocks share the residual mass max(0, p - q) of the two
+//                      rows at that position, and the last warp to finish
+//                      locates the sub-chunk where the cumulative mass crosses
+//                      u * Z, re-reads only that piece and finds the token
+//                      with a warp scan.  The bonus draw uses the partials of
+//                      row k the same way.
 // spec_draft_sample runs stats_kernel over the draft rows, then
 // draft_select_kernel (arg-max, or the same locate + scan per row).
 
@@ -50,7 +49,7 @@ constexpr int kSub = kConsumerWarps;                // sub-chunks per chunk (one
 constexpr int kSubVecs = kSlotBytes / 16 / kSub;    // 16-byte vectors per sub-chunk (2 KB)
 
 enum UnitKind : int { kEnd = 0, kSoft = 1, kArg = 2 };
-enum JobKind : int { kJobNone = 0, kJobResid = 1, kJobBonus = 2 };
+enum DrawKind : int { kJobNone = 0, kJobResid = 1, kJobBonus = 2 };
 
 struct Geometry {
     int V;
@@ -68,25 +67,14 @@ struct UnitDesc {
     int64_t out_idx;
 };
 
-// Decision left for the select kernel, one per sequence.
-struct SeqJob {
-    int kind;
-    int list_idx;  // residual list position
-    int64_t trow;  // target row = output slot of the drawn token
-    float c, M, u, pad;
-};
-
-// Residual job, one per rejected sequence (list order).
-struct RJob {
-    int64_t trow, drow;
-    float c, lth, ltl, ldh, ldl, pad;
-};
+// Words of the workspace's counter block.
+// Status word, then stats_kernel's unit tickets and count of CTAs done.
+enum CounterWord : int { kStatus = 1, kTicket = 2, kDone = 3, kCounterWords = 4 };
 
 struct WsPtrs {
     float2 *part;        // [rows_cap * n_sub] sub-chunk partials
-    SeqJob *jobs;        // [B]
-    RJob *rjobs;         // [B]
-    int *counters;       // [0] residual count, [1] status, [2] bad k_offsets
+    int *counters;       // CounterWord: status, unit tickets and CTAs done
+    int *seqcnt;         // [B] resolve_kernel arrivals per sequence
     float *resid_part;   // [B * n_sub] residual mass per sub-chunk
 };
 
@@ -190,23 +178,59 @@ __device__ double block_sum_d(double v, double *s_warp) {
     return r;
 }
 
+// ------------------------------------------------------------ unit tickets
+// stats_kernel hands out its units dynamically: an SM that streams faster
+// takes more of them, so all CTAs finish together.  Ticket t (one atomic
+// add on a counter) is a batch of kStatsBatch consecutive units while at
+// least kStatsTailPerCta units per CTA remain after it, then a batch of
+// kStatsTailBatch, which keeps the finishing times within a fraction of a
+// microsecond without an atomic per unit.
+#ifndef SPEC_STATS_BATCH
+#define SPEC_STATS_BATCH 4
+#endif
+#ifndef SPEC_STATS_TAIL_BATCH
+#define SPEC_STATS_TAIL_BATCH 1
+#endif
+#ifndef SPEC_STATS_TAIL_PER_CTA
+#define SPEC_STATS_TAIL_PER_CTA 8
+#endif
+constexpr int kStatsBatch = SPEC_STATS_BATCH;
+constexpr int kStatsTailBatch = SPEC_STATS_TAIL_BATCH;
+constexpr int kStatsTailPerCta = SPEC_STATS_TAIL_PER_CTA;
+
+__device__ __forceinline__ int64_t big_batches(int64_t total_units, int grid) {
+    return max(static_cast<int64_t>(0), (total_units - static_cast<int64_t>(grid) * kStatsTailPerCta) / kStatsBatch);
+}
+
+__device__ __forceinline__ void unit_batch(int t, int64_t n_big, int64_t *u0, int *cnt) {
+    if (t < n_big) {
+        *u0 = static_cast<int64_t>(t) * kStatsBatch;
+        *cnt = kStatsBatch;
+    } else {
+        *u0 = n_big * kStatsBatch + (t - n_big) * static_cast<int64_t>(kStatsTailBatch);
+        *cnt = kStatsTailBatch;
+    }
+}
+
 // ================================================================== kernel 1
 // Persistent streaming kernel.  Unit u = (row r of the virtual row list,
 // chunk ch).  Virtual row list, by sequence b in order:
 //   verify mode: target rows of b (k_b + 1), then draft rows of b (k_b) if
 //                b is sampled; nothing for a bad temperature;
 //   draft mode:  draft rows of b (k_b); nothing for a bad temperature.
-// CTA g takes units g, g + G, g + 2G, ...  One lane of warp 8 is the
+// Units are taken by tickets (unit_batch).  One lane of warp 8 is the
 // producer: it waits for a free ring slot and issues the bulk copy of the
 // next unit into it.  Warps 0..7 consume: warp w owns the w-th 2 KB
 // sub-chunk of the slot (128 16-byte vectors, lane l reading vectors
 // l + 32 j), reduces it to a partial (online softmax or arg-max) and writes
 // that partial straight to global memory.
+// (the bound caps registers at 40, which leaves room on an SM with four
+// of these CTAs for one resolve_kernel block of the other stream)
 template <int DT, bool DRAFT>
-__global__ void __launch_bounds__(kThreads) stats_kernel(
+__global__ void __launch_bounds__(kThreads, 5) stats_kernel(
     const void *__restrict__ target, const void *__restrict__ draft,
-    const float *__restrict__ temperature, const int *__restrict__ k_offsets, int B, Geometry g,
-    int ns, float2 *__restrict__ part, int *__restrict__ counters) {
+    const float *__restrict__ temperature, const int *__restrict__ k_offsets, int B, Geometry g, int ns,
+    float2 *__restrict__ part, int *__restrict__ counters, int *__restrict__ seqcnt) {
     using E = Elem<DT>;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char *ring = smem;
@@ -230,34 +254,35 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(
     const int b0 = min(B, tid * seg), b1 = min(B, b0 + seg);
     int bad = (tid == 0 && s_kofs[0] != 0) ? 1 : 0;
     int rows = 0;
+    // rows of sequence b: none for a bad temperature
+    auto seq_rows = [&](int b) -> int {
+        const int k = s_kofs[b + 1] - s_kofs[b];
+        const float c = s_c[b];
+        if (c != c) return 0;
+        return DRAFT ? k : (c == 0.0f ? k + 1 : 2 * k + 1);
+    };
     for (int b = b0; b < b1; ++b) {
         const int k = s_kofs[b + 1] - s_kofs[b];
         if (k < 0 || k > kMaxK) bad = 1;
-        const float c = s_c[b];
-        if (c != c) continue;
-        rows += DRAFT ? k : (c == 0.0f ? k + 1 : 2 * k + 1);
+        rows += seq_rows(b);
     }
     int total_rows;
     int base = block_excl_scan(rows, s_tmp, &total_rows);
     for (int b = b0; b < b1; ++b) {
         s_rowpre[b] = base;
-        const int k = s_kofs[b + 1] - s_kofs[b];
-        const float c = s_c[b];
-        if (c == c) base += DRAFT ? k : (c == 0.0f ? k + 1 : 2 * k + 1);
+        base += seq_rows(b);
     }
     if (tid == 0) s_rowpre[B] = total_rows;
     // everything above only read the inputs; from here on the workspace is
     // written, so the previous kernel on the stream must have finished
     grid_dependency_wait();
     const bool any_bad = __syncthreads_or(bad);
-    if (!DRAFT && blockIdx.x == 0 && tid == 0) {
-        counters[0] = 0;  // residual list
-        counters[2] = any_bad ? 1 : 0;
-    }
-    if (any_bad) {
-        grid_launch_dependents();
-        return;
-    }
+    if (!DRAFT)
+        for (int i = blockIdx.x * kThreads + tid; i < B; i += gridDim.x * kThreads) seqcnt[i] = 0;
+    // the next kernel may be scheduled as soon as SMs free up; it waits for
+    // this grid's completion before it reads anything written here
+    grid_launch_dependents();
+    if (any_bad) return;
 
     if (tid == 0) {
         for (int s = 0; s < ns; ++s) {
@@ -273,89 +298,96 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(
 
     if (warp_id() == kConsumerWarps) {
         // ------------------------------------------------------ producer
-        if (lane != 0) return;
-        int issued = 0;
-        bool ok = true;
-        // unit index u = r * n_chunks + ch, stepped by the grid size
-        // without 64-bit divisions in the loop
-        const int G = gridDim.x;
-        const int dq = G / g.n_chunks, dr = G - dq * g.n_chunks;
-        int r = static_cast<int>(blockIdx.x / g.n_chunks);
-        int ch = static_cast<int>(blockIdx.x - r * g.n_chunks);
-        int b = 0;
-        int islot = 0;
-        uint32_t iphase = 0;  // slot and use parity of the next issue
-        for (; r < total_rows;) {
-            if (issued >= ns && !mbar_wait_bounded(&empty[islot], iphase ^ 1u)) {
-                ok = false;
-                break;
+        if (lane == 0) {
+            int issued = 0;
+            bool ok = true;
+            // units u = r * n_chunks + ch are handed out by tickets (see
+            // unit_batch); each CTA's units increase, so b only moves forward
+            const int64_t total_units = static_cast<int64_t>(total_rows) * g.n_chunks;
+            const int64_t n_big = big_batches(total_units, gridDim.x);
+            int b = 0;
+            int islot = 0;
+            uint32_t iphase = 0;  // slot and use parity of the next issue
+            int t = atomicAdd(counters + kTicket, 1);
+            while (ok) {
+                int64_t u0;
+                int cnt;
+                unit_batch(t, n_big, &u0, &cnt);
+                if (u0 >= total_units) break;
+                const int tn = atomicAdd(counters + kTicket, 1);  // next batch, in flight meanwhile
+                cnt = static_cast<int>(min(static_cast<int64_t>(cnt), total_units - u0));
+                int r = static_cast<int>(u0 / g.n_chunks);
+                int ch = static_cast<int>(u0 - static_cast<int64_t>(r) * g.n_chunks);
+                for (int q = 0; q < cnt; ++q) {
+                    if (issued >= ns && !mbar_wait_bounded(&empty[islot], iphase ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    while (s_rowpre[b + 1] <= r) ++b;
+                    const int l = r - s_rowpre[b];
+                    const int k = s_kofs[b + 1] - s_kofs[b];
+                    const float c = s_c[b];
+                    const void *base_ptr;
+                    int64_t row, slot_row;
+                    if (DRAFT) {
+                        row = s_kofs[b] + l;
+                        base_ptr = draft;
+                        slot_row = row;
+                    } else if (l <= k) {
+                        row = static_cast<int64_t>(s_kofs[b]) + b + l;
+                        base_ptr = target;
+                        slot_row = row;
+                    } else {
+                        row = static_cast<int64_t>(s_kofs[b]) + (l - k - 1);
+                        base_ptr = draft;
+                        slot_row = R_t + row;
+                    }
+                    const int e0 = ch * g.chunk_elems;
+                    const int e1 = min(g.V, e0 + g.chunk_elems);
+                    UnitDesc d;
+                    d.nbytes = static_cast<uint32_t>(e1 - e0) * E::kBytes;
+                    d.kind = (c == 0.0f) ? kArg : kSoft;
+                    d.c = c;
+                    d.elem0 = e0;
+                    d.out_idx = (slot_row * g.n_chunks + ch) * kSub;
+                    desc[islot] = d;
+                    const unsigned char *src = static_cast<const unsigned char *>(base_ptr) +
+                                               (row * g.V + e0) * static_cast<int64_t>(E::kBytes);
+                    mbar_arrive_expect_tx(&full[islot], d.nbytes);
+                    bulk_g2s(ring + static_cast<size_t>(islot) * kSlotBytes, src, d.nbytes, &full[islot]);
+                    ++issued;
+                    if (++islot == ns) {
+                        islot = 0;
+                        iphase ^= 1u;
+                    }
+                    if (++ch == g.n_chunks) {
+                        ch = 0;
+                        ++r;
+                    }
+                }
+                t = tn;
             }
-            while (s_rowpre[b + 1] <= r) ++b;
-            const int l = r - s_rowpre[b];
-            const int k = s_kofs[b + 1] - s_kofs[b];
-            const float c = s_c[b];
-            const void *base_ptr;
-            int64_t row, slot_row;
-            if (DRAFT) {
-                row = s_kofs[b] + l;
-                base_ptr = draft;
-                slot_row = row;
-            } else if (l <= k) {
-                row = static_cast<int64_t>(s_kofs[b]) + b + l;
-                base_ptr = target;
-                slot_row = row;
-            } else {
-                row = static_cast<int64_t>(s_kofs[b]) + (l - k - 1);
-                base_ptr = draft;
-                slot_row = R_t + row;
+            if (ok && issued >= ns) ok = mbar_wait_bounded(&empty[islot], iphase ^ 1u);
+            {
+                // end marker (also on time-out, so that consumers leave)
+                desc[islot].kind = kEnd;
+                mbar_arrive(&full[islot]);
             }
-            const int e0 = ch * g.chunk_elems;
-            const int e1 = min(g.V, e0 + g.chunk_elems);
-            UnitDesc d;
-            d.nbytes = static_cast<uint32_t>(e1 - e0) * E::kBytes;
-            d.kind = (c == 0.0f) ? kArg : kSoft;
-            d.c = c;
-            d.elem0 = e0;
-            d.out_idx = (slot_row * g.n_chunks + ch) * kSub;
-            desc[islot] = d;
-            const unsigned char *src = static_cast<const unsigned char *>(base_ptr) +
-                                       (row * g.V + e0) * static_cast<int64_t>(E::kBytes);
-            mbar_arrive_expect_tx(&full[islot], d.nbytes);
-            bulk_g2s(ring + static_cast<size_t>(islot) * kSlotBytes, src, d.nbytes, &full[islot]);
-            ++issued;
-            if (++islot == ns) {
-                islot = 0;
-                iphase ^= 1u;
-            }
-            ch += dr;
-            r += dq;
-            if (ch >= g.n_chunks) {
-                ch -= g.n_chunks;
-                ++r;
+            if (!ok) {
+                set_status(counters + kStatus, SPEC_ERR_TIMEOUT);
+                // let issued copies land before the CTA exits (bounded)
+                for (int i = max(0, issued - ns); i < issued; ++i) mbar_wait_bounded(&full[i % ns], (i / ns) & 1);
             }
         }
-        grid_launch_dependents();
-        if (ok && issued >= ns) ok = mbar_wait_bounded(&empty[islot], iphase ^ 1u);
-        {
-            // end marker (also on time-out, so that consumers leave)
-            desc[islot].kind = kEnd;
-            mbar_arrive(&full[islot]);
-        }
-        if (!ok) {
-            set_status(counters + 1, SPEC_ERR_TIMEOUT);
-            // let issued copies land before the CTA exits (bounded)
-            for (int i = max(0, issued - ns); i < issued; ++i) mbar_wait_bounded(&full[i % ns], (i / ns) & 1);
-        }
-        return;
-    }
-
+        __syncwarp();
+    } else {
     // ---------------------------------------------------------- consumers
     const int w = warp_id();
     int slot = 0;
     uint32_t phase = 0;
     for (;;) {
         if (!mbar_wait_bounded(&full[slot], phase)) {
-            set_status(counters + 1, SPEC_ERR_TIMEOUT);
+            set_status(counters + kStatus, SPEC_ERR_TIMEOUT);
             break;
         }
         const UnitDesc d = desc[slot];
@@ -433,6 +465,14 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(
         }
         if (lane == 0) part[d.out_idx + w] = res;
     }
+    }
+    // the last CTA out resets the ticket counters for the next launch on the
+    // stream (the library zeroes them once when it allocates a workspace)
+    __syncthreads();
+    if (tid == 0 && atomic_add_acq_rel_gpu(counters + kDone, 1) == static_cast<int>(gridDim.x) - 1) {
+        counters[kTicket] = 0;
+        counters[kDone] = 0;
+    }
 }
 
 // ================================================================== warp tools
@@ -477,12 +517,27 @@ __device__ __forceinline__ double lse2(float M, float S) {
 }
 
 // Row combine of the n sub-chunk partials of one row by a whole warp:
-// M = max of the partial maxima, S = sum s_i 2^(m_i - M) (>= 1).
+// M = max of the partial maxima, S = sum s_i 2^(m_i - M) (>= 1).  The
+// first 32 * kCache partials are loaded once into registers (one memory
+// round trip for rows of up to 256 sub-chunks); lane l adds its partials in
+// index order whether cached or not.
 __device__ bool warp_combine_soft(const float2 *p, int n, float *M_out, float *S_out) {
     const int lane = lane_id();
+    constexpr int kCache = 8;
+    float2 cache[kCache];
+#pragma unroll
+    for (int j = 0; j < kCache; ++j) {
+        const int i = lane + 32 * j;
+        cache[j] = (i < n) ? __ldcg(p + i) : make_float2(-INFINITY, 0.0f);
+    }
     float M = -INFINITY;
     bool nan = false;
-    for (int i = lane; i < n; i += 32) {
+#pragma unroll
+    for (int j = 0; j < kCache; ++j) {
+        nan |= (cache[j].y != cache[j].y);
+        M = fmaxf(M, cache[j].x);
+    }
+    for (int i = lane + 32 * kCache; i < n; i += 32) {
         const float2 v = __ldcg(p + i);
         nan |= (v.y != v.y);
         M = fmaxf(M, v.x);
@@ -492,7 +547,10 @@ __device__ bool warp_combine_soft(const float2 *p, int n, float *M_out, float *S
     nan = __any_sync(0xffffffffu, nan);
     if (nan || !(M > -INFINITY) || !(M < INFINITY)) return false;
     Acc2 acc;
-    for (int i = lane; i < n; i += 32) {
+#pragma unroll
+    for (int j = 0; j < kCache; ++j)
+        if (cache[j].x > -INFINITY) acc.add(cache[j].y * ex2(cache[j].x - M));
+    for (int i = lane + 32 * kCache; i < n; i += 32) {
         const float2 v = __ldcg(p + i);
         if (v.x > -INFINITY) acc.add(v.y * ex2(v.x - M));
     }
@@ -661,39 +719,70 @@ __device__ int warp_draw_row(const void *logits, int64_t row, const float2 *part
 }
 
 // ================================================================== kernel 2
-// One block per sequence: warps combine the sub-chunk partials of the
-// sequence's rows (one row per warp at a time) into shared memory; warp 0
-// then decides (lane i = drafted position i, ballot for the first
-// rejection), writes the accepted prefix and queues the residual or bonus
-// draw for select_kernel.
-struct DecideSmem {
+// The epilogue of spec_verify in one launch of B * nsplit blocks; block
+// (b, s) serves sequence b and the s-th of nsplit slices of a row's
+// sub-chunks (nsplit is sized so that the grid has a few blocks per SM).
+//  1. Every block of b combines the sub-chunk partials of b's rows, forms
+//     alpha_i and finds the first rejection n with a warp ballot.  All
+//     blocks of b run the same arithmetic on the same data, so they reach
+//     the same decision.
+//  2. If a drafted token of a sampled sequence was rejected, block s sums
+//     max(0, p - q) over its slice of the two rows at position n.
+//  3. The warp of b that finishes step 2 last (per-sequence arrival
+//     counter, zeroed by stats_kernel) draws the residual token: it locates
+//     the sub-chunk where the cumulative mass crosses u * Z and scans its
+//     elements.  Block s == 0 writes the accepted prefix, the count and the
+//     aux outputs, and draws the bonus (all k accepted) or greedy token.
+// The call's inputs (the k_offsets check, drafted tokens and their logits)
+// are read before the wait on stats_kernel, which hides that latency behind
+// the streaming pass's tail.
+struct ResolveSmem {
     float M[2 * kMaxK + 1];
     float S[2 * kMaxK + 1];
     int arg[2 * kMaxK + 1];
     int ok[2 * kMaxK + 1];
+    int n;     // accepted count, -1 on a data error
+    int kind;  // kJobNone, kJobResid or kJobBonus
+    float lth, ltl, ldh, ldl, u;
 };
 
+#ifndef SPEC_RESOLVE_MIN_BLOCKS
+#define SPEC_RESOLVE_MIN_BLOCKS 4
+#endif
 template <int DT>
-__global__ void __launch_bounds__(256) decide_kernel(
+__global__ void __launch_bounds__(256, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
     const void *__restrict__ target, const void *__restrict__ draft,
     const int32_t *__restrict__ tokens, const float *__restrict__ u_accept,
     const float *__restrict__ u_resample, const float *__restrict__ temperature,
-    const int *__restrict__ k_offsets, int B, Geometry g, WsPtrs ws, int32_t *__restrict__ out_tokens,
-    int32_t *__restrict__ out_num, spec_verify_aux_t aux) {
+    const int *__restrict__ k_offsets, int B, Geometry g, int nsplit, WsPtrs ws,
+    int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_num, spec_verify_aux_t aux) {
     using E = Elem<DT>;
-    __shared__ DecideSmem sm;
-    grid_dependency_wait();
-    grid_launch_dependents();
-    const int b = blockIdx.x;
+    __shared__ ResolveSmem sm;
+    const int b = blockIdx.x / nsplit;
+    const int s = blockIdx.x - b * nsplit;
     const int lane = lane_id(), warp = warp_id();
-    SeqJob job{kJobNone, -1, 0, 0.f, 0.f, 0.f, 0.f};
-    if (__ldcg(ws.counters + 2) != 0) {
-        // invalid k_offsets: the whole call fails, outputs of unknown size untouched
-        if (threadIdx.x == 0) {
+
+    // --- inputs only (written before this call) --------------------------
+    // the same k_offsets check as stats_kernel: only with it do the row
+    // indices below stay inside the caller's buffers
+    int bad = 0;
+    for (int i = threadIdx.x; i <= B; i += blockDim.x) {
+        const int v = k_offsets[i];
+        if (i == 0) {
+            bad |= v != 0;
+        } else {
+            const int kk = v - k_offsets[i - 1];
+            bad |= (kk < 0 || kk > kMaxK);
+        }
+    }
+    bad = __syncthreads_or(bad);
+    if (bad) {
+        // the whole call fails; outputs of unknown size stay untouched
+        grid_dependency_wait();
+        if (s == 0 && threadIdx.x == 0) {
             out_num[b] = -1;
-            ws.jobs[b] = job;
             if (aux.residual_mass) aux.residual_mass[b] = NAN;
-            if (b == 0) set_status(ws.counters + 1, SPEC_ERR_INVALID_ARG);
+            if (b == 0) set_status(ws.counters + kStatus, SPEC_ERR_INVALID_ARG);
         }
         return;
     }
@@ -705,20 +794,24 @@ __global__ void __launch_bounds__(256) decide_kernel(
     const float c = temp_scale(temperature[b]);
     const int V = g.V;
     const bool greedy = (c == 0.0f);
-
-    // warp 0 fetches the drafted tokens and their logits early
     int x = 0;
     bool xbad = false;
-    float zt = 0.0f, zd = 0.0f;
-    if (warp == 0 && lane < k) {
-        x = tokens[od + lane];
-        xbad = (x < 0 || x >= V);
-        if (!xbad && !greedy && c == c) {
-            zt = E::load1(target, (ot + lane) * V + x);
-            zd = E::load1(draft, (od + lane) * V + x);
+    float zt = 0.0f, zd = 0.0f, ua = 0.0f, ur = 0.0f;
+    if (warp == 0 && lane <= k) {
+        ur = u_resample[ot + lane];  // lane <= k <= 32 is at most lane 31 here
+        if (lane < k) {
+            x = tokens[od + lane];
+            ua = u_accept[od + lane];
+            xbad = (x < 0 || x >= V);
+            if (!xbad && !greedy && c == c) {
+                zt = E::load1(target, (ot + lane) * V + x);
+                zd = E::load1(draft, (od + lane) * V + x);
+            }
         }
     }
-    // row statistics: target rows 0..k at [0, k], draft rows at [kMaxK+1 ...]
+
+    // --- 1. row statistics and the decision -------------------------------
+    grid_dependency_wait();
     if (c == c) {
         const int nrows = greedy ? k + 1 : 2 * k + 1;
         for (int rr = warp; rr < nrows; rr += blockDim.x >> 5) {
@@ -745,129 +838,142 @@ __global__ void __launch_bounds__(256) decide_kernel(
         }
     }
     __syncthreads();
-    if (warp != 0) return;
-
-    bool err = (c != c) || __any_sync(0xffffffffu, xbad);
-    int n = -1, tok = -1;
-    float alpha_out = NAN;
-    double Lt = NAN, Ld = NAN;
-    if (!err) {
-        bool rows_ok = true;
-        for (int i = lane; i <= k; i += 32) rows_ok &= sm.ok[i] != 0;
-        if (!greedy)
-            for (int i = lane; i < k; i += 32) rows_ok &= sm.ok[kMaxK + 1 + i] != 0;
-        err = !__all_sync(0xffffffffu, rows_ok);
-    }
-    if (!err && greedy) {
-        // greedy: accept while x_i == argmax p_i
-        const int a = (lane <= k) ? sm.arg[lane] : 0;
-        const unsigned mism = __ballot_sync(0xffffffffu, lane < k && x != a);
-        n = mism ? (__ffs(mism) - 1) : k;
-        tok = sm.arg[n];
-    } else if (!err) {
-        // alpha_i = min(1, p_i(x_i) / q_i(x_i)) in the log domain: log-ratio
-        // in fp64 scalars, the exponential in fp32 (alpha abs. error ~1e-7)
-        bool acc = false;
-        if (lane < k) {
-            Lt = lse2(sm.M[lane], sm.S[lane]);
-            Ld = lse2(sm.M[kMaxK + 1 + lane], sm.S[kMaxK + 1 + lane]);
-            float alpha;
-            if (zt == -INFINITY) {
-                alpha = 0.0f;
-            } else if (zd == -INFINITY) {
-                alpha = 1.0f;
-            } else {
-                const double cd = static_cast<double>(c);
-                const double lr = (static_cast<double>(zt) * cd - Lt) - (static_cast<double>(zd) * cd - Ld);
-                alpha = lr >= 0.0 ? 1.0f : exp2f(static_cast<float>(lr));
-            }
-            alpha_out = alpha;
-            acc = u_accept[od + lane] < alpha;
-        } else if (lane == k) {
-            Lt = lse2(sm.M[k], sm.S[k]);
+    if (warp == 0) {
+        bool err = (c != c) || __any_sync(0xffffffffu, xbad);
+        int n = -1, tok = -1, kind = kJobNone;
+        float alpha_out = NAN;
+        double Lt = NAN, Ld = NAN;
+        if (!err) {
+            bool rows_ok = true;
+            for (int i = lane; i <= k; i += 32) rows_ok &= sm.ok[i] != 0;
+            if (!greedy)
+                for (int i = lane; i < k; i += 32) rows_ok &= sm.ok[kMaxK + 1 + i] != 0;
+            err = !__all_sync(0xffffffffu, rows_ok);
         }
-        const unsigned rej = __ballot_sync(0xffffffffu, lane < k && !acc);
-        n = rej ? (__ffs(rej) - 1) : k;
+        if (!err && greedy) {
+            // greedy: accept while x_i == argmax p_i
+            const int a = (lane <= k) ? sm.arg[lane] : 0;
+            const unsigned mism = __ballot_sync(0xffffffffu, lane < k && x != a);
+            n = mism ? (__ffs(mism) - 1) : k;
+            tok = sm.arg[n];
+        } else if (!err) {
+            // alpha_i = min(1, p_i(x_i) / q_i(x_i)) in the log domain: log-ratio
+            // in fp64 scalars, the exponential in fp32 (alpha abs. error ~1e-7)
+            bool acc = false;
+            if (lane < k) {
+                Lt = lse2(sm.M[lane], sm.S[lane]);
+                Ld = lse2(sm.M[kMaxK + 1 + lane], sm.S[kMaxK + 1 + lane]);
+                float alpha;
+                if (zt == -INFINITY) {
+                    alpha = 0.0f;
+                } else if (zd == -INFINITY) {
+                    alpha = 1.0f;
+                } else {
+                    const double cd = static_cast<double>(c);
+                    const double lr = (static_cast<double>(zt) * cd - Lt) - (static_cast<double>(zd) * cd - Ld);
+                    alpha = lr >= 0.0 ? 1.0f : exp2f(static_cast<float>(lr));
+                }
+                alpha_out = alpha;
+                acc = ua < alpha;
+            } else if (lane == k) {
+                Lt = lse2(sm.M[k], sm.S[k]);
+            }
+            const unsigned rej = __ballot_sync(0xffffffffu, lane < k && !acc);
+            n = rej ? (__ffs(rej) - 1) : k;
+            kind = n < k ? kJobResid : kJobBonus;
+            // u at position n; position 32 (k = 32, all accepted) has no lane
+            float u_n = __shfl_sync(0xffffffffu, ur, n & 31);
+            if (n == 32) u_n = u_resample[ot + 32];
+            if (lane == 0) {
+                if (n < k) {
+                    const double Ltn = lse2(sm.M[n], sm.S[n]);
+                    const double Ldn = lse2(sm.M[kMaxK + 1 + n], sm.S[kMaxK + 1 + n]);
+                    sm.lth = static_cast<float>(Ltn);
+                    sm.ltl = static_cast<float>(Ltn - static_cast<double>(sm.lth));
+                    sm.ldh = static_cast<float>(Ldn);
+                    sm.ldl = static_cast<float>(Ldn - static_cast<double>(sm.ldh));
+                }
+                sm.u = u_n;
+            }
+        }
         if (lane == 0) {
-            if (n < k) {
-                const double Ltn = lse2(sm.M[n], sm.S[n]);
-                const double Ldn = lse2(sm.M[kMaxK + 1 + n], sm.S[kMaxK + 1 + n]);
-                const int e = atomicAdd(ws.counters + 0, 1);
-                RJob r;
-                r.trow = ot + n;
-                r.drow = od + n;
-                r.c = c;
-                r.lth = static_cast<float>(Ltn);
-                r.ltl = static_cast<float>(Ltn - static_cast<double>(r.lth));
-                r.ldh = static_cast<float>(Ldn);
-                r.ldl = static_cast<float>(Ldn - static_cast<double>(r.ldh));
-                r.pad = 0.f;
-                ws.rjobs[e] = r;
-                job.kind = kJobResid;
-                job.list_idx = e;
-            } else {
-                job.kind = kJobBonus;
-                job.M = sm.M[k];
+            sm.n = n;
+            sm.kind = kind;
+        }
+        if (s == 0) {
+            // outputs: prefix, the greedy token at n (sampled draws are
+            // written by the drawing block), -1 after; everything -1 on a
+            // data error
+            for (int i = lane; i <= k; i += 32) {
+                if (i == n && kind != kJobNone) continue;
+                int32_t o = -1;
+                if (n >= 0) {
+                    if (i < n) o = x;  // i < n <= 32, so i == lane: this lane's own token
+                    else if (i == n && greedy) o = tok;
+                }
+                out_tokens[ot + i] = o;
             }
-            job.trow = ot + n;
-            job.c = c;
-            job.u = u_resample[ot + n];
+            if (lane == 0) {
+                out_num[b] = n;
+                if (aux.residual_mass && kind != kJobResid) aux.residual_mass[b] = NAN;
+            }
+            if (aux.accept_prob && lane < k) aux.accept_prob[od + lane] = (n >= 0 && !greedy) ? alpha_out : NAN;
+            if (aux.lse_target)
+                for (int i = lane; i <= k; i += 32) {
+                    float v = NAN;
+                    if (n >= 0 && !greedy) v = static_cast<float>(lse2(sm.M[i], sm.S[i]) * kLn2D);
+                    aux.lse_target[ot + i] = v;
+                }
+            if (aux.lse_draft && lane < k)
+                aux.lse_draft[od + lane] = (n >= 0 && !greedy) ? static_cast<float>(Ld * kLn2D) : NAN;
         }
+    }
+    __syncthreads();
+    const int kind = sm.kind;
+    if (kind == kJobNone) return;
+    const int n = sm.n;
+    const int64_t trow = ot + n;
+
+    if (kind == kJobBonus) {
+        // --- bonus draw from p at position k, by block 0 of b --------------
+        if (s != 0 || warp != 0) return;
+        const int token = warp_draw_row<DT>(target, trow, ws.part + trow * g.n_sub, g, c, sm.M[k], sm.u);
+        if (lane == 0) out_tokens[trow] = token;
+        return;
     }
 
-    // outputs: prefix, the greedy token at n (sampled draws are written by
-    // select_kernel), -1 after; everything -1 on a data error
-    for (int i = lane; i <= k; i += 32) {
-        int32_t o = -1;
-        if (n >= 0) {
-            if (i < n) o = x;  // i < n <= 32, so i == lane: this lane's own token
-            else if (i == n && greedy) o = tok;
+    // --- 2. residual mass of this block's slice of sub-chunks -------------
+    const int64_t drow = od + n;
+    const float lth = sm.lth, ltl = sm.ltl, ldh = sm.ldh, ldl = sm.ldl;
+    const float2 c2 = make_float2(c, c), nlth2 = make_float2(-lth, -lth), nltl2 = make_float2(-ltl, -ltl);
+    const float2 nldh2 = make_float2(-ldh, -ldh), nldl2 = make_float2(-ldl, -ldl);
+    float *rp = ws.resid_part + static_cast<int64_t>(b) * g.n_sub;
+    const int per = (g.n_sub + nsplit - 1) / nsplit;
+    const int sc_begin = s * per;
+    const int sc_end = min(g.n_sub, (s + 1) * per);
+    if (warp == 0 && sc_begin < sc_end) {
+        // the slice of both rows goes to L2 in bulk (up to 32 KB per lane),
+        // so the warps' loads below wait on L2, not on DRAM round trips
+        int a0, a1, e0, e1;
+        sub_range(g, sc_begin, &a0, &e0);
+        sub_range(g, sc_end - 1, &a1, &e1);
+        const int64_t nbytes = static_cast<int64_t>(e1 - a0) * E::kBytes;
+        const unsigned char *t0 = static_cast<const unsigned char *>(target) + (trow * V + a0) * static_cast<int64_t>(E::kBytes);
+        const unsigned char *d0 = static_cast<const unsigned char *>(draft) + (drow * V + a0) * static_cast<int64_t>(E::kBytes);
+        constexpr int64_t kPiece = 32768;
+        for (int64_t off = static_cast<int64_t>(lane >> 1) * kPiece; off < nbytes; off += 16 * kPiece) {
+            const uint32_t len = static_cast<uint32_t>(min(kPiece, nbytes - off));
+            bulk_prefetch_l2(((lane & 1) ? d0 : t0) + off, len);
         }
-        out_tokens[ot + i] = o;
     }
-    if (lane == 0) {
-        out_num[b] = n;
-        ws.jobs[b] = job;
-        if (aux.residual_mass) aux.residual_mass[b] = NAN;
-    }
-    if (aux.accept_prob && lane < k) aux.accept_prob[od + lane] = (n >= 0 && !greedy) ? alpha_out : NAN;
-    if (aux.lse_target)
-        for (int i = lane; i <= k; i += 32) {
-            float v = NAN;
-            if (n >= 0 && !greedy) v = static_cast<float>(lse2(sm.M[i], sm.S[i]) * kLn2D);
-            aux.lse_target[ot + i] = v;
-        }
-    if (aux.lse_draft && lane < k)
-        aux.lse_draft[od + lane] = (n >= 0 && !greedy) ? static_cast<float>(Ld * kLn2D) : NAN;
-}
-
-// ================================================================== kernel 3
-// Residual mass max(0, p - q) per sub-chunk of the two rows at the rejected
-// position.  One warp per unit (list entry e, sub-chunk sc), grid-stride;
-// every lane issues its 8 16-byte loads before using them.
-template <int DT>
-__global__ void __launch_bounds__(256) resid_kernel(const void *__restrict__ target,
-                                                    const void *__restrict__ draft, Geometry g,
-                                                    WsPtrs ws) {
-    using E = Elem<DT>;
-    grid_dependency_wait();
-    grid_launch_dependents();
-    const int lane = lane_id();
-    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const int count = __ldcg(ws.counters + 0);
-    const int64_t total = static_cast<int64_t>(count) * g.n_sub;
-    for (int64_t u = gw; u < total; u += nw) {
-        const int e = static_cast<int>(u / g.n_sub);
-        const int sc = static_cast<int>(u - static_cast<int64_t>(e) * g.n_sub);
-        const RJob r = ws.rjobs[e];
-        int a, b;
-        sub_range(g, sc, &a, &b);
-        const int nvec = (b - a) / E::kPerVec;  // <= 128
+    for (int sc = sc_begin + warp; sc < sc_end; sc += blockDim.x >> 5) {
+        int a, e1;
+        sub_range(g, sc, &a, &e1);
+        const int nvec = (e1 - a) / E::kPerVec;  // <= 128
         const uint4 *pt = reinterpret_cast<const uint4 *>(static_cast<const unsigned char *>(target) +
-                                                          (r.trow * g.V + a) * static_cast<int64_t>(E::kBytes));
+                                                          (trow * V + a) * static_cast<int64_t>(E::kBytes));
         const uint4 *pd = reinterpret_cast<const uint4 *>(static_cast<const unsigned char *>(draft) +
-                                                          (r.drow * g.V + a) * static_cast<int64_t>(E::kBytes));
+                                                          (drow * V + a) * static_cast<int64_t>(E::kBytes));
         uint4 xt4[4], xd4[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -877,58 +983,46 @@ __global__ void __launch_bounds__(256) resid_kernel(const void *__restrict__ tar
                 xd4[j] = __ldg(pd + i);
             }
         }
-        float sum = 0.0f;
+        float2 acc0 = make_float2(0.0f, 0.0f), acc1 = acc0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             if (lane + 32 * j >= nvec) continue;
-            float xt[E::kPerVec], xd[E::kPerVec];
-            E::unpack(xt4[j], xt);
-            E::unpack(xd4[j], xd);
 #pragma unroll
-            for (int q = 0; q < E::kPerVec; ++q) sum += resid_weight(xt[q], xd[q], r.c, r.lth, r.ltl, r.ldh, r.ldl);
+            for (int p = 0; p < E::kPairs; ++p) {
+                const float2 w2 = resid_weight2(E::pair(xt4[j], p), E::pair(xd4[j], p), c2, nlth2, nltl2, nldh2, nldl2);
+                if (p & 1) acc1 = fadd2(acc1, w2); else acc0 = fadd2(acc0, w2);
+            }
         }
-        sum = warp_sum_f(sum);
-        if (lane == 0) ws.resid_part[u] = sum;  // u = e * n_sub + sc
+        const float sum = warp_sum_f((acc0.x + acc0.y) + (acc1.x + acc1.y));
+        if (lane == 0) rp[sc] = sum;
     }
-}
+    // arrival, one per warp (no block barrier): the warp that arrives last,
+    // of all nsplit * 8 warps of b, draws
+    // (acquire-release add: this warp's masses are released with it, and
+    // the last warp acquires everyone's)
+    bool last = false;
+    if (lane == 0)
+        last = atomic_add_acq_rel_gpu(ws.seqcnt + b, 1) == nsplit * static_cast<int>(blockDim.x >> 5) - 1;
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __syncwarp();  // lane 0's acquire, before the other lanes' reads
 
-// ================================================================== kernel 4
-// One warp per sequence: the residual draw (locate the sub-chunk from the
-// residual masses, scan its elements) or the bonus draw.
-template <int DT>
-__global__ void __launch_bounds__(256) select_kernel(const void *__restrict__ target,
-                                                     const void *__restrict__ draft, int B, Geometry g,
-                                                     WsPtrs ws, int32_t *__restrict__ out_tokens,
-                                                     spec_verify_aux_t aux) {
-    using E = Elem<DT>;
-    grid_dependency_wait();
-    grid_launch_dependents();
-    const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (b >= B) return;
-    const int lane = lane_id();
-    const SeqJob job = ws.jobs[b];
-    if (job.kind == kJobNone) return;
-    int token;
-    if (job.kind == kJobBonus) {
-        token = warp_draw_row<DT>(target, job.trow, ws.part + job.trow * g.n_sub, g, job.c, job.M, job.u);
-    } else {
-        const RJob r = ws.rjobs[job.list_idx];
-        const float *pr = ws.resid_part + static_cast<int64_t>(job.list_idx) * g.n_sub;
-        auto wsub = [&](int i) -> float { return __ldcg(pr + i); };
-        double before, Z, tgt;
-        const int sc = warp_locate(g.n_sub, wsub, job.u, &before, &Z, &tgt);
-        token = -1;
-        if (sc >= 0) {
-            int a, e1;
-            sub_range(g, sc, &a, &e1);
-            const void *rt = static_cast<const unsigned char *>(target) + r.trow * g.V * static_cast<int64_t>(E::kBytes);
-            const void *rd = static_cast<const unsigned char *>(draft) + r.drow * g.V * static_cast<int64_t>(E::kBytes);
-            auto W = [&](float zt, float zd) -> float { return resid_weight(zt, zd, r.c, r.lth, r.ltl, r.ldh, r.ldl); };
-            token = warp_scan_elems<DT>(rt, rd, a, e1, W, before, tgt);
-        }
-        if (lane == 0 && aux.residual_mass) aux.residual_mass[b] = static_cast<float>(Z);
+    // --- 3. the residual draw, by the last warp of b -----------------------
+    auto wsub = [&](int i) -> float { return __ldcg(rp + i); };
+    double before, Z, tgt;
+    const int sc = warp_locate(g.n_sub, wsub, sm.u, &before, &Z, &tgt);
+    int token = -1;
+    if (sc >= 0) {
+        int a, e1;
+        sub_range(g, sc, &a, &e1);
+        const void *rt = static_cast<const unsigned char *>(target) + trow * V * static_cast<int64_t>(E::kBytes);
+        const void *rd = static_cast<const unsigned char *>(draft) + drow * V * static_cast<int64_t>(E::kBytes);
+        auto W = [&](float a1, float a2) -> float { return resid_weight(a1, a2, c, lth, ltl, ldh, ldl); };
+        token = warp_scan_elems<DT>(rt, rd, a, e1, W, before, tgt);
     }
-    if (lane == 0) out_tokens[job.trow] = token;
+    if (lane == 0) {
+        out_tokens[trow] = token;
+        if (aux.residual_mass) aux.residual_mass[b] = static_cast<float>(Z);
+    }
 }
 
 // Draft-side draw: one warp per draft row (grid-stride over rows).
@@ -954,7 +1048,7 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
     grid_dependency_wait();
     grid_launch_dependents();
     if (s_bad) {
-        if (blockIdx.x == 0 && threadIdx.x == 0) set_status(counters + 1, SPEC_ERR_INVALID_ARG);
+        if (blockIdx.x == 0 && threadIdx.x == 0) set_status(counters + kStatus, SPEC_ERR_INVALID_ARG);
         return;
     }
     const int R = s_kofs[B];
@@ -1013,12 +1107,13 @@ bool make_geometry(int V, int dtype, Geometry *g) {
 }
 
 struct WsLayout {
-    size_t part, jobs, rjobs, counters, resid, total;
+    size_t part, counters, seqcnt, resid, total;
 };
 
 // Workspace layout.  The counters block comes first so that the status word
 // has a fixed offset (kStatusOffset) whatever B and V are.
-constexpr size_t kStatusOffset = sizeof(int);  // counters[1]
+constexpr size_t kStatusOffset = sizeof(int) * kStatus;
+constexpr size_t kTicketOffset = sizeof(int) * kTicket;  // the ticket words up to kCounterWords
 constexpr size_t kCountersBytes = 256;
 
 WsLayout ws_layout(int B, const Geometry &g) {
@@ -1029,10 +1124,8 @@ WsLayout ws_layout(int B, const Geometry &g) {
     off = align_up(off + kCountersBytes, 256);
     l.part = off;
     off = align_up(off + rows_cap * g.n_sub * sizeof(float2), 256);
-    l.jobs = off;
-    off = align_up(off + B * sizeof(SeqJob), 256);
-    l.rjobs = off;
-    off = align_up(off + B * sizeof(RJob), 256);
+    l.seqcnt = off;
+    off = align_up(off + B * sizeof(int), 256);
     l.resid = off;
     off = align_up(off + static_cast<size_t>(B) * g.n_sub * sizeof(float), 256);
     l.total = off;
@@ -1043,9 +1136,8 @@ WsPtrs ws_ptrs(void *base, const WsLayout &l) {
     unsigned char *p = static_cast<unsigned char *>(base);
     WsPtrs w;
     w.part = reinterpret_cast<float2 *>(p + l.part);
-    w.jobs = reinterpret_cast<SeqJob *>(p + l.jobs);
-    w.rjobs = reinterpret_cast<RJob *>(p + l.rjobs);
     w.counters = reinterpret_cast<int *>(p + l.counters);
+    w.seqcnt = reinterpret_cast<int *>(p + l.seqcnt);
     w.resid_part = reinterpret_cast<float *>(p + l.resid);
     return w;
 }
@@ -1103,14 +1195,15 @@ size_t stats_smem(int ns, int B) {
 }
 
 // Ring depth and CTAs per SM of stats_kernel: the preferred shape
-// (SPEC_STATS_CTAS_PER_SM CTAs with SPEC_STATS_SLOTS slots each; three CTAs
-// of four 16 KB slots give 24 consumer warps and 192 KB in flight per SM)
-// if the tables fit beside it, else two CTAs with up to kMaxSlots, else one.
+// (SPEC_STATS_CTAS_PER_SM CTAs with SPEC_STATS_SLOTS slots each; four CTAs
+// of three 16 KB slots give 32 consumer warps and 192 KB in flight per SM,
+// measured a little faster than three CTAs of four slots) if the tables fit
+// beside it, else two CTAs with up to kMaxSlots, else one.
 #ifndef SPEC_STATS_CTAS_PER_SM
-#define SPEC_STATS_CTAS_PER_SM 3
+#define SPEC_STATS_CTAS_PER_SM 4
 #endif
 #ifndef SPEC_STATS_SLOTS
-#define SPEC_STATS_SLOTS 4
+#define SPEC_STATS_SLOTS 3
 #endif
 void pick_ring(const DeviceState &st, int B, int *ns, size_t *smem, int *ctas_per_sm) {
     struct Opt {
@@ -1152,6 +1245,15 @@ void *get_internal_ws(DeviceState &st, size_t need) {
     return p;
 }
 
+// A caller-owned workspace may hold anything: zero its unit-ticket words on
+// the stream before the call's first kernel.  (The library-owned workspaces
+// are zeroed when allocated; stats_kernel leaves the words at zero.)
+bool reset_tickets(void *ws, cudaStream_t stream) {
+    return cuda_ok(cudaMemsetAsync(static_cast<unsigned char *>(ws) + kTicketOffset, 0,
+                                   (kCounterWords - kTicket) * sizeof(int), stream),
+                   "cudaMemsetAsync(workspace tickets)");
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_common(int B, int V, int dtype) {
@@ -1184,6 +1286,15 @@ cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, 
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+#ifndef SPEC_RESOLVE_BLOCKS_PER_SM
+#define SPEC_RESOLVE_BLOCKS_PER_SM 8
+#endif
+// resolve_kernel blocks per sequence for n sequences on an idle GPU:
+// 1..kSub, as many as fit one wave of SPEC_RESOLVE_BLOCKS_PER_SM per SM.
+int resolve_split(const DeviceState &st, const Geometry &g, int n) {
+    return std::max(1, std::min({kSub, g.n_sub, (SPEC_RESOLVE_BLOCKS_PER_SM * st.sms) / std::max(n, 1)}));
+}
+
 template <int DT>
 int launch_verify(const void *target, const void *draft, const int32_t *tokens, const float *u_accept,
                   const float *u_resample, const float *temperature, int B, const int32_t *k_offsets,
@@ -1195,17 +1306,13 @@ int launch_verify(const void *target, const void *draft, const int32_t *tokens, 
     if (ns == 0) return SPEC_ERR_INVALID_ARG;
     const WsPtrs w = ws_ptrs(ws_base, l);
     const int grid = st.sms * per_sm;
+    const int nsplit = resolve_split(st, g, B);
     if (!cuda_ok(launch_k(false, stats_kernel<DT, false>, dim3(grid), dim3(kThreads), smem, stream, target, draft,
-                            temperature, k_offsets, B, g, ns, w.part, w.counters),
+                          temperature, k_offsets, B, g, ns, w.part, w.counters, w.seqcnt),
                  "launch stats_kernel") ||
-        !cuda_ok(launch_k(true, decide_kernel<DT>, dim3(B), dim3(256), 0, stream, target, draft, tokens,
-                            u_accept, u_resample, temperature, k_offsets, B, g, w, out_tokens, out_num, aux),
-                 "launch decide_kernel") ||
-        !cuda_ok(launch_k(true, resid_kernel<DT>, dim3(st.sms * 8), dim3(256), 0, stream, target, draft, g, w),
-                 "launch resid_kernel") ||
-        !cuda_ok(launch_k(true, select_kernel<DT>, dim3((B + 7) / 8), dim3(256), 0, stream, target, draft, B, g,
-                            w, out_tokens, aux),
-                 "launch select_kernel"))
+        !cuda_ok(launch_k(true, resolve_kernel<DT>, dim3(B * nsplit), dim3(256), 0, stream, target, draft, tokens,
+                          u_accept, u_resample, temperature, k_offsets, B, g, nsplit, w, out_tokens, out_num, aux),
+                 "launch resolve_kernel"))
         return SPEC_ERR_CUDA;
     return SPEC_OK;
 }
@@ -1222,7 +1329,7 @@ int launch_draft(const void *draft, const float *temperature, const float *u_dra
     // one warp per draft row: at most B * kMaxK rows, 8 warps per block
     const int grid = static_cast<int>(std::min(static_cast<int64_t>(st.sms) * 8, (static_cast<int64_t>(B) * kMaxK + 7) / 8));
     if (!cuda_ok(launch_k(false, stats_kernel<DT, true>, dim3(st.sms * per_sm), dim3(kThreads), smem, stream, draft,
-                          draft, temperature, k_offsets, B, g, ns, w.part, w.counters),
+                          draft, temperature, k_offsets, B, g, ns, w.part, w.counters, nullptr),
                  "launch stats_kernel") ||
         !cuda_ok(launch_k(true, draft_select_kernel<DT>, dim3(std::max(grid, 1)), dim3(256),
                           (B + 1) * sizeof(int), stream, draft, temperature, u_draft, k_offsets, B, g,
@@ -1266,6 +1373,7 @@ int spec_verify_ex(const void *target_logits, const void *draft_logits, const in
     if (ws) {
         if (workspace_bytes < l.total) return SPEC_ERR_WORKSPACE;
         if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SPEC_ERR_ALIGNMENT;
+        if (!reset_tickets(ws, static_cast<cudaStream_t>(stream))) return SPEC_ERR_CUDA;
     } else {
         ws = get_internal_ws(*st, l.total);
         if (!ws) return SPEC_ERR_CUDA;
@@ -1307,6 +1415,7 @@ int spec_draft_sample_ex(const void *draft_logits, const float *temperature, con
     if (ws) {
         if (workspace_bytes < l.total) return SPEC_ERR_WORKSPACE;
         if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SPEC_ERR_ALIGNMENT;
+        if (!reset_tickets(ws, static_cast<cudaStream_t>(stream))) return SPEC_ERR_CUDA;
     } else {
         ws = get_internal_ws(*st, l.total);
         if (!ws) return SPEC_ERR_CUDA;
@@ -1496,10 +1605,13 @@ int spec_verify_noalloc(const void *target_logits, const void *draft_logits, con
         ws = g_noalloc_addr[dev];
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the array keeps the previous call's contents: the status word is the
-    // only field that must start at zero (the kernels reset their counters)
-    if (!cuda_ok(cudaMemsetAsync(static_cast<unsigned char *>(ws) + kStatusOffset, 0, sizeof(int), s),
-                 "cudaMemsetAsync(noalloc status)"))
+    // the array keeps the previous call's contents: the status word must
+    // start at zero; the unit-ticket words, which stats_kernel leaves at
+    // zero, are cleared by the same memset at no extra cost; the
+    // per-sequence counters are reset by stats_kernel
+    if (!cuda_ok(cudaMemsetAsync(static_cast<unsigned char *>(ws) + kStatusOffset, 0,
+                                 (kCounterWords - kStatus) * sizeof(int), s),
+                 "cudaMemsetAsync(noalloc status and tickets)"))
         return SPEC_ERR_CUDA;
     const spec_verify_aux_t a{};
     if (dtype == SPEC_F32)
