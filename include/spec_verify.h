@@ -177,7 +177,7 @@ int spec_round_host(const void *target_logits_host, const void *draft_logits_hos
  * fixed array inside the library (SPEC_NOALLOC_SCRATCH_BYTES, held on every
  * GPU that loads the library until the process exits), so the call performs
  * no cudaMalloc, cudaFree or other allocation.
- *   - A call whose scratch need, spec_workspace_bytes(B, V, dtype), exceeds
+ *   - A call whose scratch need, spec_noalloc_bytes(B, V, dtype), exceeds
  *     SPEC_NOALLOC_SCRATCH_BYTES is rejected with SPEC_ERR_WORKSPACE before
  *     anything is launched (spec_last_error() names the sizes).  The limit
  *     covers, e.g., B = 512 at V = 152064 in bf16.
@@ -202,6 +202,12 @@ int spec_verify_noalloc(const void *target_logits, const void *draft_logits,
 /* Bytes of device workspace needed by spec_verify_ex / spec_draft_sample_ex
  * for a call with B sequences over vocabulary V (0 for invalid arguments). */
 size_t spec_workspace_bytes(int B, int V, int dtype);
+
+/* Bytes of the fixed scratch array a spec_verify_noalloc call with B
+ * sequences over vocabulary V uses (0 for invalid arguments; the same as
+ * spec_workspace_bytes, as both run the same kernels); the call is refused
+ * when this exceeds SPEC_NOALLOC_SCRATCH_BYTES.  Host only. */
+size_t spec_noalloc_bytes(int B, int V, int dtype);
 
 /*
  * Device status word of a workspace (NULL: the library-owned one of the

@@ -22,6 +22,7 @@ from ._binding import (  # noqa: F401
     exported_symbols,
     lib,
     lib_path,
+    noalloc_bytes,
     spec_draft_sample,
     spec_round_host,
     spec_verify,

@@ -16,7 +16,8 @@ SPEC_ERRORS = {0: "SPEC_OK", -1: "SPEC_ERR_INVALID_ARG", -2: "SPEC_ERR_ALIGNMENT
 # every symbol include/spec_verify.h declares
 EXPORTS = ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",
            "spec_round_host", "spec_workspace_bytes", "spec_workspace_status",
-           "spec_status_string", "spec_abi_version", "spec_last_error", "spec_verify_noalloc")
+           "spec_status_string", "spec_abi_version", "spec_last_error", "spec_verify_noalloc",
+           "spec_noalloc_bytes")
 
 
 class SpecError(RuntimeError):
@@ -56,6 +57,8 @@ def lib():
     L.spec_round_host.argtypes = [vp, vp, vp, vp, vp, vp, ip, vp, ip, ip, vp, vp, vp, vp]
     L.spec_workspace_bytes.argtypes = [ip, ip, ip]
     L.spec_workspace_bytes.restype = sz
+    L.spec_noalloc_bytes.argtypes = [ip, ip, ip]
+    L.spec_noalloc_bytes.restype = sz
     L.spec_workspace_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int), ip]
     L.spec_status_string.argtypes = [ip]
     L.spec_status_string.restype = ctypes.c_char_p
@@ -221,6 +224,11 @@ def spec_round_host(target_logits, draft_logits, u_draft, u_accept, u_resample, 
 
 def workspace_bytes(B: int, V: int, dtype: int) -> int:
     return int(lib().spec_workspace_bytes(B, V, dtype))
+
+
+def noalloc_bytes(B: int, V: int, dtype: int) -> int:
+    """Scratch a spec_verify_noalloc call uses (refused above MAX_NOALLOC_SCRATCH)."""
+    return int(lib().spec_noalloc_bytes(B, V, dtype))
 
 
 def workspace_status(workspace=None, clear: bool = False) -> int:

@@ -1352,6 +1352,8 @@ size_t spec_workspace_bytes(int B, int V, int dtype) {
     return ws_layout(std::max(B, 1), g).total;
 }
 
+size_t spec_noalloc_bytes(int B, int V, int dtype) { return spec_workspace_bytes(B, V, dtype); }
+
 int spec_verify_ex(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
                    const float *u_accept, const float *u_resample, const float *temperature, int B,
                    const int32_t *k_offsets, int V, int dtype, int32_t *out_tokens, int32_t *out_num_accepted,

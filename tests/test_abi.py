@@ -57,6 +57,8 @@ def test_workspace_bytes_host_only(lib):
     a = sv.workspace_bytes(512, 128256, sv.BF16)
     b = sv.workspace_bytes(64, 128256, sv.BF16)
     assert a > b > 0 and a % 256 == 0
+    assert sv.noalloc_bytes(512, 128256, sv.BF16) == a   # the same kernels, the same scratch
+    assert sv.noalloc_bytes(4, 1001, sv.BF16) == 0
     assert sv.workspace_bytes(4, 1001, sv.BF16) == 0      # V * 2 not a multiple of 16
     assert sv.workspace_bytes(-1, 1000, sv.F32) == 0
     assert sv.workspace_bytes(4, 1000, 7) == 0

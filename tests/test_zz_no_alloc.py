@@ -87,10 +87,10 @@ def test_noalloc_matches_spec_verify_twice(sv, case):
 def test_noalloc_refuses_batches_beyond_the_array(sv):
     limit = 48 << 20
     V = 262144  # bf16: a large vocabulary; B = 4096 needs far more scratch than the array
-    assert sv.workspace_bytes(4096, V, sv.BF16) > limit
+    assert sv.noalloc_bytes(4096, V, sv.BF16) > limit
     fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the size check comes first
     rc = sv.lib().spec_verify_noalloc(fake, fake, fake, fake, fake, fake, 4096, fake, V, sv.BF16,
                                       fake, fake, None)
     assert rc == -5  # SPEC_ERR_WORKSPACE
     assert b"scratch" in sv.lib().spec_last_error()
-    assert sv.workspace_bytes(512, 152064, sv.BF16) <= limit
+    assert sv.noalloc_bytes(512, 152064, sv.BF16) <= limit
