@@ -53,6 +53,38 @@ def parse():
     return ap.parse_args()
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "spec_verify_traffic_B512_ragged_k1to10_V128256_bf16.txt")
+
+
+def kernel_source_hash() -> str:
+    """sha256 over the CUDA sources (file names and contents, sorted)."""
+    import hashlib
+    d = os.path.join(ROOT, "speculative_decoding_verification_61_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh")):
+            h.update(name.encode())
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per spec_verify call from the committed ncu summary, if it
+    was taken on this workload with the current kernel sources; else None."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    kv = {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            if "=" in line and not line.lstrip().startswith("#"):
+                k, v = line.split("=", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("workload") != workload or kv.get("csrc_sha256") != kernel_source_hash():
+        return None
+    return int(kv["traffic_bytes_per_call"])
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -372,7 +404,9 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "spec_verify (all its launches)",
                      "achieved": verify_gbs, "peak": peak, "unit": "GB/s",
                      "frac": verify_gbs / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
-                     "traffic": None, "algorithmic_bytes_per_launch": ab["verify"]},
+                     "traffic": measured_traffic(w.name), "algorithmic_bytes_per_launch": ab["verify"],
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the call's kernels "
+                                       "(profiles/, null unless taken with the current kernel sources)"},
         "gpu_launches": 6 * args.steps,
         "cpu_baseline": cpu,
         "e2e": e2e_line,
