@@ -56,16 +56,19 @@ def parse():
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "spec_verify_traffic_B512_ragged_k1to10_V128256_bf16.txt")
 
 
+# the sources of the kernels a spec_verify call launches
+VERIFY_SOURCES = ("spec_verify.cu", "device_utils.cuh")
+
+
 def kernel_source_hash() -> str:
-    """sha256 over the CUDA sources (file names and contents, sorted)."""
+    """sha256 over the sources of spec_verify's kernels (names and contents)."""
     import hashlib
     d = os.path.join(ROOT, "speculative_decoding_verification_61_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh")):
-            h.update(name.encode())
-            with open(os.path.join(d, name), "rb") as f:
-                h.update(f.read())
+    for name in VERIFY_SOURCES:
+        h.update(name.encode())
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()
 
 
@@ -223,6 +226,27 @@ class _Null:
         return False
 
 
+def adaptive_k_timing(torch, sv, dev, B=4096, reps=1000):
+    """Device time of one adaptive-k update (spec_adapt_update) for B
+    sequences, the round-to-round step of a serving loop."""
+    import numpy as np
+    ctl = sv.AdaptiveK(B, 1, 10, device=dev)
+    rng = np.random.default_rng(7)
+    counts = [torch.from_numpy(rng.integers(0, 6, size=B).astype(np.int32)).to(dev) for _ in range(8)]
+    for i in range(20):
+        ctl.update(counts[i % 8])
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(reps):
+        ctl.update(counts[i % 8])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return {"B": B, "update_us": 1000.0 * e0.elapsed_time(e1) / reps, "launches_per_update": 1,
+            "kernel": "update_kernel (one block; history update, exact mean test, k_offsets scan)"}
+
+
 def e2e(w, steps, torch, sv):
     """Through the public host-buffer entry point: H2D of the step's inputs
     from pinned memory, draft sample + verify, D2H of the results."""
@@ -371,6 +395,8 @@ def main():
             "verify_bytes": abc["verify"], "mean_accepted": mc["mean_accepted"]}
         del wc
 
+    adapt = adaptive_k_timing(torch, sv, dev) if rank == 0 else None
+
     e2e_line = None
     if rank == 0 and args.e2e_steps > 0:
         ms, h2d, d2h = e2e(w, args.e2e_steps, torch, sv)
@@ -407,11 +433,13 @@ def main():
                      "traffic": measured_traffic(w.name), "algorithmic_bytes_per_launch": ab["verify"],
                      "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the call's kernels "
                                        "(profiles/, null unless taken with the current kernel sources)"},
-        "gpu_launches": 6 * args.steps,
+        # per step: stats_kernel + draft_select_kernel, stats_kernel + resolve_kernel
+        "gpu_launches": 4 * args.steps,
         "cpu_baseline": cpu,
         "e2e": e2e_line,
         "clocks": clocks,
         "other_workloads": extra,
+        "adaptive_k": adapt,
     }
     print(json.dumps(line))
     if world > 1:

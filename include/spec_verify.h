@@ -199,6 +199,36 @@ int spec_verify_noalloc(const void *target_logits, const void *draft_logits,
                         const int32_t *k_offsets, int V, int dtype, int32_t *out_tokens,
                         int32_t *out_num_accepted, void *stream);
 
+/*
+ * Adaptive draft length (sxl-space.tk "【大模型】- 推测解码", 自适应推测解码:
+ * AdaptiveSpeculativeDecoder.adapt_k), per sequence and on the device.
+ *
+ * After each round the sequence's acceptance rate n_b / k_b (accepted drafted
+ * tokens over the round's draft length) joins its history; once the history
+ * holds 10 rates, a mean of the last 10 above 0.8 lengthens the next round's
+ * draft by one (at most max_k), below 0.5 shortens it by one (at least
+ * min_k).  The first length is (min_k + max_k) / 2, rounded down.  The mean
+ * is compared exactly (rates are rationals with denominators <= 32), so a
+ * mean of exactly 0.8 or 0.5 changes nothing.  A sequence whose round
+ * carries no rate (num_accepted < 0, a draft length of 0, or num_accepted
+ * greater than its length) keeps its state.
+ *
+ *   state          device buffer of spec_adapt_state_bytes(B) bytes, 8-byte
+ *                  aligned, owned by the caller; spec_adapt_init fills it.
+ *   num_accepted   [B] int32, device: out_num_accepted of the round just
+ *                  verified, which must have used the lengths of the last
+ *                  k_offsets_out this state produced.
+ *   k_offsets_out  [B+1] int32, device: the next round's k_offsets.
+ *   min_k, max_k   1 <= min_k <= max_k <= SPEC_MAX_K (the pages use 1, 10).
+ * Both calls are asynchronous on `stream` (one single-block kernel each) and
+ * return only host-checkable errors: SPEC_ERR_INVALID_ARG (null pointers,
+ * B outside 1..SPEC_MAX_B, bad bounds), SPEC_ERR_ALIGNMENT, SPEC_ERR_CUDA.
+ */
+size_t spec_adapt_state_bytes(int B);
+int spec_adapt_init(void *state, int B, int min_k, int max_k, int32_t *k_offsets_out, void *stream);
+int spec_adapt_update(void *state, const int32_t *num_accepted, int B, int min_k, int max_k,
+                      int32_t *k_offsets_out, void *stream);
+
 /* Bytes of device workspace needed by spec_verify_ex / spec_draft_sample_ex
  * for a call with B sequences over vocabulary V (0 for invalid arguments). */
 size_t spec_workspace_bytes(int B, int V, int dtype);

@@ -12,6 +12,7 @@ from __future__ import annotations
 
 from ._binding import (  # noqa: F401
     ABI_VERSION,
+    AdaptiveK,
     BF16,
     F32,
     MAX_B,

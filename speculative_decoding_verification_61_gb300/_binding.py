@@ -17,7 +17,7 @@ SPEC_ERRORS = {0: "SPEC_OK", -1: "SPEC_ERR_INVALID_ARG", -2: "SPEC_ERR_ALIGNMENT
 EXPORTS = ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",
            "spec_round_host", "spec_workspace_bytes", "spec_workspace_status",
            "spec_status_string", "spec_abi_version", "spec_last_error", "spec_verify_noalloc",
-           "spec_noalloc_bytes")
+           "spec_noalloc_bytes", "spec_adapt_state_bytes", "spec_adapt_init", "spec_adapt_update")
 
 
 class SpecError(RuntimeError):
@@ -67,6 +67,12 @@ def lib():
     L.spec_verify_noalloc.restype = ip
     L.spec_last_error.argtypes = []
     L.spec_last_error.restype = ctypes.c_char_p
+    L.spec_adapt_state_bytes.argtypes = [ip]
+    L.spec_adapt_state_bytes.restype = sz
+    L.spec_adapt_init.argtypes = [vp, ip, ip, ip, vp, vp]
+    L.spec_adapt_init.restype = ip
+    L.spec_adapt_update.argtypes = [vp, vp, ip, ip, ip, vp, vp]
+    L.spec_adapt_update.restype = ip
     for name in ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",
                  "spec_round_host", "spec_workspace_status", "spec_abi_version"):
         getattr(L, name).restype = ip
@@ -265,3 +271,29 @@ def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, u_accept, u_r
                                    _p(out_tokens), _p(out_num_accepted), _stream(stream))
     _raise(rc, "spec_verify_noalloc")
     return out_tokens, out_num_accepted
+
+
+class AdaptiveK:
+    """Device-side adaptive draft length for a batch of B sequences (the
+    spec_adapt_* entry points): holds the state buffer and the next round's
+    k_offsets on the device."""
+
+    def __init__(self, B: int, min_k: int = 1, max_k: int = 10, device="cuda", stream=None):
+        import torch
+        nbytes = int(lib().spec_adapt_state_bytes(B))
+        if nbytes == 0:
+            raise SpecError(-1, "spec_adapt_state_bytes")
+        self.B, self.min_k, self.max_k = B, min_k, max_k
+        self.state = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.k_offsets = torch.empty(B + 1, dtype=torch.int32, device=device)
+        _raise(lib().spec_adapt_init(_p(self.state), B, min_k, max_k, _p(self.k_offsets), _stream(stream)),
+               "spec_adapt_init")
+
+    def update(self, num_accepted, stream=None):
+        """Feed one round's out_num_accepted ([B] int32, device); returns the
+        next round's k_offsets ([B+1] int32, device, updated in place)."""
+        import torch
+        _check_dev("num_accepted", num_accepted, torch.int32)
+        _raise(lib().spec_adapt_update(_p(self.state), _p(num_accepted), self.B, self.min_k, self.max_k,
+                                       _p(self.k_offsets), _stream(stream)), "spec_adapt_update")
+        return self.k_offsets

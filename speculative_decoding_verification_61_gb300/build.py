@@ -1,8 +1,9 @@
 """Build the sm_103a CUDA library in-tree:
 speculative_decoding_verification_61_gb300/_build/libspecverify.so
 
-One translation unit, one -gencode (sm_103a), static CUDA runtime, so the
-shared object loads with plain ctypes and needs no GPU at load time.
+Two translation units (the verify step and the adaptive-k controller), one
+-gencode (sm_103a), static CUDA runtime, so the shared object loads with
+plain ctypes and needs no GPU at load time.
 """
 from __future__ import annotations
 
@@ -17,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libspecverify.so")
-SOURCES = [os.path.join(CSRC, "spec_verify.cu")]
+SOURCES = [os.path.join(CSRC, "spec_verify.cu"), os.path.join(CSRC, "adapt_k.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "device_utils.cuh"), os.path.join(INCLUDE, "spec_verify.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
