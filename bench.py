@@ -1,15 +1,18 @@
 #!/usr/bin/env python
 """Benchmark of the speculative-decoding sampling round on one GB300.
 
-One step = spec_draft_sample (draft-side softmax + multinomial over every
-draft row) + spec_verify (softmax of every target/draft row, accept test,
-first rejection, residual or bonus draw) on the ragged adaptive-k batch
-(B = 512 sequences, k_b uniform in 1..10, V = 128256, bf16 logits, T = 1).
-Inputs are resident in HBM and larger than L2 (no flush needed).
+One step = spec_draft_sample_lse (draft-side softmax + multinomial over
+every draft row, keeping each row's normaliser) + spec_verify_lse (softmax
+of every target row, accept test, first rejection, residual or bonus draw,
+with the draft rows' normalisers from the first call) on the ragged
+adaptive-k batch (B = 512 sequences, k_b uniform in 1..10, V = 128256,
+bf16 logits, T = 1).  Inputs are resident in HBM and larger than L2 (no
+flush needed).  The standalone spec_verify (which streams the draft rows
+again) is timed on the same batch beside it.
 
 metric: verified logit rows/s (R_t + R_d rows per step) and achieved HBM
-GB/s of algorithmic bytes (every needed row once, plus one row-equivalent
-per sampled sequence for the resample, plus the draft-sampling pass).
+GB/s of algorithmic bytes (every logit row once, plus one row-equivalent
+per sampled sequence for the resample).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -53,10 +56,10 @@ def parse():
     return ap.parse_args()
 
 
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "spec_verify_traffic_B512_ragged_k1to10_V128256_bf16.txt")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "spec_verify_lse_traffic_B512_ragged_k1to10_V128256_bf16.txt")
 
 
-# the sources of the kernels a spec_verify call launches
+# the sources of the kernels a verify call launches
 VERIFY_SOURCES = ("spec_verify.cu", "device_utils.cuh")
 
 
@@ -73,8 +76,8 @@ def kernel_source_hash() -> str:
 
 
 def measured_traffic(workload: str):
-    """DRAM bytes per spec_verify call from the committed ncu summary, if it
-    was taken on this workload with the current kernel sources; else None."""
+    """DRAM bytes per spec_verify_lse call from the committed ncu summary, if
+    it was taken on this workload with the current kernel sources; else None."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     kv = {}
@@ -172,22 +175,35 @@ def to_device(w, torch, dev):
                 ud=t(w.u_draft), T=t(w.temperature), ko=t(w.k_offsets))
 
 
-def measure(w, steps, warmup, torch, sv, dev, sampler=None, barrier=None):
+def measure(w, steps, warmup, torch, sv, dev, sampler=None, barrier=None, fused=True):
     """Device-resident timing of draft sample + verify with CUDA events on
-    the launching stream.  Returns per-step, per-call times (ms)."""
+    the launching stream.  fused: spec_draft_sample_lse + spec_verify_lse
+    (each row read once); else spec_draft_sample + spec_verify.  Returns
+    per-step, per-call times (ms)."""
     d = to_device(w, torch, dev)
     toks = torch.empty(w.rows_draft, dtype=torch.int32, device=dev)
+    lse2 = torch.empty(max(w.rows_draft, 1), dtype=torch.float64, device=dev)
     out_t = torch.empty(w.rows_target, dtype=torch.int32, device=dev)
     out_n = torch.empty(w.B, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
-        sv.spec_draft_sample(d["dl"], d["T"], d["ud"], d["ko"], out_draft_tokens=toks)
-        sv.spec_verify(d["tl"], d["dl"], toks, d["ua"], d["ur"], d["T"], d["ko"], out_tokens=out_t,
-                       out_num_accepted=out_n)
+    def draft():
+        if fused:
+            sv.spec_draft_sample_lse(d["dl"], d["T"], d["ud"], d["ko"], out_draft_tokens=toks, out_draft_lse2=lse2)
+        else:
+            sv.spec_draft_sample(d["dl"], d["T"], d["ud"], d["ko"], out_draft_tokens=toks)
+
+    def verify():
+        if fused:
+            sv.spec_verify_lse(d["tl"], d["dl"], lse2, toks, d["ua"], d["ur"], d["T"], d["ko"], out_tokens=out_t,
+                               out_num_accepted=out_n)
+        else:
+            sv.spec_verify(d["tl"], d["dl"], toks, d["ua"], d["ur"], d["T"], d["ko"], out_tokens=out_t,
+                           out_num_accepted=out_n)
 
     for _ in range(max(3, warmup)):
-        step()
+        draft()
+        verify()
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -200,10 +216,9 @@ def measure(w, steps, warmup, torch, sv, dev, sampler=None, barrier=None):
         for i in range(steps):
             e = ev[i]
             e[0].record(stream)
-            sv.spec_draft_sample(d["dl"], d["T"], d["ud"], d["ko"], out_draft_tokens=toks)
+            draft()
             e[1].record(stream)
-            sv.spec_verify(d["tl"], d["dl"], toks, d["ua"], d["ur"], d["T"], d["ko"], out_tokens=out_t,
-                           out_num_accepted=out_n)
+            verify()
             e[2].record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
@@ -369,7 +384,7 @@ def main():
     w = workloads.make_config(args.config)
     ab = workloads.algorithmic_bytes(w)
     sampler = ClockSampler(local, enabled=(rank == 0 and not args.no_clocks))
-    m = measure(w, args.steps, args.warmup, torch, sv, dev, sampler=sampler, barrier=barrier)
+    m = measure(w, args.steps, args.warmup, torch, sv, dev, sampler=sampler, barrier=barrier, fused=True)
     step_ms = m["step_ms"]
     if world > 1:
         import torch.distributed as dist
@@ -378,21 +393,33 @@ def main():
         step_ms = float(t.item())
     rows = w.rows_target + w.rows_draft
     value = world * rows / (step_ms * 1e-3)
-    step_bytes = ab["verify"] + ab["draft_sample"]
-    verify_gbs = ab["verify"] / (m["verify_ms"] * 1e-3) / 1e9
-    draft_gbs = ab["draft_sample"] / (m["draft_ms"] * 1e-3) / 1e9
+    step_bytes = ab["verify_lse"] + ab["draft_sample"]
+    gbs = lambda nbytes, ms: nbytes / (ms * 1e-3) / 1e9  # noqa: E731
+    verify_lse_gbs = gbs(ab["verify_lse"], m["verify_ms"])
+    draft_gbs = gbs(ab["draft_sample"], m["draft_ms"])
+
+    # the separate calls on the same batch: spec_verify streams the draft rows again
+    sep = measure(w, max(50, args.steps // 4), args.warmup, torch, sv, dev, fused=False) if rank == 0 else None
 
     extra = {}
     for c in [int(x) for x in args.extra_configs.split(",") if x.strip()] if rank == 0 else []:
         wc = workloads.make_config(c)
         abc = workloads.algorithmic_bytes(wc)
-        mc = measure(wc, max(50, args.steps // 4), args.warmup, torch, sv, dev)
+        reps = max(50, args.steps // 4)
+        mc = measure(wc, reps, args.warmup, torch, sv, dev, fused=False)
+        mf = measure(wc, reps, args.warmup, torch, sv, dev, fused=True)
         extra[wc.name] = {
             "verify_ms": round(mc["verify_ms"], 5), "draft_sample_ms": round(mc["draft_ms"], 5),
             "verify_rows_per_s": (wc.rows_target + wc.rows_draft) / (mc["verify_ms"] * 1e-3),
-            "verify_gbs": abc["verify"] / (mc["verify_ms"] * 1e-3) / 1e9,
-            "verify_frac_of_8tbs": abc["verify"] / (mc["verify_ms"] * 1e-3) / 8e12,
-            "verify_bytes": abc["verify"], "mean_accepted": mc["mean_accepted"]}
+            "verify_gbs": gbs(abc["verify"], mc["verify_ms"]),
+            "verify_frac_of_8tbs": gbs(abc["verify"], mc["verify_ms"]) / 8000.0,
+            "verify_bytes": abc["verify"], "mean_accepted": mc["mean_accepted"],
+            "verify_lse_ms": round(mf["verify_ms"], 5),
+            "verify_lse_gbs": gbs(abc["verify_lse"], mf["verify_ms"]),
+            "verify_lse_frac_of_8tbs": gbs(abc["verify_lse"], mf["verify_ms"]) / 8000.0,
+            "round_ms": round(mf["step_ms"], 5),
+            "round_rows_per_s": (wc.rows_target + wc.rows_draft) / (mf["step_ms"] * 1e-3),
+            "round_gbs": gbs(abc["verify_lse"] + abc["draft_sample"], mf["step_ms"])}
         del wc
 
     adapt = adaptive_k_timing(torch, sv, dev) if rank == 0 else None
@@ -418,19 +445,27 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Zipf-like logits + Gaussian noise)",
         "config": {"workload": w.name, "B": w.B, "V": w.V, "k": "uniform 1..10 per sequence",
                    "temperature": 1.0, "rows_target": w.rows_target, "rows_draft": w.rows_draft,
-                   "step": "spec_draft_sample + spec_verify", "l2": "inputs > L2 (no flush)",
+                   "step": "spec_draft_sample_lse + spec_verify_lse", "l2": "inputs > L2 (no flush)",
                    "parallelism": f"replicas x{world}"},
         "hbm_gbs": step_bytes / (step_ms * 1e-3) / 1e9,
         "frac_of_8tbs": step_bytes / (step_ms * 1e-3) / 8e12,
         "bytes_per_step": step_bytes,
-        "kernels": {"spec_verify_ms": m["verify_ms"], "spec_verify_gbs": verify_gbs,
-                    "spec_verify_frac_of_8tbs": verify_gbs / 8000.0,
-                    "spec_draft_sample_ms": m["draft_ms"], "spec_draft_sample_gbs": draft_gbs,
-                    "mean_accepted": m["mean_accepted"]},
-        "roofline": {"bound": "hbm", "kernel": "spec_verify (all its launches)",
-                     "achieved": verify_gbs, "peak": peak, "unit": "GB/s",
-                     "frac": verify_gbs / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
-                     "traffic": measured_traffic(w.name), "algorithmic_bytes_per_launch": ab["verify"],
+        "kernels": {"spec_verify_lse_ms": m["verify_ms"], "spec_verify_lse_gbs": verify_lse_gbs,
+                    "spec_verify_lse_frac_of_8tbs": verify_lse_gbs / 8000.0,
+                    "spec_draft_sample_lse_ms": m["draft_ms"], "spec_draft_sample_lse_gbs": draft_gbs,
+                    "mean_accepted": m["mean_accepted"],
+                    "separate_calls": None if sep is None else {
+                        "step_ms": sep["step_ms"],
+                        "rows_per_s": rows / (sep["step_ms"] * 1e-3),
+                        "spec_verify_ms": sep["verify_ms"],
+                        "spec_verify_gbs": gbs(ab["verify"], sep["verify_ms"]),
+                        "spec_verify_frac_of_8tbs": gbs(ab["verify"], sep["verify_ms"]) / 8000.0,
+                        "spec_draft_sample_ms": sep["draft_ms"]}},
+        "roofline": {"bound": "hbm", "kernel": "spec_verify_lse (all its launches: stats_kernel over the "
+                                               "target rows + resolve_kernel)",
+                     "achieved": verify_lse_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": verify_lse_gbs / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": measured_traffic(w.name), "algorithmic_bytes_per_launch": ab["verify_lse"],
                      "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the call's kernels "
                                        "(profiles/, null unless taken with the current kernel sources)"},
         # per step: stats_kernel + draft_select_kernel, stats_kernel + resolve_kernel

@@ -149,9 +149,64 @@ int spec_draft_sample_ex(const void *draft_logits, const float *temperature,
                          size_t workspace_bytes, void *stream);
 
 /*
+ * Draft sampling that also keeps each draft row's normaliser for the verify
+ * step.  docs.ifdog.com "投机解码", section 动手实践: the drafting loop keeps
+ * the draft distribution q of every position and step 3 reuses it instead
+ * of recomputing it; here only q's normaliser is kept (8 bytes per row),
+ * since q(v) = exp(z_v / T_b) / 2^L follows from it and the draft logits.
+ *
+ * Same arguments and outputs as spec_draft_sample_ex, plus
+ *   out_draft_lse2  double [R_d], device: for every sampled row r of
+ *                   sequence b, L_r = log2(sum_v exp(z_r,v / T_b)) (the
+ *                   natural log-sum-exp divided by ln 2); NaN for greedy
+ *                   rows (T_b = 0) and for rows that give token -1.
+ * Pass out_draft_lse2 to spec_verify_lse with the same logits, temperature
+ * and k_offsets.  SPEC_ERR_INVALID_ARG if out_draft_lse2 is NULL (B > 0).
+ */
+int spec_draft_sample_lse(const void *draft_logits, const float *temperature,
+                          const float *u_draft, int B, const int32_t *k_offsets, int V,
+                          int dtype, int32_t *out_draft_tokens, double *out_draft_lse2,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * spec_verify_ex with the draft rows' normalisers given (draft_lse2, from
+ * spec_draft_sample_lse on the same draft logits, temperature and
+ * k_offsets): only the target rows are streamed; of the draft logits it
+ * reads the drafted token's logit at each position and the one draft row
+ * at a rejected position (the residual max(0, p - q) needs the whole q row
+ * there).  With the same inputs its outputs equal spec_verify's bit for
+ * bit (both derive L from the same partial sums).  A draft_lse2 entry that
+ * is NaN or infinite, for a position of a sampled sequence, is a data error
+ * of that sequence.  aux, workspace: as in spec_verify_ex (aux->lse_draft
+ * echoes draft_lse2 * ln 2).  SPEC_ERR_INVALID_ARG if draft_lse2 is NULL
+ * (B > 0).
+ */
+int spec_verify_lse(const void *target_logits, const void *draft_logits,
+                    const double *draft_lse2, const int32_t *draft_tokens,
+                    const float *u_accept, const float *u_resample,
+                    const float *temperature, int B, const int32_t *k_offsets, int V,
+                    int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
+                    const spec_verify_aux_t *aux, void *workspace,
+                    size_t workspace_bytes, void *stream);
+
+/*
+ * One sampling round on DEVICE buffers: spec_draft_sample_lse (filling
+ * out_draft_tokens [R_d]) and then spec_verify_lse on those tokens, with the
+ * draft rows' normalisers kept in the library-owned workspace between the
+ * two passes, so every logit row is read once (plus the two rows at a
+ * rejected position).  Arguments as in spec_draft_sample and spec_verify;
+ * outputs equal those of spec_draft_sample followed by spec_verify.
+ */
+int spec_round(const void *target_logits, const void *draft_logits, const float *u_draft,
+               const float *u_accept, const float *u_resample, const float *temperature,
+               int B, const int32_t *k_offsets, int V, int dtype,
+               int32_t *out_draft_tokens, int32_t *out_tokens,
+               int32_t *out_num_accepted, void *stream);
+
+/*
  * One sampling round from HOST memory: copies the inputs to the device,
- * runs spec_draft_sample (which fills the draft tokens) and then
- * spec_verify, copies the draft tokens and the verify outputs back, and
+ * runs spec_round (draft sampling, which fills the draft tokens, then
+ * verify), copies the draft tokens and the verify outputs back, and
  * returns after the stream has finished.  All pointers are host pointers
  * (pinned memory gives full copy bandwidth); k_offsets [B+1] is read on the
  * host to size the copies.  Uses a library-owned device staging area that

@@ -25,8 +25,11 @@ from ._binding import (  # noqa: F401
     lib_path,
     noalloc_bytes,
     spec_draft_sample,
+    spec_draft_sample_lse,
+    spec_round,
     spec_round_host,
     spec_verify,
+    spec_verify_lse,
     spec_verify_noalloc,
     workspace_bytes,
     workspace_status,

@@ -17,7 +17,8 @@ SPEC_ERRORS = {0: "SPEC_OK", -1: "SPEC_ERR_INVALID_ARG", -2: "SPEC_ERR_ALIGNMENT
 EXPORTS = ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",
            "spec_round_host", "spec_workspace_bytes", "spec_workspace_status",
            "spec_status_string", "spec_abi_version", "spec_last_error", "spec_verify_noalloc",
-           "spec_noalloc_bytes", "spec_adapt_state_bytes", "spec_adapt_init", "spec_adapt_update")
+           "spec_noalloc_bytes", "spec_adapt_state_bytes", "spec_adapt_init", "spec_adapt_update",
+           "spec_draft_sample_lse", "spec_verify_lse", "spec_round")
 
 
 class SpecError(RuntimeError):
@@ -55,6 +56,10 @@ def lib():
     L.spec_draft_sample.argtypes = [vp, vp, vp, ip, vp, ip, ip, vp, vp]
     L.spec_draft_sample_ex.argtypes = [vp, vp, vp, ip, vp, ip, ip, vp, vp, sz, vp]
     L.spec_round_host.argtypes = [vp, vp, vp, vp, vp, vp, ip, vp, ip, ip, vp, vp, vp, vp]
+    L.spec_draft_sample_lse.argtypes = [vp, vp, vp, ip, vp, ip, ip, vp, vp, vp, sz, vp]
+    L.spec_verify_lse.argtypes = [vp, vp, vp, vp, vp, vp, vp, ip, vp, ip, ip, vp, vp,
+                                  ctypes.POINTER(_Aux), vp, sz, vp]
+    L.spec_round.argtypes = [vp, vp, vp, vp, vp, vp, ip, vp, ip, ip, vp, vp, vp, vp]
     L.spec_workspace_bytes.argtypes = [ip, ip, ip]
     L.spec_workspace_bytes.restype = sz
     L.spec_noalloc_bytes.argtypes = [ip, ip, ip]
@@ -74,7 +79,8 @@ def lib():
     L.spec_adapt_update.argtypes = [vp, vp, ip, ip, ip, vp, vp]
     L.spec_adapt_update.restype = ip
     for name in ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",
-                 "spec_round_host", "spec_workspace_status", "spec_abi_version"):
+                 "spec_round_host", "spec_workspace_status", "spec_abi_version",
+                 "spec_draft_sample_lse", "spec_verify_lse", "spec_round"):
         getattr(L, name).restype = ip
     _lib = L
     return L
@@ -148,16 +154,7 @@ def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_resample,
         out_num_accepted = torch.empty(B, dtype=torch.int32, device=dev)
     L = lib()
     ws_ptr, ws_bytes = (None, 0) if workspace is None else (_p(workspace), workspace.numel() * workspace.element_size())
-    ax = None
-    aux_out = None
-    if aux:
-        R_d = draft_tokens.numel()
-        aux_out = dict(accept_prob=torch.full((R_d,), float("nan"), device=dev),
-                       residual_mass=torch.full((B,), float("nan"), device=dev),
-                       lse_target=torch.full((R_t,), float("nan"), device=dev),
-                       lse_draft=torch.full((R_d,), float("nan"), device=dev))
-        ax = _Aux(*(ctypes.c_void_p(aux_out[k].data_ptr()) for k in
-                    ("accept_prob", "residual_mass", "lse_target", "lse_draft")))
+    aux_out, ax = _aux_buffers(B, R_t, draft_tokens.numel(), dev) if aux else (None, None)
     if ax is None and workspace is None:
         rc = L.spec_verify(_p(target_logits), _p(draft_logits), _p(draft_tokens), _p(u_accept),
                            _p(u_resample), _p(temperature), B, _p(k_offsets), V, dt,
@@ -197,6 +194,115 @@ def spec_draft_sample(draft_logits, temperature, u_draft, k_offsets, out_draft_t
                                     workspace.numel() * workspace.element_size(), _stream(stream))
     _raise(rc, "spec_draft_sample")
     return out_draft_tokens
+
+
+def _aux_buffers(B, R_t, R_d, dev):
+    import torch
+    out = dict(accept_prob=torch.full((R_d,), float("nan"), device=dev),
+               residual_mass=torch.full((B,), float("nan"), device=dev),
+               lse_target=torch.full((R_t,), float("nan"), device=dev),
+               lse_draft=torch.full((R_d,), float("nan"), device=dev))
+    ax = _Aux(*(ctypes.c_void_p(out[k].data_ptr()) for k in
+                ("accept_prob", "residual_mass", "lse_target", "lse_draft")))
+    return out, ax
+
+
+def spec_draft_sample_lse(draft_logits, temperature, u_draft, k_offsets, out_draft_tokens=None,
+                          out_draft_lse2=None, workspace=None, stream=None):
+    """Draft sampling that also returns each draft row's log2-domain
+    log-sum-exp (float64 [R_d], NaN for greedy/invalid rows), for
+    spec_verify_lse.  Returns (draft_tokens int32 [R_d], draft_lse2)."""
+    import torch
+    B = temperature.numel()
+    V = draft_logits.shape[-1]
+    dt = _dtype_code(draft_logits)
+    _check_dev("draft_logits", draft_logits)
+    _check_dev("temperature", temperature, torch.float32)
+    _check_dev("u_draft", u_draft, torch.float32)
+    _check_dev("k_offsets", k_offsets, torch.int32)
+    R_d = u_draft.numel()
+    dev = draft_logits.device
+    if out_draft_tokens is None:
+        out_draft_tokens = torch.empty(R_d, dtype=torch.int32, device=dev)
+    if out_draft_lse2 is None:
+        out_draft_lse2 = torch.empty(max(R_d, 1), dtype=torch.float64, device=dev)
+    _check_dev("out_draft_lse2", out_draft_lse2, torch.float64)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_p(workspace), workspace.numel() * workspace.element_size())
+    rc = lib().spec_draft_sample_lse(_p(draft_logits), _p(temperature), _p(u_draft), B, _p(k_offsets), V, dt,
+                                     _p(out_draft_tokens), _p(out_draft_lse2), ws_ptr, ws_bytes, _stream(stream))
+    _raise(rc, "spec_draft_sample_lse")
+    return out_draft_tokens, out_draft_lse2[:R_d]
+
+
+def spec_verify_lse(target_logits, draft_logits, draft_lse2, draft_tokens, u_accept, u_resample,
+                    temperature, k_offsets, out_tokens=None, out_num_accepted=None, aux: bool = False,
+                    workspace=None, stream=None):
+    """spec_verify with the draft rows' normalisers given (from
+    spec_draft_sample_lse): only the target rows are streamed.  Same
+    returns as spec_verify."""
+    import torch
+    B = temperature.numel()
+    V = target_logits.shape[-1]
+    dt = _dtype_code(target_logits)
+    for name, t in (("target_logits", target_logits), ("draft_logits", draft_logits)):
+        _check_dev(name, t, target_logits.dtype)
+    _check_dev("draft_lse2", draft_lse2, torch.float64)
+    _check_dev("draft_tokens", draft_tokens, torch.int32)
+    _check_dev("u_accept", u_accept, torch.float32)
+    _check_dev("u_resample", u_resample, torch.float32)
+    _check_dev("temperature", temperature, torch.float32)
+    _check_dev("k_offsets", k_offsets, torch.int32)
+    if k_offsets.numel() != B + 1:
+        raise ValueError("k_offsets must have B + 1 entries")
+    R_t, R_d = u_resample.numel(), draft_tokens.numel()
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty(R_t, dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    aux_out, ax = _aux_buffers(B, R_t, R_d, dev) if aux else (None, None)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_p(workspace), workspace.numel() * workspace.element_size())
+    rc = lib().spec_verify_lse(_p(target_logits), _p(draft_logits), _p(draft_lse2), _p(draft_tokens),
+                               _p(u_accept), _p(u_resample), _p(temperature), B, _p(k_offsets), V, dt,
+                               _p(out_tokens), _p(out_num_accepted),
+                               ctypes.byref(ax) if ax is not None else None, ws_ptr, ws_bytes, _stream(stream))
+    _raise(rc, "spec_verify_lse")
+    if aux:
+        return out_tokens, out_num_accepted, aux_out
+    return out_tokens, out_num_accepted
+
+
+def spec_round(target_logits, draft_logits, u_draft, u_accept, u_resample, temperature, k_offsets,
+               out_draft_tokens=None, out_tokens=None, out_num_accepted=None, stream=None):
+    """One sampling round on device tensors: draft sampling, then verify
+    with the draft rows' normalisers kept between the passes (every row
+    read once).  Returns (draft_tokens [R_d], out_tokens [R_t],
+    out_num_accepted [B])."""
+    import torch
+    B = temperature.numel()
+    V = target_logits.shape[-1]
+    dt = _dtype_code(target_logits)
+    for name, t in (("target_logits", target_logits), ("draft_logits", draft_logits)):
+        _check_dev(name, t, target_logits.dtype)
+    for name, t in (("u_draft", u_draft), ("u_accept", u_accept), ("u_resample", u_resample),
+                    ("temperature", temperature)):
+        _check_dev(name, t, torch.float32)
+    _check_dev("k_offsets", k_offsets, torch.int32)
+    if k_offsets.numel() != B + 1:
+        raise ValueError("k_offsets must have B + 1 entries")
+    R_t, R_d = u_resample.numel(), u_accept.numel()
+    dev = target_logits.device
+    if out_draft_tokens is None:
+        out_draft_tokens = torch.empty(R_d, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(R_t, dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    rc = lib().spec_round(_p(target_logits), _p(draft_logits), _p(u_draft), _p(u_accept), _p(u_resample),
+                          _p(temperature), B, _p(k_offsets), V, dt, _p(out_draft_tokens), _p(out_tokens),
+                          _p(out_num_accepted), _stream(stream))
+    _raise(rc, "spec_round")
+    return out_draft_tokens, out_tokens, out_num_accepted
 
 
 def spec_round_host(target_logits, draft_logits, u_draft, u_accept, u_resample, temperature,

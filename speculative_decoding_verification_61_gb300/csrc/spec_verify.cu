@@ -213,11 +213,19 @@ __device__ __forceinline__ void unit_batch(int t, int64_t n_big, int64_t *u0, in
 }
 
 // ================================================================== kernel 1
+// Streaming modes of stats_kernel (which rows it reads).
+enum StatsMode : int {
+    kModeVerify = 0,  // target rows, plus the draft rows of sampled sequences
+    kModeDraft = 1,   // draft rows only (spec_draft_sample)
+    kModeTarget = 2   // target rows only (verify with the draft rows' lse given)
+};
+
 // Persistent streaming kernel.  Unit u = (row r of the virtual row list,
 // chunk ch).  Virtual row list, by sequence b in order:
 //   verify mode: target rows of b (k_b + 1), then draft rows of b (k_b) if
 //                b is sampled; nothing for a bad temperature;
-//   draft mode:  draft rows of b (k_b); nothing for a bad temperature.
+//   draft mode:  draft rows of b (k_b); nothing for a bad temperature;
+//   target mode: target rows of b (k_b + 1); nothing for a bad temperature.
 // Units are taken by tickets (unit_batch).  One lane of warp 8 is the
 // producer: it waits for a free ring slot and issues the bulk copy of the
 // next unit into it.  Warps 0..7 consume: warp w owns the w-th 2 KB
@@ -226,12 +234,13 @@ __device__ __forceinline__ void unit_batch(int t, int64_t n_big, int64_t *u0, in
 // that partial straight to global memory.
 // (the bound caps registers at 40, which leaves room on an SM with four
 // of these CTAs for one resolve_kernel block of the other stream)
-template <int DT, bool DRAFT>
+template <int DT, int MODE>
 __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
     const void *__restrict__ target, const void *__restrict__ draft,
     const float *__restrict__ temperature, const int *__restrict__ k_offsets, int B, Geometry g, int ns,
     float2 *__restrict__ part, int *__restrict__ counters, int *__restrict__ seqcnt) {
     using E = Elem<DT>;
+    constexpr bool DRAFT = MODE == kModeDraft;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)ns * kSlotBytes);
@@ -259,7 +268,9 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
         const int k = s_kofs[b + 1] - s_kofs[b];
         const float c = s_c[b];
         if (c != c) return 0;
-        return DRAFT ? k : (c == 0.0f ? k + 1 : 2 * k + 1);
+        if (MODE == kModeDraft) return k;
+        if (MODE == kModeTarget) return k + 1;
+        return c == 0.0f ? k + 1 : 2 * k + 1;
     };
     for (int b = b0; b < b1; ++b) {
         const int k = s_kofs[b + 1] - s_kofs[b];
@@ -736,10 +747,15 @@ __device__ int warp_draw_row(const void *logits, int64_t row, const float2 *part
 // The call's inputs (the k_offsets check, drafted tokens and their logits)
 // are read before the wait on stats_kernel, which hides that latency behind
 // the streaming pass's tail.
+// With draft_lse2 given (the draft rows' log2-domain log-sum-exp, written by
+// the draft-sampling pass from the same partials this kernel would combine),
+// the draft rows were not streamed: their Ld comes from that array, bit for
+// bit what the combine below would give.
 struct ResolveSmem {
-    float M[2 * kMaxK + 1];
-    float S[2 * kMaxK + 1];
-    int arg[2 * kMaxK + 1];
+    float M[kMaxK + 1];       // target rows: max of z*c
+    float S[kMaxK + 1];       // target rows: sum 2^(z*c - M)
+    double Ld[kMaxK];         // draft rows: log2-domain log-sum-exp
+    int arg[kMaxK + 1];       // greedy target rows: arg-max
     int ok[2 * kMaxK + 1];
     int n;     // accepted count, -1 on a data error
     int kind;  // kJobNone, kJobResid or kJobBonus
@@ -754,8 +770,8 @@ __global__ void __launch_bounds__(256, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
     const void *__restrict__ target, const void *__restrict__ draft,
     const int32_t *__restrict__ tokens, const float *__restrict__ u_accept,
     const float *__restrict__ u_resample, const float *__restrict__ temperature,
-    const int *__restrict__ k_offsets, int B, Geometry g, int nsplit, WsPtrs ws,
-    int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_num, spec_verify_aux_t aux) {
+    const int *__restrict__ k_offsets, const double *__restrict__ draft_lse2, int B, Geometry g, int nsplit,
+    WsPtrs ws, int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_num, spec_verify_aux_t aux) {
     using E = Elem<DT>;
     __shared__ ResolveSmem sm;
     const int b = blockIdx.x / nsplit;
@@ -794,6 +810,7 @@ __global__ void __launch_bounds__(256, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
     const float c = temp_scale(temperature[b]);
     const int V = g.V;
     const bool greedy = (c == 0.0f);
+    const bool given = draft_lse2 != nullptr;
     int x = 0;
     bool xbad = false;
     float zt = 0.0f, zd = 0.0f, ua = 0.0f, ur = 0.0f;
@@ -806,6 +823,7 @@ __global__ void __launch_bounds__(256, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
             if (!xbad && !greedy && c == c) {
                 zt = E::load1(target, (ot + lane) * V + x);
                 zd = E::load1(draft, (od + lane) * V + x);
+                if (given) sm.Ld[lane] = draft_lse2[od + lane];  // read by warp 0 only
             }
         }
     }
@@ -813,7 +831,7 @@ __global__ void __launch_bounds__(256, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
     // --- 1. row statistics and the decision -------------------------------
     grid_dependency_wait();
     if (c == c) {
-        const int nrows = greedy ? k + 1 : 2 * k + 1;
+        const int nrows = (greedy || given) ? k + 1 : 2 * k + 1;
         for (int rr = warp; rr < nrows; rr += blockDim.x >> 5) {
             const bool is_t = rr <= k;
             const int i = is_t ? rr : rr - k - 1;
@@ -830,8 +848,12 @@ __global__ void __launch_bounds__(256, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
                 float M, S;
                 const bool ok = warp_combine_soft(p, g.n_sub, &M, &S);
                 if (lane == 0) {
-                    sm.M[si] = M;
-                    sm.S[si] = S;
+                    if (is_t) {
+                        sm.M[i] = M;
+                        sm.S[i] = S;
+                    } else {
+                        sm.Ld[i] = ok ? lse2(M, S) : NAN;
+                    }
                     sm.ok[si] = ok;
                 }
             }
@@ -846,8 +868,12 @@ __global__ void __launch_bounds__(256, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
         if (!err) {
             bool rows_ok = true;
             for (int i = lane; i <= k; i += 32) rows_ok &= sm.ok[i] != 0;
-            if (!greedy)
-                for (int i = lane; i < k; i += 32) rows_ok &= sm.ok[kMaxK + 1 + i] != 0;
+            if (!greedy) {
+                if (given)
+                    rows_ok &= lane >= k || isfinite(sm.Ld[lane]);
+                else
+                    for (int i = lane; i < k; i += 32) rows_ok &= sm.ok[kMaxK + 1 + i] != 0;
+            }
             err = !__all_sync(0xffffffffu, rows_ok);
         }
         if (!err && greedy) {
@@ -862,7 +888,7 @@ __global__ void __launch_bounds__(256, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
             bool acc = false;
             if (lane < k) {
                 Lt = lse2(sm.M[lane], sm.S[lane]);
-                Ld = lse2(sm.M[kMaxK + 1 + lane], sm.S[kMaxK + 1 + lane]);
+                Ld = sm.Ld[lane];
                 float alpha;
                 if (zt == -INFINITY) {
                     alpha = 0.0f;
@@ -884,10 +910,10 @@ __global__ void __launch_bounds__(256, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
             // u at position n; position 32 (k = 32, all accepted) has no lane
             float u_n = __shfl_sync(0xffffffffu, ur, n & 31);
             if (n == 32) u_n = u_resample[ot + 32];
+            const double Ldn = __shfl_sync(0xffffffffu, Ld, n & 31);  // used only if n < k
             if (lane == 0) {
                 if (n < k) {
                     const double Ltn = lse2(sm.M[n], sm.S[n]);
-                    const double Ldn = lse2(sm.M[kMaxK + 1 + n], sm.S[kMaxK + 1 + n]);
                     sm.lth = static_cast<float>(Ltn);
                     sm.ltl = static_cast<float>(Ltn - static_cast<double>(sm.lth));
                     sm.ldh = static_cast<float>(Ldn);
@@ -1025,12 +1051,15 @@ __global__ void __launch_bounds__(256, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
     }
 }
 
-// Draft-side draw: one warp per draft row (grid-stride over rows).
+// Draft-side draw: one warp per draft row (grid-stride over rows).  With
+// out_lse2 given, each row's log2-domain log-sum-exp (the value
+// resolve_kernel would combine from the same partials) is written too: NaN
+// for greedy and invalid rows.
 template <int DT>
 __global__ void __launch_bounds__(256) draft_select_kernel(
     const void *__restrict__ draft, const float *__restrict__ temperature, const float *__restrict__ u_draft,
     const int *__restrict__ k_offsets, int B, Geometry g, const float2 *__restrict__ part,
-    int32_t *__restrict__ out, int *__restrict__ counters) {
+    int32_t *__restrict__ out, double *__restrict__ out_lse2, int *__restrict__ counters) {
     extern __shared__ int s_kofs[];  // [B+1]
     __shared__ int s_bad;
     if (threadIdx.x == 0) s_bad = 0;
@@ -1063,13 +1092,20 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
         const float c = temp_scale(temperature[lo]);
         const float2 *pr = part + static_cast<int64_t>(r) * g.n_sub;
         int token = -1;
+        double L = NAN;
         if (c == 0.0f) {
             token = warp_combine_arg(pr, g.n_sub);
         } else if (c == c) {
             float M, S;
-            if (warp_combine_soft(pr, g.n_sub, &M, &S)) token = warp_draw_row<DT>(draft, r, pr, g, c, M, u_draft[r]);
+            if (warp_combine_soft(pr, g.n_sub, &M, &S)) {
+                L = lse2(M, S);
+                token = warp_draw_row<DT>(draft, r, pr, g, c, M, u_draft[r]);
+            }
         }
-        if (lane == 0) out[r] = token;
+        if (lane == 0) {
+            out[r] = token;
+            if (out_lse2) out_lse2[r] = L;
+        }
     }
 }
 
@@ -1107,7 +1143,7 @@ bool make_geometry(int V, int dtype, Geometry *g) {
 }
 
 struct WsLayout {
-    size_t part, counters, seqcnt, resid, total;
+    size_t part, counters, seqcnt, resid, lse2, total;
 };
 
 // Workspace layout.  The counters block comes first so that the status word
@@ -1128,6 +1164,8 @@ WsLayout ws_layout(int B, const Geometry &g) {
     off = align_up(off + B * sizeof(int), 256);
     l.resid = off;
     off = align_up(off + static_cast<size_t>(B) * g.n_sub * sizeof(float), 256);
+    l.lse2 = off;  // spec_round: the draft rows' lse2 between its two passes
+    off = align_up(off + static_cast<size_t>(B) * kMaxK * sizeof(double), 256);
     l.total = off;
     return l;
 }
@@ -1153,13 +1191,19 @@ bool cuda_ok(cudaError_t e, const char *what) {
 }
 
 // Allow the kernel the opt-in dynamic shared memory minus its static part.
-template <int DT, bool DRAFT>
+template <int DT, int MODE>
 bool set_stats_attrs(int smem_optin) {
     cudaFuncAttributes fa{};
-    if (!cuda_ok(cudaFuncGetAttributes(&fa, stats_kernel<DT, DRAFT>), "cudaFuncGetAttributes")) return false;
+    if (!cuda_ok(cudaFuncGetAttributes(&fa, stats_kernel<DT, MODE>), "cudaFuncGetAttributes")) return false;
     const int dyn = smem_optin - static_cast<int>(fa.sharedSizeBytes);
-    return cuda_ok(cudaFuncSetAttribute(stats_kernel<DT, DRAFT>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn),
+    return cuda_ok(cudaFuncSetAttribute(stats_kernel<DT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn),
                    "cudaFuncSetAttribute(stats_kernel)");
+}
+
+template <int DT>
+bool set_stats_attrs_all(int smem_optin) {
+    return set_stats_attrs<DT, kModeVerify>(smem_optin) && set_stats_attrs<DT, kModeDraft>(smem_optin) &&
+           set_stats_attrs<DT, kModeTarget>(smem_optin);
 }
 
 DeviceState *device_state(int *dev_out) {
@@ -1174,8 +1218,7 @@ DeviceState *device_state(int *dev_out) {
             !cuda_ok(cudaDeviceGetAttribute(&st.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
                      "cudaDeviceGetAttribute"))
             return nullptr;
-        if (!set_stats_attrs<SPEC_F32, false>(st.smem_optin) || !set_stats_attrs<SPEC_F32, true>(st.smem_optin) ||
-            !set_stats_attrs<SPEC_BF16, false>(st.smem_optin) || !set_stats_attrs<SPEC_BF16, true>(st.smem_optin))
+        if (!set_stats_attrs_all<SPEC_F32>(st.smem_optin) || !set_stats_attrs_all<SPEC_BF16>(st.smem_optin))
             return nullptr;
         st.smem_optin -= 1024;  // headroom for the kernels' static shared memory
         st.init = true;
@@ -1295,11 +1338,16 @@ int resolve_split(const DeviceState &st, const Geometry &g, int n) {
     return std::max(1, std::min({kSub, g.n_sub, (SPEC_RESOLVE_BLOCKS_PER_SM * st.sms) / std::max(n, 1)}));
 }
 
+// The verify pass: stats_kernel streams the target rows (and, without
+// draft_lse2, the draft rows of sampled sequences), then resolve_kernel.
+// pdl_first: the call's first kernel may start early, which is safe only
+// when an earlier kernel of the same call precedes it on the stream.
 template <int DT>
-int launch_verify(const void *target, const void *draft, const int32_t *tokens, const float *u_accept,
-                  const float *u_resample, const float *temperature, int B, const int32_t *k_offsets,
-                  const Geometry &g, int32_t *out_tokens, int32_t *out_num, const spec_verify_aux_t &aux,
-                  void *ws_base, const WsLayout &l, const DeviceState &st, cudaStream_t stream) {
+int launch_verify(const void *target, const void *draft, const double *draft_lse2, const int32_t *tokens,
+                  const float *u_accept, const float *u_resample, const float *temperature, int B,
+                  const int32_t *k_offsets, const Geometry &g, int32_t *out_tokens, int32_t *out_num,
+                  const spec_verify_aux_t &aux, void *ws_base, const WsLayout &l, const DeviceState &st,
+                  cudaStream_t stream, bool pdl_first = false) {
     int ns, per_sm;
     size_t smem;
     pick_ring(st, B, &ns, &smem, &per_sm);
@@ -1307,11 +1355,15 @@ int launch_verify(const void *target, const void *draft, const int32_t *tokens, 
     const WsPtrs w = ws_ptrs(ws_base, l);
     const int grid = st.sms * per_sm;
     const int nsplit = resolve_split(st, g, B);
-    if (!cuda_ok(launch_k(false, stats_kernel<DT, false>, dim3(grid), dim3(kThreads), smem, stream, target, draft,
-                          temperature, k_offsets, B, g, ns, w.part, w.counters, w.seqcnt),
-                 "launch stats_kernel") ||
+    const cudaError_t e1 =
+        draft_lse2 ? launch_k(pdl_first, stats_kernel<DT, kModeTarget>, dim3(grid), dim3(kThreads), smem, stream,
+                              target, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, w.seqcnt)
+                   : launch_k(pdl_first, stats_kernel<DT, kModeVerify>, dim3(grid), dim3(kThreads), smem, stream,
+                              target, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, w.seqcnt);
+    if (!cuda_ok(e1, "launch stats_kernel") ||
         !cuda_ok(launch_k(true, resolve_kernel<DT>, dim3(B * nsplit), dim3(256), 0, stream, target, draft, tokens,
-                          u_accept, u_resample, temperature, k_offsets, B, g, nsplit, w, out_tokens, out_num, aux),
+                          u_accept, u_resample, temperature, k_offsets, draft_lse2, B, g, nsplit, w, out_tokens,
+                          out_num, aux),
                  "launch resolve_kernel"))
         return SPEC_ERR_CUDA;
     return SPEC_OK;
@@ -1319,8 +1371,8 @@ int launch_verify(const void *target, const void *draft, const int32_t *tokens, 
 
 template <int DT>
 int launch_draft(const void *draft, const float *temperature, const float *u_draft, int B,
-                 const int32_t *k_offsets, const Geometry &g, int32_t *out, void *ws_base, const WsLayout &l,
-                 const DeviceState &st, cudaStream_t stream) {
+                 const int32_t *k_offsets, const Geometry &g, int32_t *out, double *out_lse2, void *ws_base,
+                 const WsLayout &l, const DeviceState &st, cudaStream_t stream) {
     int ns, per_sm;
     size_t smem;
     pick_ring(st, B, &ns, &smem, &per_sm);
@@ -1328,12 +1380,12 @@ int launch_draft(const void *draft, const float *temperature, const float *u_dra
     const WsPtrs w = ws_ptrs(ws_base, l);
     // one warp per draft row: at most B * kMaxK rows, 8 warps per block
     const int grid = static_cast<int>(std::min(static_cast<int64_t>(st.sms) * 8, (static_cast<int64_t>(B) * kMaxK + 7) / 8));
-    if (!cuda_ok(launch_k(false, stats_kernel<DT, true>, dim3(st.sms * per_sm), dim3(kThreads), smem, stream, draft,
-                          draft, temperature, k_offsets, B, g, ns, w.part, w.counters, nullptr),
+    if (!cuda_ok(launch_k(false, stats_kernel<DT, kModeDraft>, dim3(st.sms * per_sm), dim3(kThreads), smem, stream,
+                          draft, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, nullptr),
                  "launch stats_kernel") ||
         !cuda_ok(launch_k(true, draft_select_kernel<DT>, dim3(std::max(grid, 1)), dim3(256),
                           (B + 1) * sizeof(int), stream, draft, temperature, u_draft, k_offsets, B, g,
-                          static_cast<const float2 *>(w.part), out, w.counters),
+                          static_cast<const float2 *>(w.part), out, out_lse2, w.counters),
                  "launch draft_select_kernel"))
         return SPEC_ERR_CUDA;
     return SPEC_OK;
@@ -1354,10 +1406,31 @@ size_t spec_workspace_bytes(int B, int V, int dtype) {
 
 size_t spec_noalloc_bytes(int B, int V, int dtype) { return spec_workspace_bytes(B, V, dtype); }
 
-int spec_verify_ex(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
-                   const float *u_accept, const float *u_resample, const float *temperature, int B,
-                   const int32_t *k_offsets, int V, int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
-                   const spec_verify_aux_t *aux, void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace specv {
+
+// The workspace of one call: the caller's (checked, its ticket words
+// zeroed on the stream) or the library-owned one.  nullptr with *rc set on
+// failure.
+void *call_workspace(void *workspace, size_t workspace_bytes, const WsLayout &l, DeviceState &st,
+                     cudaStream_t stream, int *rc) {
+    *rc = SPEC_OK;
+    if (workspace) {
+        if (workspace_bytes < l.total) *rc = SPEC_ERR_WORKSPACE;
+        else if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) *rc = SPEC_ERR_ALIGNMENT;
+        else if (!reset_tickets(workspace, stream)) *rc = SPEC_ERR_CUDA;
+        return *rc == SPEC_OK ? workspace : nullptr;
+    }
+    void *ws = get_internal_ws(st, l.total);
+    if (!ws) *rc = SPEC_ERR_CUDA;
+    return ws;
+}
+
+int verify_call(const void *target_logits, const void *draft_logits, const double *draft_lse2,
+                const int32_t *draft_tokens, const float *u_accept, const float *u_resample, const float *temperature,
+                int B, const int32_t *k_offsets, int V, int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
+                const spec_verify_aux_t *aux, void *workspace, size_t workspace_bytes, void *stream) {
     int rc = check_common(B, V, dtype);
     if (rc != SPEC_OK) return rc;
     if (B == 0) return SPEC_OK;
@@ -1371,37 +1444,21 @@ int spec_verify_ex(const void *target_logits, const void *draft_logits, const in
     int dev;
     DeviceState *st = device_state(&dev);
     if (!st) return SPEC_ERR_CUDA;
-    void *ws = workspace;
-    if (ws) {
-        if (workspace_bytes < l.total) return SPEC_ERR_WORKSPACE;
-        if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SPEC_ERR_ALIGNMENT;
-        if (!reset_tickets(ws, static_cast<cudaStream_t>(stream))) return SPEC_ERR_CUDA;
-    } else {
-        ws = get_internal_ws(*st, l.total);
-        if (!ws) return SPEC_ERR_CUDA;
-    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *ws = call_workspace(workspace, workspace_bytes, l, *st, s, &rc);
+    if (!ws) return rc;
     spec_verify_aux_t a{};
     if (aux) a = *aux;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == SPEC_F32)
-        return launch_verify<SPEC_F32>(target_logits, draft_logits, draft_tokens, u_accept, u_resample,
-                                       temperature, B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st,
-                                       s);
-    return launch_verify<SPEC_BF16>(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature,
-                                    B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st, s);
+        return launch_verify<SPEC_F32>(target_logits, draft_logits, draft_lse2, draft_tokens, u_accept, u_resample,
+                                       temperature, B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st, s);
+    return launch_verify<SPEC_BF16>(target_logits, draft_logits, draft_lse2, draft_tokens, u_accept, u_resample,
+                                    temperature, B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st, s);
 }
 
-int spec_verify(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
-                const float *u_accept, const float *u_resample, const float *temperature, int B,
-                const int32_t *k_offsets, int V, int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
-                void *stream) {
-    return spec_verify_ex(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature, B,
-                          k_offsets, V, dtype, out_tokens, out_num_accepted, nullptr, nullptr, 0, stream);
-}
-
-int spec_draft_sample_ex(const void *draft_logits, const float *temperature, const float *u_draft, int B,
-                         const int32_t *k_offsets, int V, int dtype, int32_t *out_draft_tokens, void *workspace,
-                         size_t workspace_bytes, void *stream) {
+int draft_call(const void *draft_logits, const float *temperature, const float *u_draft, int B,
+               const int32_t *k_offsets, int V, int dtype, int32_t *out_draft_tokens, double *out_draft_lse2,
+               void *workspace, size_t workspace_bytes, void *stream) {
     int rc = check_common(B, V, dtype);
     if (rc != SPEC_OK) return rc;
     if (B == 0) return SPEC_OK;
@@ -1413,27 +1470,111 @@ int spec_draft_sample_ex(const void *draft_logits, const float *temperature, con
     int dev;
     DeviceState *st = device_state(&dev);
     if (!st) return SPEC_ERR_CUDA;
-    void *ws = workspace;
-    if (ws) {
-        if (workspace_bytes < l.total) return SPEC_ERR_WORKSPACE;
-        if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SPEC_ERR_ALIGNMENT;
-        if (!reset_tickets(ws, static_cast<cudaStream_t>(stream))) return SPEC_ERR_CUDA;
-    } else {
-        ws = get_internal_ws(*st, l.total);
-        if (!ws) return SPEC_ERR_CUDA;
-    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *ws = call_workspace(workspace, workspace_bytes, l, *st, s, &rc);
+    if (!ws) return rc;
     if (dtype == SPEC_F32)
-        return launch_draft<SPEC_F32>(draft_logits, temperature, u_draft, B, k_offsets, g, out_draft_tokens, ws, l,
-                                      *st, s);
-    return launch_draft<SPEC_BF16>(draft_logits, temperature, u_draft, B, k_offsets, g, out_draft_tokens, ws, l,
-                                   *st, s);
+        return launch_draft<SPEC_F32>(draft_logits, temperature, u_draft, B, k_offsets, g, out_draft_tokens,
+                                      out_draft_lse2, ws, l, *st, s);
+    return launch_draft<SPEC_BF16>(draft_logits, temperature, u_draft, B, k_offsets, g, out_draft_tokens,
+                                   out_draft_lse2, ws, l, *st, s);
+}
+
+// One round on device buffers: the draft pass (tokens and the draft rows'
+// lse2, kept in the workspace), then the verify pass over the target rows.
+int round_call(const void *target_logits, const void *draft_logits, const float *u_draft, const float *u_accept,
+               const float *u_resample, const float *temperature, int B, const int32_t *k_offsets, int V, int dtype,
+               int32_t *out_draft_tokens, int32_t *out_tokens, int32_t *out_num_accepted, void *stream) {
+    int rc = check_common(B, V, dtype);
+    if (rc != SPEC_OK) return rc;
+    if (B == 0) return SPEC_OK;
+    if (!target_logits || !draft_logits || !u_draft || !u_accept || !u_resample || !temperature || !k_offsets ||
+        !out_draft_tokens || !out_tokens || !out_num_accepted)
+        return SPEC_ERR_INVALID_ARG;
+    if (!aligned16(target_logits) || !aligned16(draft_logits)) return SPEC_ERR_ALIGNMENT;
+    Geometry g;
+    make_geometry(V, dtype, &g);
+    const WsLayout l = ws_layout(B, g);
+    int dev;
+    DeviceState *st = device_state(&dev);
+    if (!st) return SPEC_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *ws = call_workspace(nullptr, 0, l, *st, s, &rc);
+    if (!ws) return rc;
+    double *lse2 = reinterpret_cast<double *>(static_cast<unsigned char *>(ws) + l.lse2);
+    const spec_verify_aux_t a{};
+    if (dtype == SPEC_F32) {
+        rc = launch_draft<SPEC_F32>(draft_logits, temperature, u_draft, B, k_offsets, g, out_draft_tokens, lse2, ws,
+                                    l, *st, s);
+        if (rc != SPEC_OK) return rc;
+        return launch_verify<SPEC_F32>(target_logits, draft_logits, lse2, out_draft_tokens, u_accept, u_resample,
+                                       temperature, B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st, s,
+                                       true);
+    }
+    rc = launch_draft<SPEC_BF16>(draft_logits, temperature, u_draft, B, k_offsets, g, out_draft_tokens, lse2, ws, l,
+                                 *st, s);
+    if (rc != SPEC_OK) return rc;
+    return launch_verify<SPEC_BF16>(target_logits, draft_logits, lse2, out_draft_tokens, u_accept, u_resample,
+                                    temperature, B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st, s,
+                                    true);
+}
+
+}  // namespace specv
+
+extern "C" {
+
+int spec_verify_ex(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
+                   const float *u_accept, const float *u_resample, const float *temperature, int B,
+                   const int32_t *k_offsets, int V, int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
+                   const spec_verify_aux_t *aux, void *workspace, size_t workspace_bytes, void *stream) {
+    return verify_call(target_logits, draft_logits, nullptr, draft_tokens, u_accept, u_resample, temperature, B,
+                       k_offsets, V, dtype, out_tokens, out_num_accepted, aux, workspace, workspace_bytes, stream);
+}
+
+int spec_verify(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
+                const float *u_accept, const float *u_resample, const float *temperature, int B,
+                const int32_t *k_offsets, int V, int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
+                void *stream) {
+    return verify_call(target_logits, draft_logits, nullptr, draft_tokens, u_accept, u_resample, temperature, B,
+                       k_offsets, V, dtype, out_tokens, out_num_accepted, nullptr, nullptr, 0, stream);
+}
+
+int spec_verify_lse(const void *target_logits, const void *draft_logits, const double *draft_lse2,
+                    const int32_t *draft_tokens, const float *u_accept, const float *u_resample,
+                    const float *temperature, int B, const int32_t *k_offsets, int V, int dtype,
+                    int32_t *out_tokens, int32_t *out_num_accepted, const spec_verify_aux_t *aux, void *workspace,
+                    size_t workspace_bytes, void *stream) {
+    if (B > 0 && !draft_lse2) return SPEC_ERR_INVALID_ARG;
+    return verify_call(target_logits, draft_logits, draft_lse2, draft_tokens, u_accept, u_resample, temperature, B,
+                       k_offsets, V, dtype, out_tokens, out_num_accepted, aux, workspace, workspace_bytes, stream);
+}
+
+int spec_draft_sample_ex(const void *draft_logits, const float *temperature, const float *u_draft, int B,
+                         const int32_t *k_offsets, int V, int dtype, int32_t *out_draft_tokens, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+    return draft_call(draft_logits, temperature, u_draft, B, k_offsets, V, dtype, out_draft_tokens, nullptr,
+                      workspace, workspace_bytes, stream);
 }
 
 int spec_draft_sample(const void *draft_logits, const float *temperature, const float *u_draft, int B,
                       const int32_t *k_offsets, int V, int dtype, int32_t *out_draft_tokens, void *stream) {
-    return spec_draft_sample_ex(draft_logits, temperature, u_draft, B, k_offsets, V, dtype, out_draft_tokens,
-                                nullptr, 0, stream);
+    return draft_call(draft_logits, temperature, u_draft, B, k_offsets, V, dtype, out_draft_tokens, nullptr,
+                      nullptr, 0, stream);
+}
+
+int spec_draft_sample_lse(const void *draft_logits, const float *temperature, const float *u_draft, int B,
+                          const int32_t *k_offsets, int V, int dtype, int32_t *out_draft_tokens,
+                          double *out_draft_lse2, void *workspace, size_t workspace_bytes, void *stream) {
+    if (B > 0 && !out_draft_lse2) return SPEC_ERR_INVALID_ARG;
+    return draft_call(draft_logits, temperature, u_draft, B, k_offsets, V, dtype, out_draft_tokens, out_draft_lse2,
+                      workspace, workspace_bytes, stream);
+}
+
+int spec_round(const void *target_logits, const void *draft_logits, const float *u_draft, const float *u_accept,
+               const float *u_resample, const float *temperature, int B, const int32_t *k_offsets, int V, int dtype,
+               int32_t *out_draft_tokens, int32_t *out_tokens, int32_t *out_num_accepted, void *stream) {
+    return round_call(target_logits, draft_logits, u_draft, u_accept, u_resample, temperature, B, k_offsets, V,
+                      dtype, out_draft_tokens, out_tokens, out_num_accepted, stream);
 }
 
 int spec_round_host(const void *target_logits_host, const void *draft_logits_host, const float *u_draft_host,
@@ -1491,14 +1632,11 @@ int spec_round_host(const void *target_logits_host, const void *draft_logits_hos
     cudaMemcpyAsync(d + o_ur, u_resample_host, R_t * 4, cudaMemcpyHostToDevice, s);
     cudaMemcpyAsync(d + o_T, temperature_host, B * 4, cudaMemcpyHostToDevice, s);
     cudaMemcpyAsync(d + o_k, k_offsets_host, (B + 1) * 4, cudaMemcpyHostToDevice, s);
-    rc = spec_draft_sample(d + o_d, reinterpret_cast<const float *>(d + o_T), reinterpret_cast<const float *>(d + o_ud),
-                           B, reinterpret_cast<const int32_t *>(d + o_k), V, dtype,
-                           reinterpret_cast<int32_t *>(d + o_xd), stream);
-    if (rc != SPEC_OK) return rc;
-    rc = spec_verify(d + o_t, d + o_d, reinterpret_cast<const int32_t *>(d + o_xd),
-                     reinterpret_cast<const float *>(d + o_ua), reinterpret_cast<const float *>(d + o_ur),
-                     reinterpret_cast<const float *>(d + o_T), B, reinterpret_cast<const int32_t *>(d + o_k), V,
-                     dtype, reinterpret_cast<int32_t *>(d + o_ot), reinterpret_cast<int32_t *>(d + o_on), stream);
+    rc = round_call(d + o_t, d + o_d, reinterpret_cast<const float *>(d + o_ud),
+                    reinterpret_cast<const float *>(d + o_ua), reinterpret_cast<const float *>(d + o_ur),
+                    reinterpret_cast<const float *>(d + o_T), B, reinterpret_cast<const int32_t *>(d + o_k), V, dtype,
+                    reinterpret_cast<int32_t *>(d + o_xd), reinterpret_cast<int32_t *>(d + o_ot),
+                    reinterpret_cast<int32_t *>(d + o_on), stream);
     if (rc != SPEC_OK) return rc;
     if (R_d) cudaMemcpyAsync(out_draft_tokens_host, d + o_xd, R_d * 4, cudaMemcpyDeviceToHost, s);
     cudaMemcpyAsync(out_tokens_host, d + o_ot, R_t * 4, cudaMemcpyDeviceToHost, s);
@@ -1617,10 +1755,10 @@ int spec_verify_noalloc(const void *target_logits, const void *draft_logits, con
         return SPEC_ERR_CUDA;
     const spec_verify_aux_t a{};
     if (dtype == SPEC_F32)
-        return launch_verify<SPEC_F32>(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature,
-                                       B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st, s);
-    return launch_verify<SPEC_BF16>(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature,
-                                    B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st, s);
+        return launch_verify<SPEC_F32>(target_logits, draft_logits, nullptr, draft_tokens, u_accept, u_resample,
+                                       temperature, B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st, s);
+    return launch_verify<SPEC_BF16>(target_logits, draft_logits, nullptr, draft_tokens, u_accept, u_resample,
+                                    temperature, B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st, s);
 }
 
 }  // extern "C"

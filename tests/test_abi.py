@@ -31,7 +31,8 @@ def test_header_declares_expected_entry_points():
     names = declared_functions()
     for n in ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",
               "spec_round_host", "spec_workspace_bytes", "spec_workspace_status",
-              "spec_status_string", "spec_abi_version"):
+              "spec_status_string", "spec_abi_version", "spec_draft_sample_lse", "spec_verify_lse",
+              "spec_round"):
         assert n in names
 
 
@@ -85,3 +86,17 @@ def test_host_argument_errors_launch_nothing(lib):
     assert lib.spec_verify(None, None, None, None, None, None, 0, None, 1000, 0, None, None, None) == 0
     assert lib.spec_draft_sample(None, None, None, 0, None, 1000, 0, None, None) == 0
     assert lib.spec_draft_sample(fake, fake, fake, 4, fake, 1000, 3, fake, None) == -1
+
+
+def test_fused_round_host_argument_errors(lib):
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)  # never dereferenced: validation fails first
+    # the normaliser arrays of the fused path are required
+    assert lib.spec_verify_lse(fake, fake, None, fake, fake, fake, fake, 4, fake, 1000, 0, fake, fake,
+                               None, None, 0, None) == -1
+    assert lib.spec_draft_sample_lse(fake, fake, fake, 4, fake, 1000, 0, fake, None, None, 0, None) == -1
+    # spec_round: null output, bad dtype, V not a multiple of 16 bytes, B == 0 no-op
+    assert lib.spec_round(fake, fake, fake, fake, fake, fake, 4, fake, 1000, 0, fake, None, fake, None) == -1
+    assert lib.spec_round(fake, fake, fake, fake, fake, fake, 4, fake, 1000, 5, fake, fake, fake, None) == -1
+    assert lib.spec_round(fake, fake, fake, fake, fake, fake, 4, fake, 1001, 1, fake, fake, fake, None) == -2
+    assert lib.spec_round(None, None, None, None, None, None, 0, None, 1000, 0, None, None, None, None) == 0

@@ -219,7 +219,8 @@ def algorithmic_bytes(w: Workload, n_sampled: int | None = None) -> dict:
     """Bytes the verify step must move at minimum, by the accounting rule:
     every needed logit row read once (target rows; draft rows of sampled
     sequences only) plus one row-equivalent per sampled sequence for the
-    resample.  Also the draft-sampling pass (every draft row once)."""
+    resample.  Also the draft-sampling pass (every draft row once), and
+    the verify pass that takes the draft rows' normalisers from it."""
     s = w.elem_bytes
     sampled = w.temperature > 0
     ks = w.k
@@ -228,7 +229,10 @@ def algorithmic_bytes(w: Workload, n_sampled: int | None = None) -> dict:
     small = (w.B + 1) * 4 + w.B * 4 + w.rows_draft * 4 * 2 + w.rows_target * 4 * 2 + w.B * 4
     verify = s * w.V * (rows_needed + n_s) + small
     draft = s * w.V * w.rows_draft + w.rows_draft * 4 * 2 + (w.B + 1) * 4 + w.B * 4
-    return dict(verify=int(verify), draft_sample=int(draft),
+    # verify with the draft rows' normalisers given: target rows once, the
+    # resample row-equivalent, and 8 bytes of normaliser per sampled draft row
+    verify_lse = s * w.V * (w.rows_target + n_s) + 8 * int(ks[sampled].sum()) + small
+    return dict(verify=int(verify), draft_sample=int(draft), verify_lse=int(verify_lse),
                 rows_verified=int(w.rows_target + w.rows_draft),
                 rows_needed=int(rows_needed), sampled_sequences=n_s)
 
