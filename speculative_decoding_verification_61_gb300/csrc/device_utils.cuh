@@ -237,26 +237,6 @@ struct Elem<SPEC_BF16> {
 };
 
 // ---------------------------------------------------------------- partials
-// Online-softmax partial over a chunk: s = sum 2^(x*c - m).  NaN in s marks
-// an invalid row (NaN / +inf logit).  m = -inf, s = 0 means no mass.
-struct SoftPart {
-    float m, s;
-};
-
-__device__ __forceinline__ SoftPart soft_merge(SoftPart a, SoftPart b) {
-    if (a.m < b.m) {
-        SoftPart t = a;
-        a = b;
-        b = t;
-    }
-    if (b.m == -INFINITY) {
-        if (b.s != b.s) a.s = b.s;  // keep a NaN marker
-        return a;
-    }
-    a.s = a.s + b.s * ex2(b.m - a.m);
-    return a;
-}
-
 // Arg-max partial: largest value, lowest index among equals; idx = -1 marks
 // a NaN; idx = INT_MAX marks "no element".
 struct ArgPart {
@@ -270,18 +250,8 @@ __device__ __forceinline__ ArgPart arg_merge(ArgPart a, ArgPart b) {
     return a;
 }
 
-__device__ __forceinline__ SoftPart shfl_soft(SoftPart p, int off) {
-    return SoftPart{__shfl_xor_sync(0xffffffffu, p.m, off), __shfl_xor_sync(0xffffffffu, p.s, off)};
-}
-
 __device__ __forceinline__ ArgPart shfl_arg(ArgPart p, int off) {
     return ArgPart{__shfl_xor_sync(0xffffffffu, p.v, off), __shfl_xor_sync(0xffffffffu, p.i, off)};
-}
-
-__device__ __forceinline__ SoftPart warp_soft(SoftPart p) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) p = soft_merge(p, shfl_soft(p, off));
-    return p;
 }
 
 __device__ __forceinline__ ArgPart warp_arg(ArgPart p) {

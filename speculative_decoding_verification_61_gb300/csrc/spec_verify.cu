@@ -119,65 +119,6 @@ __device__ int block_excl_scan(int v, int *s_warp, int *total) {
     return r;
 }
 
-__device__ double block_excl_scan_d(double v, double *s_warp, double *total) {
-    const int lane = lane_id(), w = warp_id(), nw = blockDim.x >> 5;
-    double incl = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        double n = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += n;
-    }
-    if (lane == 31) s_warp[w] = incl;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        double acc = 0.0;
-        for (int i = 0; i < nw; ++i) {
-            double t = s_warp[i];
-            s_warp[i] = acc;
-            acc += t;
-        }
-        s_warp[nw] = acc;
-    }
-    __syncthreads();
-    const double r = incl - v + s_warp[w];
-    *total = s_warp[nw];
-    __syncthreads();
-    return r;
-}
-
-__device__ int block_min_int(int v, int *s_warp) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, off));
-    if (lane_id() == 0) s_warp[warp_id()] = v;
-    __syncthreads();
-    int r = s_warp[0];
-    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) r = min(r, s_warp[i]);
-    __syncthreads();
-    return r;
-}
-
-__device__ int block_max_int(int v, int *s_warp) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, off));
-    if (lane_id() == 0) s_warp[warp_id()] = v;
-    __syncthreads();
-    int r = s_warp[0];
-    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) r = max(r, s_warp[i]);
-    __syncthreads();
-    return r;
-}
-
-__device__ double block_sum_d(double v, double *s_warp) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    if (lane_id() == 0) s_warp[warp_id()] = v;
-    __syncthreads();
-    double r = 0.0;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) r += s_warp[i];
-    __syncthreads();
-    return r;
-}
-
 // ------------------------------------------------------------ unit tickets
 // stats_kernel hands out its units dynamically: an SM that streams faster
 // takes more of them, so all CTAs finish together.  Ticket t (one atomic
@@ -503,6 +444,54 @@ struct Acc2 {
     __device__ __forceinline__ float value() const { return hi + lo; }
 };
 
+// Unevaluated sum hi + lo of two fp32 values, |lo| <= ulp(hi) / 2 once
+// normalised: about 44 bits of precision from fp32 operations.  The running
+// masses of the inverse CDF use it instead of fp64, whose pipe is a small
+// fraction of GB300's fp32 rate.  (Error-free sums after Knuth and Dekker.)
+struct F2 {
+    float hi, lo;
+};
+
+__device__ __forceinline__ F2 f2_two_sum(float a, float b) {  // a + b = hi + lo exactly
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    return F2{s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+
+__device__ __forceinline__ F2 f2_norm(float s, float e) {  // |s| >= |e| (or s == 0)
+    const float t = __fadd_rn(s, e);
+    return F2{t, __fsub_rn(e, __fsub_rn(t, s))};
+}
+
+__device__ __forceinline__ F2 f2_add(F2 a, float b) {
+    const F2 t = f2_two_sum(a.hi, b);
+    return f2_norm(t.hi, __fadd_rn(t.lo, a.lo));
+}
+
+__device__ __forceinline__ F2 f2_sub(F2 a, F2 b) {
+    const F2 t = f2_two_sum(a.hi, -b.hi);
+    return f2_norm(t.hi, __fadd_rn(t.lo, __fsub_rn(a.lo, b.lo)));
+}
+
+__device__ __forceinline__ F2 f2_scale(float u, F2 a) {  // u * (hi + lo)
+    const float p = __fmul_rn(u, a.hi);
+    return f2_norm(p, __fmaf_rn(u, a.lo, __fmaf_rn(u, a.hi, -p)));
+}
+
+__device__ __forceinline__ bool f2_gt(F2 a, F2 b) {
+    const F2 d = f2_sub(a, b);
+    return d.hi > 0.0f || (d.hi == 0.0f && d.lo > 0.0f);
+}
+
+__device__ __forceinline__ F2 shfl_f2(F2 v, int src) {
+    return F2{__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+
+// Largest fp32 value <= hi + lo (normalised pair).
+__device__ __forceinline__ float f2_round_down(F2 x) {
+    return x.lo < 0.0f ? nextafterf(x.hi, -INFINITY) : x.hi;
+}
+
 __device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
@@ -527,28 +516,34 @@ __device__ __forceinline__ double lse2(float M, float S) {
     return static_cast<double>(M) + static_cast<double>(e) + static_cast<double>(log2f(m));
 }
 
-// Row combine of the n sub-chunk partials of one row by a whole warp:
-// M = max of the partial maxima, S = sum s_i 2^(m_i - M) (>= 1).  The
-// first 32 * kCache partials are loaded once into registers (one memory
-// round trip for rows of up to 256 sub-chunks); lane l adds its partials in
-// index order whether cached or not.
-__device__ bool warp_combine_soft(const float2 *p, int n, float *M_out, float *S_out) {
+// Sub-chunk partials a lane holds in registers: p[lane + 32 j], j < 8, so
+// rows of up to 256 sub-chunks take one memory round trip; the rest of a
+// longer row is read again where needed.
+constexpr int kPartCache = 8;
+
+__device__ __forceinline__ void load_parts(const float2 *p, int n, float2 (&c)[kPartCache]) {
     const int lane = lane_id();
-    constexpr int kCache = 8;
-    float2 cache[kCache];
 #pragma unroll
-    for (int j = 0; j < kCache; ++j) {
+    for (int j = 0; j < kPartCache; ++j) {
         const int i = lane + 32 * j;
-        cache[j] = (i < n) ? __ldcg(p + i) : make_float2(-INFINITY, 0.0f);
+        c[j] = (i < n) ? __ldcg(p + i) : make_float2(-INFINITY, 0.0f);
     }
+}
+
+// Row combine of the n sub-chunk partials of one row by a whole warp:
+// M = max of the partial maxima, S = sum s_i 2^(m_i - M) (>= 1); lane l
+// adds its partials in index order whether cached or not.
+__device__ bool combine_soft(const float2 (&cache)[kPartCache], const float2 *p, int n, float *M_out,
+                             float *S_out) {
+    const int lane = lane_id();
     float M = -INFINITY;
     bool nan = false;
 #pragma unroll
-    for (int j = 0; j < kCache; ++j) {
+    for (int j = 0; j < kPartCache; ++j) {
         nan |= (cache[j].y != cache[j].y);
         M = fmaxf(M, cache[j].x);
     }
-    for (int i = lane + 32 * kCache; i < n; i += 32) {
+    for (int i = lane + 32 * kPartCache; i < n; i += 32) {
         const float2 v = __ldcg(p + i);
         nan |= (v.y != v.y);
         M = fmaxf(M, v.x);
@@ -559,9 +554,9 @@ __device__ bool warp_combine_soft(const float2 *p, int n, float *M_out, float *S
     if (nan || !(M > -INFINITY) || !(M < INFINITY)) return false;
     Acc2 acc;
 #pragma unroll
-    for (int j = 0; j < kCache; ++j)
+    for (int j = 0; j < kPartCache; ++j)
         if (cache[j].x > -INFINITY) acc.add(cache[j].y * ex2(cache[j].x - M));
-    for (int i = lane + 32 * kCache; i < n; i += 32) {
+    for (int i = lane + 32 * kPartCache; i < n; i += 32) {
         const float2 v = __ldcg(p + i);
         if (v.x > -INFINITY) acc.add(v.y * ex2(v.x - M));
     }
@@ -570,6 +565,12 @@ __device__ bool warp_combine_soft(const float2 *p, int n, float *M_out, float *S
     *M_out = M;
     *S_out = S;
     return true;
+}
+
+__device__ bool warp_combine_soft(const float2 *p, int n, float *M_out, float *S_out) {
+    float2 cache[kPartCache];
+    load_parts(p, n, cache);
+    return combine_soft(cache, p, n, M_out, S_out);
 }
 
 // Arg-max over the n sub-chunk partials of one row; -1 if a NaN was seen.
@@ -583,55 +584,69 @@ __device__ int warp_combine_arg(const float2 *p, int n) {
     return a.i == INT_MAX ? -1 : a.i;
 }
 
-// Warp-level locate over n non-negative weights wsub(i) (sub-chunk masses):
-// total Z, target = u * Z, and the first i whose cumulative mass exceeds the
+// Warp-level locate over n non-negative weights (sub-chunk masses): total
+// Z, target = u * Z, and the first i whose cumulative mass exceeds the
 // target, with the mass before it.  If rounding leaves no such i, the last
-// i with positive weight.  Returns -1 if every weight is 0.
-template <class WS>
-__device__ int warp_locate(int n, WS wsub, float u, double *before, double *total, double *target_out) {
+// i with positive weight.  Returns -1 if every weight is 0.  Weight i is
+// cache[j] of lane i % 32 for i = lane + 32 j < 32 * kPartCache, wfar(i)
+// beyond.
+template <class WF>
+__device__ int warp_locate(int n, const float (&cache)[kPartCache], WF wfar, float u, F2 *before, F2 *total,
+                           F2 *target_out) {
     const int lane = lane_id();
-    constexpr int kCache = 8;  // n <= 256: one load per cached slot
-    float cache[kCache];
-#pragma unroll
-    for (int j = 0; j < kCache; ++j) {
-        const int i = lane + 32 * j;
-        cache[j] = (i < n) ? wsub(i) : 0.0f;
-    }
+    constexpr int kCache = kPartCache;
     Acc2 acc;
 #pragma unroll
     for (int j = 0; j < kCache; ++j) acc.add(cache[j]);
-    for (int j = kCache; 32 * j < n; ++j) acc.add((lane + 32 * j < n) ? wsub(lane + 32 * j) : 0.0f);
-    const double tot = static_cast<double>(warp_sum_f(acc.hi)) + static_cast<double>(warp_sum_f(acc.lo));
-    const double target = static_cast<double>(u) * tot;
+    for (int j = kCache; 32 * j < n; ++j) acc.add((lane + 32 * j < n) ? wfar(lane + 32 * j) : 0.0f);
+    const F2 tot = f2_two_sum(warp_sum_f(acc.hi), warp_sum_f(acc.lo));
+    const F2 target = f2_scale(u, tot);
     *total = tot;
     *target_out = target;
-    double carry = 0.0, last_before = 0.0;
+    F2 carry{0.0f, 0.0f}, last_before{0.0f, 0.0f};
     int last = -1;
     for (int j = 0; 32 * j < n; ++j) {
         float w = 0.0f;
 #pragma unroll
         for (int q = 0; q < kCache; ++q)
             if (q == j) w = cache[q];
-        if (j >= kCache) w = (lane + 32 * j < n) ? wsub(lane + 32 * j) : 0.0f;
+        if (j >= kCache) w = (lane + 32 * j < n) ? wfar(lane + 32 * j) : 0.0f;
         const float incl = warp_incl_scan_f(w);
-        const double cum = carry + static_cast<double>(incl);
-        const unsigned hit = __ballot_sync(0xffffffffu, w > 0.0f && cum > target);
+        const F2 cum = f2_add(carry, incl);
+        const unsigned hit = __ballot_sync(0xffffffffu, w > 0.0f && f2_gt(cum, target));
         if (hit) {
             const int src = __ffs(hit) - 1;
-            const double bef = carry + static_cast<double>(incl - w);
-            *before = __shfl_sync(0xffffffffu, bef, src);
+            *before = shfl_f2(f2_add(carry, incl - w), src);
             return 32 * j + src;
         }
         const unsigned pos = __ballot_sync(0xffffffffu, w > 0.0f);
         if (pos) {
             const int src = 31 - __clz(pos);
             last = 32 * j + src;
-            last_before = __shfl_sync(0xffffffffu, carry + static_cast<double>(incl - w), src);
+            last_before = shfl_f2(f2_add(carry, incl - w), src);
         }
-        carry = __shfl_sync(0xffffffffu, cum, 31);
+        carry = shfl_f2(cum, 31);
     }
     *before = last_before;
     return last;
+}
+
+#ifndef SPEC_RESID_PREFETCH
+#define SPEC_RESID_PREFETCH 1
+#endif
+#ifndef SPEC_RESID_L2HINT
+#define SPEC_RESID_L2HINT 0
+#endif
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+#if SPEC_RESID_L2HINT
+    uint4 v;
+    asm volatile("ld.global.nc.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+#else
+    return __ldg(p);
+#endif
 }
 
 // Element range of sub-chunk sc of a row.
@@ -643,14 +658,26 @@ __device__ __forceinline__ void sub_range(const Geometry &g, int sc, int *a, int
     *b = min(c1, *a + g.sub_elems);
 }
 
+// Vector j (0..3, not a compile-time constant) of four held in registers:
+// a chain of selects, so that the loops over j below stay rolled.
+__device__ __forceinline__ uint4 pick4(const uint4 (&r)[4], int j) {
+    uint4 v = r[3];
+    v = (j == 2) ? r[2] : v;
+    v = (j == 1) ? r[1] : v;
+    return (j == 0) ? r[0] : v;
+}
+
 // Warp-level inverse CDF inside elements [a, b) (at most one sub-chunk) of
 // one or two rows: lane l owns vectors 4l .. 4l+3 (contiguous), weights are
 // W(x_row1, x_row2).  Returns the first element whose cumulative mass,
 // starting at `before`, exceeds `target`; else the last element with
 // positive weight (rounding fallback); else -1.
+// This runs once per draw, at the end of a kernel, so its code is kept
+// small: the loops over a lane's four vectors are rolled (fully unrolled,
+// the first pass of a draw stalled for several microseconds on
+// instruction fetches).
 template <int DT, class WF>
-__device__ int warp_scan_elems(const void *row1, const void *row2, int a, int b, WF W, double before,
-                               double target) {
+__device__ int warp_scan_elems(const void *row1, const void *row2, int a, int b, WF W, F2 before, F2 target) {
     using E = Elem<DT>;
     constexpr int PV = E::kPerVec;
     const int lane = lane_id();
@@ -663,34 +690,36 @@ __device__ int warp_scan_elems(const void *row1, const void *row2, int a, int b,
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int vi = 4 * lane + j;
+        r1[j] = make_uint4(0u, 0u, 0u, 0u);
+        r2[j] = r1[j];
         if (vi < nvec) {
             r1[j] = __ldg(p1 + vi);
             r2[j] = (row2 != row1) ? __ldg(p2 + vi) : r1[j];
         }
     }
+    // this lane's vectors are 4 * lane .. 4 * lane + nv - 1
+    const int nv = max(0, min(4, nvec - 4 * lane));
     // weights are recomputed in the second pass (same fp32 operations, same
     // order) instead of being kept live
     float lsum = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        if (4 * lane + j >= nvec) continue;
+#pragma unroll 1
+    for (int j = 0; j < nv; ++j) {
         float x1[PV], x2[PV];
-        E::unpack(r1[j], x1);
-        E::unpack(r2[j], x2);
+        E::unpack(pick4(r1, j), x1);
+        E::unpack(pick4(r2, j), x2);
 #pragma unroll
         for (int q = 0; q < PV; ++q) lsum += W(x1[q], x2[q]);
     }
     const float incl = warp_incl_scan_f(lsum);
-    const double start = before + static_cast<double>(incl - lsum);
-    const float rem = __double2float_rd(target - start);  // acc > rem  <=>  start + acc > target
+    const F2 start = f2_add(before, incl - lsum);
+    const float rem = f2_round_down(f2_sub(target, start));  // acc > rem  <=>  start + acc > target
     float acc = 0.0f;
     int found = -1, lastpos = -1;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        if (4 * lane + j >= nvec) continue;
+#pragma unroll 1
+    for (int j = 0; j < nv; ++j) {
         float x1[PV], x2[PV];
-        E::unpack(r1[j], x1);
-        E::unpack(r2[j], x2);
+        E::unpack(pick4(r1, j), x1);
+        E::unpack(pick4(r2, j), x2);
 #pragma unroll
         for (int q = 0; q < PV; ++q) {
             const float wv = W(x1[q], x2[q]);
@@ -711,16 +740,20 @@ __device__ int warp_scan_elems(const void *row1, const void *row2, int a, int b,
 }
 
 // One draw from a soft row (bonus token or draft token) by one warp:
-// locate the sub-chunk from its partials, then scan its elements.
+// locate the sub-chunk from the row's partials (pc: this lane's cached ones,
+// from load_parts), then scan its elements.
 template <int DT>
-__device__ int warp_draw_row(const void *logits, int64_t row, const float2 *part, const Geometry &g, float c,
-                             float M, float u) {
-    auto wsub = [&](int i) -> float {
+__device__ int warp_draw_row(const void *logits, int64_t row, const float2 *part, const float2 (&pc)[kPartCache],
+                             const Geometry &g, float c, float M, float u) {
+    float w[kPartCache];
+#pragma unroll
+    for (int j = 0; j < kPartCache; ++j) w[j] = pc[j].x > -INFINITY ? pc[j].y * ex2(pc[j].x - M) : 0.0f;
+    auto wfar = [&](int i) -> float {
         const float2 v = __ldcg(part + i);
         return v.x > -INFINITY ? v.y * ex2(v.x - M) : 0.0f;
     };
-    double before, total, target;
-    const int sc = warp_locate(g.n_sub, wsub, u, &before, &total, &target);
+    F2 before, total, target;
+    const int sc = warp_locate(g.n_sub, w, wfar, u, &before, &total, &target);
     if (sc < 0) return -1;
     int a, b;
     sub_range(g, sc, &a, &b);
@@ -963,7 +996,10 @@ __global__ void __launch_bounds__(256, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
     if (kind == kJobBonus) {
         // --- bonus draw from p at position k, by block 0 of b --------------
         if (s != 0 || warp != 0) return;
-        const int token = warp_draw_row<DT>(target, trow, ws.part + trow * g.n_sub, g, c, sm.M[k], sm.u);
+        const float2 *pr = ws.part + trow * g.n_sub;
+        float2 pc[kPartCache];
+        load_parts(pr, g.n_sub, pc);
+        const int token = warp_draw_row<DT>(target, trow, pr, pc, g, c, sm.M[k], sm.u);
         if (lane == 0) out_tokens[trow] = token;
         return;
     }
@@ -977,7 +1013,7 @@ __global__ void __launch_bounds__(256, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
     const int per = (g.n_sub + nsplit - 1) / nsplit;
     const int sc_begin = s * per;
     const int sc_end = min(g.n_sub, (s + 1) * per);
-    if (warp == 0 && sc_begin < sc_end) {
+    if (SPEC_RESID_PREFETCH && warp == 0 && sc_begin < sc_end) {
         // the slice of both rows goes to L2 in bulk (up to 32 KB per lane),
         // so the warps' loads below wait on L2, not on DRAM round trips
         int a0, a1, e0, e1;
@@ -1005,8 +1041,8 @@ __global__ void __launch_bounds__(256, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
         for (int j = 0; j < 4; ++j) {
             const int i = lane + 32 * j;
             if (i < nvec) {
-                xt4[j] = __ldg(pt + i);
-                xd4[j] = __ldg(pd + i);
+                xt4[j] = ld_stream(pt + i);
+                xd4[j] = ld_stream(pd + i);
             }
         }
         float2 acc0 = make_float2(0.0f, 0.0f), acc1 = acc0;
@@ -1033,9 +1069,12 @@ __global__ void __launch_bounds__(256, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
     __syncwarp();  // lane 0's acquire, before the other lanes' reads
 
     // --- 3. the residual draw, by the last warp of b -----------------------
-    auto wsub = [&](int i) -> float { return __ldcg(rp + i); };
-    double before, Z, tgt;
-    const int sc = warp_locate(g.n_sub, wsub, sm.u, &before, &Z, &tgt);
+    float w[kPartCache];
+#pragma unroll
+    for (int j = 0; j < kPartCache; ++j) w[j] = (lane + 32 * j < g.n_sub) ? __ldcg(rp + lane + 32 * j) : 0.0f;
+    auto wfar = [&](int i) -> float { return __ldcg(rp + i); };
+    F2 before, Z, tgt;
+    const int sc = warp_locate(g.n_sub, w, wfar, sm.u, &before, &Z, &tgt);
     int token = -1;
     if (sc >= 0) {
         int a, e1;
@@ -1047,7 +1086,7 @@ __global__ void __launch_bounds__(256, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
     }
     if (lane == 0) {
         out_tokens[trow] = token;
-        if (aux.residual_mass) aux.residual_mass[b] = static_cast<float>(Z);
+        if (aux.residual_mass) aux.residual_mass[b] = __fadd_rn(Z.hi, Z.lo);
     }
 }
 
@@ -1097,9 +1136,11 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
             token = warp_combine_arg(pr, g.n_sub);
         } else if (c == c) {
             float M, S;
-            if (warp_combine_soft(pr, g.n_sub, &M, &S)) {
+            float2 pc[kPartCache];
+            load_parts(pr, g.n_sub, pc);  // one round trip serves the combine and the draw
+            if (combine_soft(pc, pr, g.n_sub, &M, &S)) {
                 L = lse2(M, S);
-                token = warp_draw_row<DT>(draft, r, pr, g, c, M, u_draft[r]);
+                token = warp_draw_row<DT>(draft, r, pr, pc, g, c, M, u_draft[r]);
             }
         }
         if (lane == 0) {
@@ -1369,6 +1410,9 @@ int launch_verify(const void *target, const void *draft, const double *draft_lse
     return SPEC_OK;
 }
 
+#ifndef SPEC_SELECT_BLOCKS_PER_SM
+#define SPEC_SELECT_BLOCKS_PER_SM 8
+#endif
 template <int DT>
 int launch_draft(const void *draft, const float *temperature, const float *u_draft, int B,
                  const int32_t *k_offsets, const Geometry &g, int32_t *out, double *out_lse2, void *ws_base,
@@ -1378,8 +1422,9 @@ int launch_draft(const void *draft, const float *temperature, const float *u_dra
     pick_ring(st, B, &ns, &smem, &per_sm);
     if (ns == 0) return SPEC_ERR_INVALID_ARG;
     const WsPtrs w = ws_ptrs(ws_base, l);
-    // one warp per draft row: at most B * kMaxK rows, 8 warps per block
-    const int grid = static_cast<int>(std::min(static_cast<int64_t>(st.sms) * 8, (static_cast<int64_t>(B) * kMaxK + 7) / 8));
+    // one warp per draft row (grid-stride): at most B * kMaxK rows, 8 warps per block
+    const int grid = static_cast<int>(
+        std::min(static_cast<int64_t>(st.sms) * SPEC_SELECT_BLOCKS_PER_SM, (static_cast<int64_t>(B) * kMaxK + 7) / 8));
     if (!cuda_ok(launch_k(false, stats_kernel<DT, kModeDraft>, dim3(st.sms * per_sm), dim3(kThreads), smem, stream,
                           draft, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, nullptr),
                  "launch stats_kernel") ||
