@@ -34,6 +34,10 @@ def _bind(lib):
                                   vp, vp, vp, vp, vp, vp, ip, ip]
     lib.oracle_draft_sample.restype = ip
     lib.oracle_draft_sample.argtypes = [vp, ip, vp, vp, ip, vp, ip, vp, vp, vp, ip]
+    lib.oracle_tree_verify.restype = ip
+    lib.oracle_tree_verify.argtypes = [vp, vp, ip, vp, vp, vp, vp, vp, vp, ip, ip, vp, vp, vp, vp, ip]
+    lib.oracle_tree_draft_sample.restype = ip
+    lib.oracle_tree_draft_sample.argtypes = [vp, ip, vp, vp, vp, vp, ip, ip, vp, vp, ip]
     lib.oracle_softmax_row.restype = ip
     lib.oracle_softmax_row.argtypes = [vp, ip, ip, ctypes.c_double, vp, vp]
     return lib
@@ -115,6 +119,52 @@ def draft_sample(draft_logits, temperature, u_draft, k_offsets, nthreads: int = 
     rc = lib.oracle_draft_sample(_ptr(dl), dt, _ptr(tp), _ptr(ud), B, _ptr(k_offsets), V,
                                  _ptr(out), _ptr(margin), _ptr(lse), nthreads)
     return VerifyResult(rc=rc, tokens=out, margin=margin, lse=lse)
+
+
+def tree_verify(target_logits, draft_logits, node_offsets, parent, tokens, u_accept, u_resample,
+                temperature, nthreads: int = 1, lib=None):
+    """Oracle tree (multi-candidate) verify.  Logits [N, V] (float32 or uint16
+    bf16 bits), one target and one draft row per node.  Returns tokens [N],
+    num_accepted [B], last_node [B], margin [B]."""
+    lib = lib or load()
+    tl = np.ascontiguousarray(target_logits)
+    dl = np.ascontiguousarray(draft_logits)
+    dt = _dtype_code(tl)
+    no = _c(node_offsets, np.int32)
+    B = len(no) - 1
+    V = tl.shape[-1]
+    N = int(no[-1]) if B > 0 else 0
+    out_tokens = np.full(N, -7, dtype=np.int32)
+    out_num = np.full(B, -7, dtype=np.int32)
+    out_last = np.full(B, -7, dtype=np.int32)
+    margin = np.full(B, np.inf)
+    pa, tk = _c(parent, np.int32), _c(tokens, np.int32)
+    ua, ur, tp = _c(u_accept, np.float32), _c(u_resample, np.float32), _c(temperature, np.float32)
+    rc = lib.oracle_tree_verify(_ptr(tl), _ptr(dl), dt, _ptr(no), _ptr(pa), _ptr(tk), _ptr(ua), _ptr(ur),
+                                _ptr(tp), B, V, _ptr(out_tokens), _ptr(out_num), _ptr(out_last),
+                                _ptr(margin), nthreads)
+    return VerifyResult(rc=rc, tokens=out_tokens, num_accepted=out_num, last_node=out_last,
+                        margin=margin)
+
+
+def tree_draft_sample(draft_logits, node_offsets, parent, temperature, u_draft, nthreads: int = 1,
+                      lib=None):
+    """Oracle tree drafting: each non-root node's token from its parent's
+    draft row.  Returns tokens [N] (-1 for roots) and margin [N]."""
+    lib = lib or load()
+    dl = np.ascontiguousarray(draft_logits)
+    dt = _dtype_code(dl)
+    no = _c(node_offsets, np.int32)
+    B = len(no) - 1
+    V = dl.shape[-1]
+    N = int(no[-1]) if B > 0 else 0
+    out = np.full(N, -7, dtype=np.int32)
+    margin = np.full(N, np.inf)
+    pa = _c(parent, np.int32)
+    tp, ud = _c(temperature, np.float32), _c(u_draft, np.float32)
+    rc = lib.oracle_tree_draft_sample(_ptr(dl), dt, _ptr(no), _ptr(pa), _ptr(tp), _ptr(ud), B, V,
+                                      _ptr(out), _ptr(margin), nthreads)
+    return VerifyResult(rc=rc, tokens=out, margin=margin)
 
 
 def softmax_row(logits_row, T: float, lib=None):

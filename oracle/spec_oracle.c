@@ -426,3 +426,261 @@ int oracle_softmax_row(const void *logits, int dtype, int V, double T, double *p
     free(z);
     return rc;
 }
+
+/* ------------------------------------------------------------------------
+ * Tree (multi-candidate) verify.
+ *
+ * The pages show draft trees (docs.ifdog.com "投机解码", 进阶方案: Medusa and
+ * EAGLE verify a tree of candidates in one target forward) but give no
+ * acceptance rule for them.  Reading taken: the plainest lossless extension
+ * of the single-candidate rule of 三步流程 step 3 / [P3] 二.1-二.2 to several
+ * candidates drawn i.i.d. from the same draft distribution.  At node u with
+ * target distribution p (the target row of u) and draft distribution q (the
+ * draft row of u), u's children c_1 < c_2 < ... (ascending node index) are
+ * tried in order:
+ *   - child c_j is accepted iff u_accept[c_j] < min(1, p^(j-1)(x) / q(x)),
+ *     x its token, p^(0) = p;
+ *   - on its rejection p^(j) = norm(max(0, p^(j-1) - q));
+ *   - an accepted child becomes u, with p and q of its own rows;
+ *   - when every child of u is rejected, one token is drawn from the last
+ *     residual with u_resample[u] by inverse CDF (ascending vocabulary, on
+ *     the unnormalised weights max(0, p^(m-1) - q), as the single-candidate
+ *     residual draw); a node without children (a leaf, or the root of a
+ *     one-node tree) draws the bonus token from its p.
+ * Greedy (T = 0): the first child whose token equals argmax p (lowest index
+ * on ties) is accepted; if none, argmax p is emitted.
+ * Degenerate: if a residual mass rounds to 0, p^(j) = p^(j-1) (margin 0).
+ * Every convention of the chain verify above (temperature, strict test,
+ * q(x) = 0, data errors) carries over.
+ * ---------------------------------------------------------------------- */
+#define ORACLE_MAX_TREE 64
+
+typedef struct {
+    const void *target, *draft;
+    int dtype, V;
+    const int32_t *node_offsets, *parent, *tokens;
+    const float *u_accept, *u_resample, *temperature;
+    int32_t *out_tokens, *out_num, *out_last;
+    double *margin;
+} tree_args;
+
+/* Nodes of sequence b are valid: 1..ORACLE_MAX_TREE of them, the first is
+ * the root (parent -1), every other node's parent is an earlier node of the
+ * same sequence. */
+static int valid_tree(const tree_args *a, int b)
+{
+    const int32_t g0 = a->node_offsets[b], n = a->node_offsets[b + 1] - g0;
+    if (n < 1 || n > ORACLE_MAX_TREE) return 0;
+    if (a->parent[g0] != -1) return 0;
+    for (int i = 1; i < n; ++i) {
+        int32_t pa = a->parent[g0 + i];
+        if (pa < g0 || pa >= g0 + i) return 0;
+    }
+    return 1;
+}
+
+/* One sequence of the tree verify.  p, q, w: scratch rows of V doubles. */
+static void tree_verify_one(const tree_args *a, int b, double *rt, double *rd, double *p, double *q,
+                            double *w)
+{
+    const int V = a->V;
+    const int32_t g0 = a->node_offsets[b], n = a->node_offsets[b + 1] - g0;
+    for (int i = 0; i < n; ++i) a->out_tokens[g0 + i] = -1;
+    a->out_num[b] = -1;
+    if (a->out_last) a->out_last[b] = -1;
+    if (a->margin) a->margin[b] = INFINITY;
+    if (!valid_tree(a, b)) return;
+    const float Tf = a->temperature[b];
+    if (!valid_temperature(Tf)) return;
+    for (int i = 1; i < n; ++i)
+        if (a->tokens[g0 + i] < 0 || a->tokens[g0 + i] >= V) return;
+    const double T = (double)Tf;
+
+    int32_t path[ORACLE_MAX_TREE];
+    int nacc = 0;
+    int32_t u = g0, token = -1;
+    double mg = INFINITY;
+    for (;;) {
+        if (T == 0.0) {
+            /* greedy: the first child whose token is argmax p */
+            int am;
+            load_row(a->target, a->dtype, u, V, rt);
+            if (row_argmax(rt, V, &am) != 0) return;
+            int32_t next = -1;
+            for (int32_t c = u + 1; c < g0 + n && next < 0; ++c)
+                if (a->parent[c] == u && a->tokens[c] == am) next = c;
+            if (next < 0) {
+                token = am;
+                break;
+            }
+            path[nacc++] = a->tokens[next];
+            u = next;
+            continue;
+        }
+        double Lt, Ld = 0.0;
+        load_row(a->target, a->dtype, u, V, rt);
+        if (row_lse(rt, V, T, &Lt) != 0) return;
+        for (int v = 0; v < V; ++v) p[v] = exp(rt[v] / T - Lt);
+        int has_child = 0;
+        for (int32_t c = u + 1; c < g0 + n; ++c) has_child |= a->parent[c] == u;
+        if (!has_child) {
+            /* a leaf: the bonus token from p */
+            double m;
+            token = inverse_cdf(p, V, (double)a->u_resample[u], &m);
+            if (m < mg) mg = m;
+            break;
+        }
+        load_row(a->draft, a->dtype, u, V, rd);
+        if (row_lse(rd, V, T, &Ld) != 0) return;
+        for (int v = 0; v < V; ++v) q[v] = exp(rd[v] / T - Ld);
+        int32_t next = -1, j = 0;
+        for (int32_t c = u + 1; c < g0 + n; ++c) {
+            if (a->parent[c] != u) continue;
+            const int32_t x = a->tokens[c];
+            double alpha;
+            if (rd[x] == -INFINITY) {
+                alpha = p[x] > 0.0 ? 1.0 : 0.0;
+            } else if (j == 0) {
+                /* first candidate: the ratio in the log domain, as the chain */
+                double r = rt[x] == -INFINITY ? 0.0 : exp((rt[x] / T - Lt) - (rd[x] / T - Ld));
+                alpha = r < 1.0 ? r : 1.0;
+            } else {
+                double r = p[x] / q[x];
+                alpha = r < 1.0 ? r : 1.0;
+            }
+            const double uc = (double)a->u_accept[c];
+            const double d = fabs(uc - alpha);
+            if (d < mg) mg = d;
+            if (uc < alpha) {
+                next = c;
+                break;
+            }
+            /* rejected: p <- norm(max(0, p - q)) */
+            double Z = 0.0;
+            for (int v = 0; v < V; ++v) {
+                double e = p[v] - q[v];
+                w[v] = e > 0.0 ? e : 0.0;
+                Z += w[v];
+            }
+            if (Z > 0.0) {
+                for (int v = 0; v < V; ++v) p[v] = w[v] / Z;
+            } else {
+                mg = 0.0;
+                for (int v = 0; v < V; ++v) w[v] = p[v];
+            }
+            ++j;
+        }
+        if (next >= 0) {
+            path[nacc++] = a->tokens[next];
+            u = next;
+            continue;
+        }
+        /* every child rejected: draw from the last residual weights */
+        double m;
+        token = inverse_cdf(w, V, (double)a->u_resample[u], &m);
+        if (m < mg) mg = m;
+        break;
+    }
+    for (int i = 0; i < nacc; ++i) a->out_tokens[g0 + i] = path[i];
+    a->out_tokens[g0 + nacc] = token;
+    a->out_num[b] = nacc;
+    if (a->out_last) a->out_last[b] = u;
+    if (a->margin) a->margin[b] = mg;
+}
+
+/*
+ * Tree verify of B sequences.  Sequence b owns nodes node_offsets[b] ..
+ * node_offsets[b+1]-1 (the first is its root); parent [N] (-1 for a root),
+ * tokens [N] (a root's is ignored), target and draft logits [N, V] (row g:
+ * the distributions after the path to node g; draft rows of leaves are not
+ * read), u_accept [N] (the test of node g), u_resample [N] (the draw at node
+ * g), temperature [B].  Outputs: out_tokens [N] (the accepted path's tokens,
+ * then the drawn token, then -1, from slot node_offsets[b]),
+ * out_num_accepted [B], out_last_node [B] and margin [B] (may be NULL).
+ * Returns 0, or -1 if node_offsets is invalid (node_offsets[0] != 0 or a
+ * sequence without 1..64 nodes; then every out_num_accepted = -1).
+ */
+int oracle_tree_verify(const void *target_logits, const void *draft_logits, int dtype,
+                       const int32_t *node_offsets, const int32_t *parent, const int32_t *tokens,
+                       const float *u_accept, const float *u_resample, const float *temperature,
+                       int B, int V, int32_t *out_tokens, int32_t *out_num_accepted,
+                       int32_t *out_last_node, double *margin, int nthreads)
+{
+    if (B < 0 || V <= 0 || (dtype != ORACLE_F32 && dtype != ORACLE_BF16)) return -2;
+    if (B == 0) return 0;
+    int ok = node_offsets[0] == 0;
+    for (int b = 0; b < B && ok; ++b) {
+        int32_t n = node_offsets[b + 1] - node_offsets[b];
+        ok = n >= 1 && n <= ORACLE_MAX_TREE;
+    }
+    if (!ok) {
+        for (int b = 0; b < B; ++b) out_num_accepted[b] = -1;
+        return -1;
+    }
+    tree_args a = {target_logits, draft_logits, dtype, V, node_offsets, parent, tokens, u_accept,
+                   u_resample, temperature, out_tokens, out_num_accepted, out_last_node, margin};
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+    {
+        double *buf = (double *)malloc(sizeof(double) * (size_t)V * 5);
+#pragma omp for schedule(dynamic, 1)
+        for (int b = 0; b < B; ++b)
+            tree_verify_one(&a, b, buf, buf + V, buf + 2 * (size_t)V, buf + 3 * (size_t)V, buf + 4 * (size_t)V);
+        free(buf);
+    }
+    return 0;
+}
+
+/*
+ * Tree drafting: every non-root node g takes its token from the draft
+ * distribution of its parent, x_g = argmax z (T_b = 0) or the inverse-CDF
+ * draw from softmax(z / T_b) at u_draft[g], z the draft row of parent(g):
+ * siblings are independent draws from one distribution, as the tree verify
+ * above requires.  Roots and invalid rows give -1; margin [N] as for the
+ * chain draft sample.
+ */
+int oracle_tree_draft_sample(const void *draft_logits, int dtype, const int32_t *node_offsets,
+                             const int32_t *parent, const float *temperature, const float *u_draft,
+                             int B, int V, int32_t *out_tokens, double *margin, int nthreads)
+{
+    if (B < 0 || V <= 0 || (dtype != ORACLE_F32 && dtype != ORACLE_BF16)) return -2;
+    if (B == 0) return 0;
+    const int N = node_offsets[B];
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+    {
+        double *z = (double *)malloc(sizeof(double) * (size_t)V);
+        double *w = (double *)malloc(sizeof(double) * (size_t)V);
+#pragma omp for schedule(dynamic, 4)
+        for (int g = 0; g < N; ++g) {
+            int lo = 0, hi = B - 1;
+            while (lo < hi) {
+                int mid = (lo + hi + 1) / 2;
+                if (node_offsets[mid] <= g) lo = mid; else hi = mid - 1;
+            }
+            const int b = lo;
+            out_tokens[g] = -1;
+            if (margin) margin[g] = INFINITY;
+            const int32_t pa = parent[g];
+            if (pa < node_offsets[b] || pa >= g) continue;
+            const float Tf = temperature[b];
+            if (!valid_temperature(Tf)) continue;
+            load_row(draft_logits, dtype, pa, V, z);
+            if (Tf == 0.0f) {
+                int am;
+                if (row_argmax(z, V, &am) == 0) out_tokens[g] = am;
+                continue;
+            }
+            const double T = (double)Tf;
+            double L;
+            if (row_lse(z, V, T, &L) != 0) continue;
+            for (int v = 0; v < V; ++v) w[v] = exp(z[v] / T - L);
+            double m;
+            out_tokens[g] = inverse_cdf(w, V, (double)u_draft[g], &m);
+            if (margin) margin[g] = m;
+        }
+        free(z);
+        free(w);
+    }
+    return 0;
+}

@@ -241,3 +241,170 @@ def seq_rows(w: Workload, b: int):
     """(target row range, draft row range) of sequence b."""
     k0, k1 = int(w.k_offsets[b]), int(w.k_offsets[b + 1])
     return range(k0 + b, k1 + b + 1), range(k0, k1)
+
+
+# ------------------------------------------------------------------ trees
+@dataclass
+class TreeWorkload:
+    """One batch of tree-verify inputs (host numpy arrays).  Sequence b owns
+    nodes node_offsets[b] .. node_offsets[b+1]-1, the first being its root;
+    every node has a target row and a draft row (the distributions after the
+    path to it; a leaf's draft row is part of the layout but not needed)."""
+
+    name: str
+    B: int
+    V: int
+    dtype: str
+    node_offsets: np.ndarray       # int32 [B+1]
+    parent: np.ndarray             # int32 [N], -1 for roots
+    temperature: np.ndarray        # float32 [B]
+    target_logits: np.ndarray      # [N, V]
+    draft_logits: np.ndarray       # [N, V]
+    u_accept: np.ndarray           # float32 [N]
+    u_resample: np.ndarray         # float32 [N]
+    u_draft: np.ndarray            # float32 [N]
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def nodes(self) -> int:
+        return int(self.node_offsets[-1])
+
+    @property
+    def elem_bytes(self) -> int:
+        return 4 if self.dtype == F32 else 2
+
+    def internal(self) -> np.ndarray:
+        """bool [N]: node has at least one child."""
+        out = np.zeros(self.nodes, dtype=bool)
+        out[self.parent[self.parent >= 0]] = True
+        return out
+
+
+def tree_shape(branching) -> np.ndarray:
+    """Parent array (breadth-first order) of a full tree with the given
+    number of children per node at each depth, e.g. [3, 2, 1]."""
+    parent = [-1]
+    level = [0]
+    for m in branching:
+        nxt = []
+        for u in level:
+            for _ in range(int(m)):
+                parent.append(u)
+                nxt.append(len(parent) - 1)
+        level = nxt
+    return np.asarray(parent, dtype=np.int32)
+
+
+def make_tree_case(B: int, shape, V: int, dtype: str = F32, temperature=1.0, a: float = 1.1,
+                   sigma_t: float = 1.0, sigma_d: float = 0.5, seed: int = 4321,
+                   uniform_seed: int = 0, name: str | None = None) -> TreeWorkload:
+    """Build a tree workload.
+
+    shape: a list of branching factors (one full tree for every sequence),
+      "random_N" (per sequence a random recursive tree of 1..N nodes: node i
+      hangs under a uniformly chosen earlier node), or a list of B parent
+      arrays (local indices, -1 for the root).
+    temperature: float, a sequence, or "odd_greedy".
+    Rows follow the chain recipe: target row = Zipf slope a rotated per row +
+    N(0, sigma_t^2); draft row = that target row + N(0, sigma_d^2).
+    """
+    ss = np.random.SeedSequence(seed)
+    ss_shape, ss_layout, ss_seq = ss.spawn(3)
+    if isinstance(shape, str):
+        assert shape.startswith("random_")
+        nmax = int(shape.split("_")[1])
+        srng = np.random.default_rng(ss_shape)
+        shapes = []
+        for _ in range(B):
+            n = int(srng.integers(1, nmax + 1))
+            par = [-1] + [int(srng.integers(0, i)) for i in range(1, n)]
+            shapes.append(np.asarray(par, dtype=np.int32))
+    elif len(shape) == B and not np.isscalar(shape[0]):
+        shapes = [np.asarray(s, dtype=np.int32) for s in shape]
+    else:
+        one = tree_shape(shape)
+        shapes = [one] * B
+    sizes = np.array([len(s) for s in shapes], dtype=np.int64)
+    node_offsets = np.zeros(B + 1, dtype=np.int32)
+    node_offsets[1:] = np.cumsum(sizes)
+    N = int(node_offsets[-1])
+    parent = np.empty(N, dtype=np.int32)
+    for b, s in enumerate(shapes):
+        g0 = int(node_offsets[b])
+        parent[g0:g0 + len(s)] = np.where(s >= 0, s + g0, -1)
+
+    if isinstance(temperature, str):
+        assert temperature == "odd_greedy"
+        temp = np.where(np.arange(B) % 2 == 1, 0.0, 1.0).astype(np.float32)
+    elif np.isscalar(temperature):
+        temp = np.full(B, float(temperature), dtype=np.float32)
+    else:
+        temp = np.asarray(temperature, dtype=np.float32)
+
+    base = (-a * np.log1p(np.arange(V, dtype=np.float64))).astype(np.float32)
+    arranged = base[np.random.default_rng(ss_layout).permutation(V)]
+    odt = np.uint16 if dtype == BF16 else np.float32
+    assert dtype in (BF16, F32)
+    zt_out = np.empty((N, V), dtype=odt)
+    zd_out = np.empty((N, V), dtype=odt)
+    seq_seeds = ss_seq.spawn(B)
+
+    def store(dst, row):
+        dst[:] = round_to_bf16_bits(row) if dtype == BF16 else row
+
+    def one_sequence(b):
+        rng = np.random.default_rng(seq_seeds[b])
+        g0, n = int(node_offsets[b]), int(sizes[b])
+        shifts = rng.integers(0, V, size=n)
+        row = np.empty(V, dtype=np.float32)
+        for i in range(n):
+            c = int(shifts[i])
+            row[:V - c] = arranged[c:]
+            row[V - c:] = arranged[:c]
+            row += rng.standard_normal(V, dtype=np.float32) * np.float32(sigma_t)
+            store(zt_out[g0 + i], row)
+            d = row + rng.standard_normal(V, dtype=np.float32) * np.float32(sigma_d)
+            store(zd_out[g0 + i], d)
+
+    workers = max(1, min(32, os.cpu_count() or 1))
+    if B > 1 and workers > 1:
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(one_sequence, range(B)))
+    else:
+        for b in range(B):
+            one_sequence(b)
+
+    urng = np.random.Generator(np.random.Philox(uniform_seed))
+    u_accept = uniforms(urng, N)
+    u_resample = uniforms(urng, N)
+    u_draft = uniforms(urng, N)
+    return TreeWorkload(name=name or f"tree_B{B}_N{N}_V{V}_{dtype}", B=B, V=V, dtype=dtype,
+                        node_offsets=node_offsets, parent=parent, temperature=temp,
+                        target_logits=zt_out, draft_logits=zd_out, u_accept=u_accept,
+                        u_resample=u_resample, u_draft=u_draft,
+                        meta=dict(a=a, sigma_t=sigma_t, sigma_d=sigma_d, seed=seed,
+                                  uniform_seed=uniform_seed))
+
+
+# the tree workload measured beside the chain workloads: 64 sequences, each a
+# full tree of 3 / 2 / 1 children per depth (16 nodes), as a static
+# Medusa/EAGLE-style candidate tree
+TREE_CONFIG = dict(name="tree_B64_n16_b321_V128256_bf16", B=64, shape=[3, 2, 1], V=128256,
+                   dtype=BF16, temperature=1.0, a=1.1, sigma_t=1.0, sigma_d=0.5)
+
+
+def make_tree_config() -> TreeWorkload:
+    c = dict(TREE_CONFIG)
+    return make_tree_case(seed=2000, uniform_seed=0, **c)
+
+
+def tree_algorithmic_bytes(w: TreeWorkload) -> int:
+    """Bytes a tree verify must move at minimum: every node's target row and
+    every internal node's draft row once (sampled sequences), plus one
+    row-equivalent per sampled sequence for the residual or bonus draw."""
+    s = w.elem_bytes
+    internal = w.internal()
+    seq_of = np.repeat(np.arange(w.B), np.diff(w.node_offsets))
+    sampled = w.temperature[seq_of] > 0
+    rows = w.nodes + int((internal & sampled).sum())
+    return int(s * w.V * (rows + int((w.temperature > 0).sum())))
