@@ -53,6 +53,7 @@ def parse():
                     help="other workloads measured kernel-only (comma list, '' for none)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--tree", type=int, default=1, help="also time the tree verify workload (0: skip)")
     return ap.parse_args()
 
 
@@ -60,7 +61,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "spec_verify_lse_traffic_B512_ragg
 
 
 # the sources of the kernels a verify call launches
-VERIFY_SOURCES = ("spec_verify.cu", "device_utils.cuh")
+VERIFY_SOURCES = ("spec_verify.cu", "device_utils.cuh", "verify_common.cuh", "host_common.h")
 
 
 def kernel_source_hash() -> str:
@@ -239,6 +240,60 @@ class _Null:
 
     def __exit__(self, *a):
         return False
+
+
+def measure_tree(torch, sv, dev, reps, warmup):
+    """Tree verify on the tree workload (64 sequences, full 3/2/1 trees of 16
+    nodes, V = 128256, bf16): tokens drawn once by spec_tree_draft_sample,
+    then spec_tree_verify timed with CUDA events on the launching stream."""
+    import numpy as np
+    import workloads
+    w = workloads.make_tree_config()
+
+    def t(a):
+        x = torch.from_numpy(np.ascontiguousarray(a))
+        return (x.view(torch.bfloat16) if a.dtype == np.uint16 else x).to(dev)
+    d = {k: t(getattr(w, k)) for k in ("target_logits", "draft_logits", "node_offsets", "parent", "u_accept",
+                                       "u_resample", "u_draft", "temperature")}
+    args_draft = (d["draft_logits"], d["node_offsets"], d["parent"], d["temperature"], d["u_draft"])
+    toks = sv.spec_tree_draft_sample(*args_draft)
+    toks = torch.where(toks < 0, torch.zeros_like(toks), toks)
+    out = (torch.empty(w.nodes, dtype=torch.int32, device=dev), torch.empty(w.B, dtype=torch.int32, device=dev),
+           torch.empty(w.B, dtype=torch.int32, device=dev))
+    draft_out = torch.empty(w.nodes, dtype=torch.int32, device=dev)
+
+    def verify():
+        sv.spec_tree_verify(d["target_logits"], d["draft_logits"], d["node_offsets"], d["parent"], toks,
+                            d["u_accept"], d["u_resample"], d["temperature"], out_tokens=out[0],
+                            out_num_accepted=out[1], out_last_node=out[2])
+
+    def draft():
+        sv.spec_tree_draft_sample(*args_draft, out_tokens=draft_out)
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name, fn in (("verify", verify), ("draft", draft)):
+        for _ in range(max(3, warmup)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = e0.elapsed_time(e1) / reps
+    nbytes = workloads.tree_algorithmic_bytes(w)
+    internal = int(w.internal().sum())
+    draft_bytes = w.elem_bytes * w.V * internal
+    gbs = nbytes / (res["verify"] * 1e-3) / 1e9
+    return {"workload": w.name, "B": w.B, "nodes": w.nodes, "verify_ms": round(res["verify"], 5),
+            "verify_gbs": gbs, "verify_frac_of_8tbs": gbs / 8000.0, "verify_bytes": nbytes,
+            "nodes_per_s": w.nodes / (res["verify"] * 1e-3),
+            "mean_accepted": out[1].float().mean().item(),
+            "draft_sample_ms": round(res["draft"], 5),
+            "draft_sample_gbs": draft_bytes / (res["draft"] * 1e-3) / 1e9,
+            "calls": "spec_tree_verify (setup + stats_kernel tree mode + tree_walk_kernel); "
+                     "spec_tree_draft_sample (setup + stats_kernel tree-draft mode + tree_draft_select_kernel)"}
 
 
 def adaptive_k_timing(torch, sv, dev, B=4096, reps=1000):
@@ -423,6 +478,7 @@ def main():
         del wc
 
     adapt = adaptive_k_timing(torch, sv, dev) if rank == 0 else None
+    tree = measure_tree(torch, sv, dev, max(50, args.steps // 4), args.warmup) if rank == 0 and args.tree else None
 
     e2e_line = None
     if rank == 0 and args.e2e_steps > 0:
@@ -475,6 +531,7 @@ def main():
         "clocks": clocks,
         "other_workloads": extra,
         "adaptive_k": adapt,
+        "tree_verify": tree,
     }
     print(json.dumps(line))
     if world > 1:

@@ -86,6 +86,7 @@ extern "C" {
 #define SPEC_MAX_K 32        /* drafted positions per sequence */
 #define SPEC_MAX_B 4096      /* sequences per call */
 #define SPEC_MAX_V (1 << 24) /* vocabulary size */
+#define SPEC_MAX_TREE_NODES 64 /* nodes per sequence of a tree verify (root included) */
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
 
@@ -253,6 +254,72 @@ int spec_verify_noalloc(const void *target_logits, const void *draft_logits,
                         const float *u_resample, const float *temperature, int B,
                         const int32_t *k_offsets, int V, int dtype, int32_t *out_tokens,
                         int32_t *out_num_accepted, void *stream);
+
+/*
+ * Tree (multi-candidate) verify.  docs.ifdog.com "投机解码", 进阶方案: Medusa
+ * and EAGLE verify a tree of drafted candidates in one target forward; the
+ * pages give no acceptance rule for it.  The rule implemented is the
+ * single-candidate test of 投机解码的三步流程 step 3 (bbs.huaweicloud.com
+ * 二.1-二.2) applied to several candidates in turn: at node u, with
+ * p = softmax(target row u / T_b) and q = softmax(draft row u / T_b), u's
+ * children c_1 < c_2 < ... (ascending node index; their tokens must be
+ * independent draws from q, e.g. from spec_tree_draft_sample) are tested in
+ * order: c_j is accepted iff u_accept[c_j] < min(1, p_j-1(x)/q(x)), with
+ * p_0 = p and p_j = norm(max(0, p_j-1 - q)) after each rejection.  An
+ * accepted child becomes u.  When every child of u is rejected, one token
+ * is drawn from the last residual at u_resample[u] (inverse CDF, ascending
+ * vocabulary); at a leaf the bonus token is drawn from p.  T_b = 0: the
+ * first child whose token is argmax p (lowest index on ties) is accepted,
+ * else argmax p is emitted.  Each emitted token follows the target
+ * distribution of its node.
+ *
+ * Layout (N = node_offsets[B] nodes; every pointer a device pointer):
+ *   node_offsets  int32 [B+1]  node_offsets[0] = 0; sequence b owns nodes
+ *                              node_offsets[b] .. node_offsets[b+1]-1, 1 to
+ *                              SPEC_MAX_TREE_NODES of them, the first is
+ *                              its root
+ *   parent        int32 [N]    -1 for a root; otherwise an earlier node of
+ *                              the same sequence
+ *   tokens        int32 [N]    each non-root node's drafted token (a
+ *                              root's is ignored)
+ *   target_logits [N, V]       row g: the target logits after the path to
+ *                              node g (the distribution of g's children)
+ *   draft_logits  [N, V]       row g: the draft logits after the path to g
+ *                              (rows of leaves are not read)
+ *   u_accept      float [N]    the test of node g; u_resample float [N]: a
+ *                              draw at node g
+ *   out_tokens    int32 [N]    from slot node_offsets[b]: the accepted path's
+ *                              tokens, the drawn token, then -1
+ *   out_num_accepted int32 [B] accepted tokens, -1 for a data error
+ *   out_last_node int32 [B]    the node where the walk ended (NULL: skip)
+ * N is passed by the host as well (it sizes the library workspace) and must
+ * equal node_offsets[B].  A data error (bad temperature, token or parent
+ * array, or a needed row with NaN / +inf / all -inf) marks only its
+ * sequence; an invalid node_offsets array (or node_offsets[B] != N) fails
+ * the whole call on the device (every out_num_accepted = -1, status
+ * SPEC_ERR_INVALID_ARG).  Host errors: SPEC_ERR_INVALID_ARG for null
+ * pointers or N outside [B, B * SPEC_MAX_TREE_NODES], plus the errors of
+ * spec_verify.  Uses the library-owned workspace (calls ordered on one
+ * stream, as for spec_verify).
+ */
+int spec_tree_verify(const void *target_logits, const void *draft_logits,
+                     const int32_t *node_offsets, const int32_t *parent,
+                     const int32_t *tokens, const float *u_accept,
+                     const float *u_resample, const float *temperature, int B, int N,
+                     int V, int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
+                     int32_t *out_last_node, void *stream);
+
+/*
+ * Tree drafting: each non-root node g takes its token from the draft row of
+ * its parent (softmax(z / T_b)): the inverse-CDF draw at u_draft[g], or
+ * argmax z when T_b = 0, so that siblings are independent draws from one
+ * distribution, as spec_tree_verify requires.  Roots and invalid rows give
+ * -1.  Layout and errors as for spec_tree_verify; u_draft float [N].
+ */
+int spec_tree_draft_sample(const void *draft_logits, const int32_t *node_offsets,
+                           const int32_t *parent, const float *temperature,
+                           const float *u_draft, int B, int N, int V, int dtype,
+                           int32_t *out_tokens, void *stream);
 
 /*
  * Adaptive draft length (sxl-space.tk "【大模型】- 推测解码", 自适应推测解码:

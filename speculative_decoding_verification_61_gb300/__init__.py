@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     F32,
     MAX_B,
     MAX_K,
+    MAX_TREE_NODES,
     MAX_V,
     SPEC_ERRORS,
     SpecError,
@@ -28,6 +29,8 @@ from ._binding import (  # noqa: F401
     spec_draft_sample_lse,
     spec_round,
     spec_round_host,
+    spec_tree_draft_sample,
+    spec_tree_verify,
     spec_verify,
     spec_verify_lse,
     spec_verify_noalloc,

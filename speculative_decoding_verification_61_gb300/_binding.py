@@ -9,6 +9,7 @@ _LIB_PATH = os.path.join(PKG, "_build", "libspecverify.so")
 
 F32, BF16 = 0, 1
 MAX_K, MAX_B, MAX_V = 32, 4096, 1 << 24
+MAX_TREE_NODES = 64
 ABI_VERSION = 1
 SPEC_ERRORS = {0: "SPEC_OK", -1: "SPEC_ERR_INVALID_ARG", -2: "SPEC_ERR_ALIGNMENT",
                -3: "SPEC_ERR_CUDA", -4: "SPEC_ERR_TIMEOUT", -5: "SPEC_ERR_WORKSPACE"}
@@ -18,7 +19,8 @@ EXPORTS = ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sam
            "spec_round_host", "spec_workspace_bytes", "spec_workspace_status",
            "spec_status_string", "spec_abi_version", "spec_last_error", "spec_verify_noalloc",
            "spec_noalloc_bytes", "spec_adapt_state_bytes", "spec_adapt_init", "spec_adapt_update",
-           "spec_draft_sample_lse", "spec_verify_lse", "spec_round")
+           "spec_draft_sample_lse", "spec_verify_lse", "spec_round", "spec_tree_verify",
+           "spec_tree_draft_sample")
 
 
 class SpecError(RuntimeError):
@@ -60,6 +62,8 @@ def lib():
     L.spec_verify_lse.argtypes = [vp, vp, vp, vp, vp, vp, vp, ip, vp, ip, ip, vp, vp,
                                   ctypes.POINTER(_Aux), vp, sz, vp]
     L.spec_round.argtypes = [vp, vp, vp, vp, vp, vp, ip, vp, ip, ip, vp, vp, vp, vp]
+    L.spec_tree_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ip, ip, ip, ip, vp, vp, vp, vp]
+    L.spec_tree_draft_sample.argtypes = [vp, vp, vp, vp, vp, ip, ip, ip, ip, vp, vp]
     L.spec_workspace_bytes.argtypes = [ip, ip, ip]
     L.spec_workspace_bytes.restype = sz
     L.spec_noalloc_bytes.argtypes = [ip, ip, ip]
@@ -80,7 +84,8 @@ def lib():
     L.spec_adapt_update.restype = ip
     for name in ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",
                  "spec_round_host", "spec_workspace_status", "spec_abi_version",
-                 "spec_draft_sample_lse", "spec_verify_lse", "spec_round"):
+                 "spec_draft_sample_lse", "spec_verify_lse", "spec_round", "spec_tree_verify",
+                 "spec_tree_draft_sample"):
         getattr(L, name).restype = ip
     _lib = L
     return L
@@ -303,6 +308,61 @@ def spec_round(target_logits, draft_logits, u_draft, u_accept, u_resample, tempe
                           _p(out_num_accepted), _stream(stream))
     _raise(rc, "spec_round")
     return out_draft_tokens, out_tokens, out_num_accepted
+
+
+def spec_tree_verify(target_logits, draft_logits, node_offsets, parent, tokens, u_accept, u_resample,
+                     temperature, out_tokens=None, out_num_accepted=None, out_last_node=None,
+                     stream=None):
+    """Tree (multi-candidate) verify (device tensors, one target and one
+    draft row per node).  Returns (out_tokens [N] int32, out_num_accepted [B]
+    int32, out_last_node [B] int32)."""
+    import torch
+    B = temperature.numel()
+    N = parent.numel()
+    V = target_logits.shape[-1]
+    dt = _dtype_code(target_logits)
+    for name, t in (("target_logits", target_logits), ("draft_logits", draft_logits)):
+        _check_dev(name, t, target_logits.dtype)
+    for name, t in (("node_offsets", node_offsets), ("parent", parent), ("tokens", tokens)):
+        _check_dev(name, t, torch.int32)
+    for name, t in (("u_accept", u_accept), ("u_resample", u_resample), ("temperature", temperature)):
+        _check_dev(name, t, torch.float32)
+    if node_offsets.numel() != B + 1:
+        raise ValueError("node_offsets must have B + 1 entries")
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty(N, dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_last_node is None:
+        out_last_node = torch.empty(B, dtype=torch.int32, device=dev)
+    rc = lib().spec_tree_verify(_p(target_logits), _p(draft_logits), _p(node_offsets), _p(parent), _p(tokens),
+                                _p(u_accept), _p(u_resample), _p(temperature), B, N, V, dt, _p(out_tokens),
+                                _p(out_num_accepted), _p(out_last_node), _stream(stream))
+    _raise(rc, "spec_tree_verify")
+    return out_tokens, out_num_accepted, out_last_node
+
+
+def spec_tree_draft_sample(draft_logits, node_offsets, parent, temperature, u_draft, out_tokens=None,
+                           stream=None):
+    """Tree drafting: each non-root node's token from its parent's draft
+    row.  Returns int32 [N] (-1 for roots)."""
+    import torch
+    B = temperature.numel()
+    N = parent.numel()
+    V = draft_logits.shape[-1]
+    dt = _dtype_code(draft_logits)
+    _check_dev("draft_logits", draft_logits)
+    for name, t in (("node_offsets", node_offsets), ("parent", parent)):
+        _check_dev(name, t, torch.int32)
+    _check_dev("temperature", temperature, torch.float32)
+    _check_dev("u_draft", u_draft, torch.float32)
+    if out_tokens is None:
+        out_tokens = torch.empty(N, dtype=torch.int32, device=draft_logits.device)
+    rc = lib().spec_tree_draft_sample(_p(draft_logits), _p(node_offsets), _p(parent), _p(temperature), _p(u_draft),
+                                      B, N, V, dt, _p(out_tokens), _stream(stream))
+    _raise(rc, "spec_tree_draft_sample")
+    return out_tokens
 
 
 def spec_round_host(target_logits, draft_logits, u_draft, u_accept, u_resample, temperature,

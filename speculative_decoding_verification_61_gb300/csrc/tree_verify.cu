@@ -1,0 +1,671 @@
+// tree_verify.cu -- GB300 (sm_103a) tree (multi-candidate) verify and tree
+// drafting, behind the C ABI of include/spec_verify.h.
+//
+// The pages draw candidate trees (docs.ifdog.com "投机解码", 进阶方案:
+// Medusa and EAGLE verify a tree of drafted candidates in one target
+// forward) but give no acceptance rule for them.  The rule implemented is
+// the plainest lossless extension of the single-candidate test of
+// 投机解码的三步流程 step 3 (bbs.huaweicloud.com 二.1-二.2) to several
+// candidates drawn i.i.d. from one draft distribution: at node u (target
+// distribution p, draft distribution q, from u's rows), u's children are
+// tried in ascending node order; child j is accepted iff
+// u_accept[child] < min(1, p^(j-1)(x)/q(x)), p^(0) = p, and each rejection
+// replaces p by norm(max(0, p - q)).  An accepted child becomes u.  When
+// every child is rejected, one token is drawn from the last residual at
+// u_resample[u] by inverse CDF; a leaf draws the bonus token from its p.
+// Greedy (T = 0): the first child whose token is argmax p is accepted, else
+// argmax p is emitted.
+//
+// Pipeline of one spec_tree_verify call (all on the caller's stream):
+//   1. tree_setup_kernel  warp per sequence: checks the parent array and
+//                         lists the internal nodes (the draft rows needed);
+//   2. stats_kernel       (tree mode) streams every node's target row and
+//                         the internal nodes' draft rows once, to sub-chunk
+//                         partials, as in the chain verify;
+//   3. tree_walk_kernel   block per sequence: walks the tree from the root.
+//                         At a node it combines the node's partials, tests
+//                         the children in order and, after each rejection,
+//                         makes one pass over the node's two rows for the
+//                         residual mass (the rows are prefetched into L2 at
+//                         the first rejection, so later passes hit L2); the
+//                         last draw locates the sub-chunk from the pass's
+//                         per-sub-chunk masses and scans it.
+// spec_tree_draft_sample runs the setup, stats_kernel over the internal
+// nodes' draft rows, and tree_draft_select_kernel (warp per node: its token
+// from its parent's draft row).
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "host_common.h"
+#include "verify_common.cuh"
+
+namespace specv {
+
+// ================================================================== setup
+// Warp per sequence (<= kMaxTreeNodes nodes, two per lane): a sequence
+// whose parent array is not a tree in topological order (root first with
+// parent -1, every other node's parent an earlier node of the sequence)
+// gets nint = -1; otherwise nint = its internal nodes (nodes with a child)
+// and tint[b * kMaxTreeNodes + j] = the j-th of them (global index,
+// ascending).  Sequences whose node count is out of range are left to the
+// whole-call check of the other kernels.
+__global__ void __launch_bounds__(256) tree_setup_kernel(const int *__restrict__ node_offsets,
+                                                         const int *__restrict__ parent, int B, int N,
+                                                         int *__restrict__ nint, int *__restrict__ tint) {
+    const int b = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int lane = lane_id();
+    if (b >= B) return;
+    const int g0 = node_offsets[b];
+    const int n = node_offsets[b + 1] - g0;
+    if (n < 1 || n > kMaxTreeNodes || g0 < 0 || g0 + n > N) {
+        if (lane == 0) nint[b] = -1;
+        return;
+    }
+    const int i0 = lane, i1 = lane + 32;
+    auto local_parent = [&](int i) -> int {
+        if (i >= n) return -2;
+        const int pa = parent[g0 + i];
+        return pa < 0 ? -1 : pa - g0;
+    };
+    const int p0 = local_parent(i0), p1 = local_parent(i1);
+    auto valid = [&](int i, int p) { return i >= n || (i == 0 ? p == -1 : (p >= 0 && p < i)); };
+    if (!__all_sync(0xffffffffu, valid(i0, p0) && valid(i1, p1))) {
+        if (lane == 0) nint[b] = -1;
+        return;
+    }
+    // internal nodes: those that are some node's parent
+    bool int0 = false, int1 = false;
+    for (int t = 0; t < n; ++t) {
+        const unsigned m0 = __ballot_sync(0xffffffffu, p0 == t);
+        const unsigned m1 = __ballot_sync(0xffffffffu, p1 == t);
+        if (m0 | m1) {
+            int0 |= (t == i0);
+            int1 |= (t == i1);
+        }
+    }
+    const unsigned long long m = (static_cast<unsigned long long>(__ballot_sync(0xffffffffu, int1)) << 32) |
+                                 __ballot_sync(0xffffffffu, int0);
+    if (int0) tint[b * kMaxTreeNodes + __popcll(m & ((1ull << i0) - 1ull))] = g0 + i0;
+    if (int1) tint[b * kMaxTreeNodes + __popcll(m & ((1ull << i1) - 1ull))] = g0 + i1;
+    if (lane == 0) nint[b] = __popcll(m);
+}
+
+// ================================================================== walk
+constexpr int kWalkThreads = 512;
+constexpr int kWalkWarps = kWalkThreads / 32;
+
+struct TreeWalkSmem {
+    int par[kMaxTreeNodes];     // local parent of each node (-1: root)
+    int tok[kMaxTreeNodes];     // drafted token of each node
+    float zt[kMaxTreeNodes];    // the current node's target logit at each child's token
+    float zd[kMaxTreeNodes];    // and its draft logit
+    int path[kMaxTreeNodes];    // accepted tokens
+    float invZ[kMaxTreeNodes];  // 1 / Z of each residual level at the current node
+    double Lt, Ld;              // log2-domain log-sum-exp of the current node's rows
+    float M;                    // max of the current target row (z * c)
+    float lth, ltl, ldh, ldl;   // Lt and Ld as fp32 hi/lo pairs
+    int am;                     // greedy: arg-max of the current target row
+    int ok, okd;                // the current node's rows are valid
+    int next;                   // accepted child (local index) or -1
+    int zpos;                   // the last residual mass was > 0
+    int token;                  // the drawn token
+};
+
+// Probability of one element at residual level L of the current node:
+// p_0 = 2^(zt c - Lt), q = 2^(zd c - Ld), p_(i+1) = max(0, p_i - q) / Z_(i+1)
+// (1 / Z from invZ).  Operations are pinned, so that a candidate's test,
+// the passes and the final scan compute identical bits.
+__device__ __forceinline__ float tree_level_p(float zt, float zd, float c, float lth, float ltl, float ldh,
+                                              float ldl, const float *invZ, int L, float *q_out) {
+    const float at = __fsub_rn(__fmaf_rn(zt, c, -lth), ltl);
+    const float ad = __fsub_rn(__fmaf_rn(zd, c, -ldh), ldl);
+    float p = ex2(at);
+    const float q = ex2(ad);
+    for (int i = 0; i < L; ++i) p = __fmul_rn(fmaxf(__fsub_rn(p, q), 0.0f), invZ[i]);
+    *q_out = q;
+    return p;
+}
+
+// Weight of one element: the residual max(0, p_L - q) (p_only: p_L itself).
+struct TreeWeight {
+    float c, lth, ltl, ldh, ldl;
+    const float *invZ;
+    int L;
+    bool p_only;
+    __device__ __forceinline__ float operator()(float zt, float zd) const {
+        float q;
+        const float p = tree_level_p(zt, zd, c, lth, ltl, ldh, ldl, invZ, L, &q);
+        return p_only ? p : fmaxf(__fsub_rn(p, q), 0.0f);
+    }
+};
+
+// One pass of the whole block over the current node's two rows: the mass of
+// W over every sub-chunk, to rm[sc] (warp w takes sub-chunks w, w + 16, ...).
+template <int DT>
+__device__ void tree_pass(const unsigned char *rt, const unsigned char *rd, const Geometry &g, const TreeWeight &W,
+                          float *rm) {
+    using E = Elem<DT>;
+    const int lane = lane_id();
+    for (int sc = warp_id(); sc < g.n_sub; sc += kWalkWarps) {
+        int a, e1;
+        sub_range(g, sc, &a, &e1);
+        const int nvec = (e1 - a) / E::kPerVec;  // <= 128
+        const uint4 *pt = reinterpret_cast<const uint4 *>(rt + static_cast<int64_t>(a) * E::kBytes);
+        const uint4 *pd = reinterpret_cast<const uint4 *>(rd + static_cast<int64_t>(a) * E::kBytes);
+        uint4 xt4[4], xd4[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = lane + 32 * j;
+            if (i < nvec) {
+                xt4[j] = ld_stream(pt + i);
+                xd4[j] = ld_stream(pd + i);
+            }
+        }
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (lane + 32 * j >= nvec) continue;
+            float x1[E::kPerVec], x2[E::kPerVec];
+            E::unpack(xt4[j], x1);
+            E::unpack(xd4[j], x2);
+#pragma unroll
+            for (int q = 0; q < E::kPerVec; ++q) acc += W(x1[q], x2[q]);
+        }
+        const float sum = warp_sum_f(acc);
+        if (lane == 0) rm[sc] = sum;
+    }
+}
+
+// The total of the n masses rm[0 .. n) by one warp (fixed order: lane l
+// adds its masses l, l + 32, ... with compensation, then the two warp sums).
+__device__ __forceinline__ float warp_total(const float *rm, int n) {
+    Acc2 acc;
+    for (int i = lane_id(); i < n; i += 32) acc.add(__ldcg(rm + i));
+    return __fadd_rn(warp_sum_f(acc.hi), warp_sum_f(acc.lo));
+}
+
+// Block per sequence.  Partials: target row g at slot g, draft row g at
+// slot N + g (stats_kernel tree mode); rm: this sequence's n_sub residual
+// masses (scratch).  Data errors (a bad temperature, token or parent array,
+// or an invalid needed row) make the whole sequence -1, as in the chain
+// verify; an invalid node_offsets array fails the whole call.
+template <int DT>
+__global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
+    const void *__restrict__ target, const void *__restrict__ draft, const int *__restrict__ node_offsets,
+    const int *__restrict__ parent, const int32_t *__restrict__ tokens, const float *__restrict__ u_accept,
+    const float *__restrict__ u_resample, const float *__restrict__ temperature, int B, int N, Geometry g,
+    const float2 *__restrict__ part, const int *__restrict__ nint, float *__restrict__ resid,
+    int *__restrict__ counters, int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_num,
+    int32_t *__restrict__ out_last) {
+    using E = Elem<DT>;
+    __shared__ TreeWalkSmem sm;
+    const int b = blockIdx.x;
+    const int lane = lane_id(), warp = warp_id(), tid = threadIdx.x;
+
+    // --- inputs only (written before this call) --------------------------
+    // the same node_offsets check as stats_kernel: only with it do the row
+    // indices below stay inside the caller's buffers
+    int bad = 0;
+    for (int i = tid; i <= B; i += blockDim.x) {
+        const int v = node_offsets[i];
+        if (i == 0) {
+            bad |= v != 0;
+        } else {
+            const int nn = v - node_offsets[i - 1];
+            bad |= (nn < 1 || nn > kMaxTreeNodes);
+        }
+        if (i == B) bad |= v != N;
+    }
+    bad = __syncthreads_or(bad);
+    if (bad) {
+        grid_dependency_wait();
+        if (tid == 0) {
+            out_num[b] = -1;
+            if (out_last) out_last[b] = -1;
+            if (b == 0) set_status(counters + kStatus, SPEC_ERR_INVALID_ARG);
+        }
+        return;
+    }
+    const int g0 = node_offsets[b], n = node_offsets[b + 1] - g0;
+    const float c = temp_scale(temperature[b]);
+    const bool greedy = c == 0.0f;
+    const int V = g.V;
+    bool tokbad = false;
+    if (tid < n) {
+        const int pa = parent[g0 + tid];
+        sm.par[tid] = pa < 0 ? -1 : pa - g0;
+        const int x = tokens[g0 + tid];
+        sm.tok[tid] = x;
+        tokbad = tid > 0 && (x < 0 || x >= V);
+    }
+    tokbad = __syncthreads_or(tokbad);
+    grid_dependency_wait();
+
+    bool err = (c != c) || tokbad || nint[b] < 0;
+    int u = 0, nacc = 0, final_token = -1;
+    float *rm = resid + static_cast<int64_t>(b) * g.n_sub;
+    const int64_t rb = static_cast<int64_t>(V) * E::kBytes;
+    for (int step = 0; !err && step < n; ++step) {
+        const int64_t urow = g0 + u;
+        // children of u, in ascending node order (the same mask in every warp)
+        const int pa0 = lane < n ? sm.par[lane] : -2, pa1 = lane + 32 < n ? sm.par[lane + 32] : -2;
+        const unsigned long long kids = (static_cast<unsigned long long>(__ballot_sync(0xffffffffu, pa1 == u)) << 32) |
+                                        __ballot_sync(0xffffffffu, pa0 == u);
+        const bool leaf = kids == 0ull;
+        // statistics of u's rows; its children's logits at their tokens
+        if (warp == 0) {
+            const float2 *pr = part + urow * g.n_sub;
+            if (greedy) {
+                const int am = warp_combine_arg(pr, g.n_sub);
+                if (lane == 0) {
+                    sm.am = am;
+                    sm.ok = am >= 0;
+                }
+            } else {
+                float M, S;
+                const bool ok = warp_combine_soft(pr, g.n_sub, &M, &S);
+                if (lane == 0) {
+                    sm.ok = ok;
+                    if (ok) {
+                        const double Lt = lse2(M, S);
+                        sm.M = M;
+                        sm.Lt = Lt;
+                        sm.lth = static_cast<float>(Lt);
+                        sm.ltl = static_cast<float>(Lt - static_cast<double>(sm.lth));
+                    }
+                }
+            }
+        } else if (warp == 1) {
+            bool ok = true;
+            if (!greedy && !leaf) {
+                float M, S;
+                ok = warp_combine_soft(part + (static_cast<int64_t>(N) + urow) * g.n_sub, g.n_sub, &M, &S);
+                if (lane == 0 && ok) {
+                    const double Ld = lse2(M, S);
+                    sm.Ld = Ld;
+                    sm.ldh = static_cast<float>(Ld);
+                    sm.ldl = static_cast<float>(Ld - static_cast<double>(sm.ldh));
+                }
+            }
+            if (lane == 0) sm.okd = ok;
+        } else if (warp == 2 && !greedy) {
+            for (int i = lane; i < n; i += 32)
+                if ((kids >> i) & 1ull) {
+                    sm.zt[i] = E::load1(target, urow * V + sm.tok[i]);
+                    sm.zd[i] = E::load1(draft, urow * V + sm.tok[i]);
+                }
+        }
+        __syncthreads();
+        if (!sm.ok || !sm.okd) {
+            err = true;
+            break;
+        }
+        if (greedy) {
+            // the first child whose token is argmax p
+            const int am = sm.am;
+            const int t0 = lane < n ? sm.tok[lane] : -1, t1 = lane + 32 < n ? sm.tok[lane + 32] : -1;
+            const unsigned long long match =
+                kids & ((static_cast<unsigned long long>(__ballot_sync(0xffffffffu, t1 == am)) << 32) |
+                        __ballot_sync(0xffffffffu, t0 == am));
+            if (!match) {
+                final_token = am;
+                break;
+            }
+            const int ch = __ffsll(static_cast<long long>(match)) - 1;
+            if (tid == 0) sm.path[nacc] = sm.tok[ch];
+            ++nacc;
+            u = ch;
+            __syncthreads();  // sm is rewritten for the next node
+            continue;
+        }
+        if (leaf) {
+            // bonus token from p_u, as the chain's bonus draw
+            if (warp == 0) {
+                const float2 *pr = part + urow * g.n_sub;
+                float2 pc[kPartCache];
+                load_parts(pr, g.n_sub, pc);
+                const int tk = warp_draw_row<DT>(target, urow, pr, pc, g, c, sm.M, u_resample[urow]);
+                if (lane == 0) sm.token = tk;
+            }
+            __syncthreads();
+            final_token = sm.token;
+            break;
+        }
+        // the children in order
+        const unsigned char *rt = static_cast<const unsigned char *>(target) + urow * rb;
+        const unsigned char *rd = static_cast<const unsigned char *>(draft) + urow * rb;
+        const TreeWeight base{c, sm.lth, sm.ltl, sm.ldh, sm.ldl, sm.invZ, 0, false};
+        int L = 0, j = 0, next = -1;
+        bool zero_last = false;
+        for (unsigned long long rest = kids; rest; rest &= rest - 1ull, ++j) {
+            const int ch = __ffsll(static_cast<long long>(rest)) - 1;
+            if (tid == 0) {
+                const float zt = sm.zt[ch], zd = sm.zd[ch];
+                float alpha;
+                if (j == 0) {
+                    // the first candidate: the log-domain ratio of the chain verify
+                    if (zt == -INFINITY) {
+                        alpha = 0.0f;
+                    } else if (zd == -INFINITY) {
+                        alpha = 1.0f;
+                    } else {
+                        const double cd = static_cast<double>(c);
+                        const double lr =
+                            (static_cast<double>(zt) * cd - sm.Lt) - (static_cast<double>(zd) * cd - sm.Ld);
+                        alpha = lr >= 0.0 ? 1.0f : exp2f(static_cast<float>(lr));
+                    }
+                } else {
+                    float q;
+                    const float px = tree_level_p(zt, zd, c, sm.lth, sm.ltl, sm.ldh, sm.ldl, sm.invZ, L, &q);
+                    alpha = (zd == -INFINITY || q == 0.0f) ? (px > 0.0f ? 1.0f : 0.0f) : fminf(1.0f, px / q);
+                }
+                sm.next = u_accept[g0 + ch] < alpha ? ch : -1;
+            }
+            __syncthreads();
+            if (sm.next >= 0) {
+                next = sm.next;
+                break;
+            }
+            // rejected: one pass over u's rows for the residual at level L
+            if (j == 0 && warp == 0 && SPEC_RESID_PREFETCH) {
+                // both rows to L2 in 32 KB bulk prefetches: the later passes hit L2
+                constexpr int64_t kPiece = 32768;
+                const unsigned char *r0 = (lane & 1) ? rd : rt;
+                for (int64_t off = static_cast<int64_t>(lane >> 1) * kPiece; off < rb; off += 16 * kPiece)
+                    bulk_prefetch_l2(r0 + off, static_cast<uint32_t>(min(kPiece, rb - off)));
+            }
+            TreeWeight W = base;
+            W.L = L;
+            tree_pass<DT>(rt, rd, g, W, rm);
+            __syncthreads();
+            if (warp == 0) {
+                const float Z = warp_total(rm, g.n_sub);
+                if (lane == 0) {
+                    sm.zpos = Z > 0.0f;
+                    if (Z > 0.0f) sm.invZ[L] = __frcp_rn(Z);
+                }
+            }
+            __syncthreads();
+            if (sm.zpos) {
+                ++L;
+                zero_last = false;
+            } else {
+                zero_last = true;  // p stays as it was (the residual mass rounded to 0)
+            }
+        }
+        if (next >= 0) {
+            if (tid == 0) sm.path[nacc] = sm.tok[next];
+            ++nacc;
+            u = next;
+            __syncthreads();
+            continue;
+        }
+        // every child rejected: draw from the last residual (after a mass
+        // that rounded to 0, from p at the current level)
+        TreeWeight W = base;
+        if (zero_last) {
+            W.L = L;
+            W.p_only = true;
+            tree_pass<DT>(rt, rd, g, W, rm);
+            __syncthreads();
+        } else {
+            W.L = L - 1;
+        }
+        if (warp == 0) {
+            float w[kPartCache];
+#pragma unroll
+            for (int q = 0; q < kPartCache; ++q) w[q] = (lane + 32 * q < g.n_sub) ? __ldcg(rm + lane + 32 * q) : 0.0f;
+            auto wfar = [&](int i) -> float { return __ldcg(rm + i); };
+            F2 before, Z, tgt;
+            const int sc = warp_locate(g.n_sub, w, wfar, u_resample[urow], &before, &Z, &tgt);
+            int tk = -1;
+            if (sc >= 0) {
+                int a, e1;
+                sub_range(g, sc, &a, &e1);
+                tk = warp_scan_elems<DT>(rt, rd, a, e1, W, before, tgt);
+            }
+            if (lane == 0) sm.token = tk;
+        }
+        __syncthreads();
+        final_token = sm.token;
+        break;
+    }
+    // outputs: the accepted path, the drawn token, then -1
+    for (int i = tid; i < n; i += blockDim.x) {
+        int32_t o = -1;
+        if (!err) o = i < nacc ? sm.path[i] : (i == nacc ? final_token : -1);
+        out_tokens[g0 + i] = o;
+    }
+    if (tid == 0) {
+        out_num[b] = err ? -1 : nacc;
+        if (out_last) out_last[b] = err ? -1 : g0 + u;
+    }
+}
+
+// ================================================================== drafting
+// Warp per node (grid-stride): a non-root node's token from its parent's
+// draft row (partials at slot parent, stats_kernel tree-draft mode):
+// arg-max at T = 0, else the inverse-CDF draw at u_draft[node].  Roots,
+// invalid sequences and invalid rows give -1.
+template <int DT>
+__global__ void __launch_bounds__(256) tree_draft_select_kernel(
+    const void *__restrict__ draft, const int *__restrict__ node_offsets, const int *__restrict__ parent,
+    const float *__restrict__ temperature, const float *__restrict__ u_draft, int B, int N, Geometry g,
+    const float2 *__restrict__ part, const int *__restrict__ nint, int32_t *__restrict__ out,
+    int *__restrict__ counters) {
+    extern __shared__ int s_no[];  // [B + 1]
+    __shared__ int s_bad;
+    if (threadIdx.x == 0) s_bad = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i <= B; i += blockDim.x) {
+        const int v = node_offsets[i];
+        s_no[i] = v;
+        if (i == 0 && v != 0) s_bad = 1;
+        if (i > 0) {
+            const int nn = v - node_offsets[i - 1];
+            if (nn < 1 || nn > kMaxTreeNodes) s_bad = 1;
+        }
+        if (i == B && v != N) s_bad = 1;
+    }
+    __syncthreads();
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (s_bad) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) set_status(counters + kStatus, SPEC_ERR_INVALID_ARG);
+        return;
+    }
+    const int lane = lane_id();
+    const int nw = (gridDim.x * blockDim.x) >> 5;
+    for (int node = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; node < N; node += nw) {
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_no[mid] <= node) lo = mid; else hi = mid - 1;
+        }
+        const int pa = parent[node];
+        const float c = temp_scale(temperature[lo]);
+        int token = -1;
+        if (pa >= s_no[lo] && pa < node && nint[lo] >= 0 && c == c) {
+            const float2 *pr = part + static_cast<int64_t>(pa) * g.n_sub;
+            if (c == 0.0f) {
+                token = warp_combine_arg(pr, g.n_sub);
+            } else {
+                float M, S;
+                float2 pc[kPartCache];
+                load_parts(pr, g.n_sub, pc);
+                if (combine_soft(pc, pr, g.n_sub, &M, &S)) token = warp_draw_row<DT>(draft, pa, pr, pc, g, c, M, u_draft[node]);
+            }
+        }
+        if (lane == 0) out[node] = token;
+    }
+}
+
+// ================================================================== host side
+struct TreeWsLayout {
+    size_t part, nint, tint, resid, total;
+};
+
+// Counters (the common 256-byte block) | partials of N target and N draft
+// rows | nint [B] | tint [B * kMaxTreeNodes] | residual masses [B * n_sub].
+TreeWsLayout tree_ws_layout(int B, int N, const Geometry &g) {
+    TreeWsLayout l;
+    size_t off = kCountersBytes;
+    l.part = off;
+    off = align_up(off + static_cast<size_t>(2) * N * g.n_sub * sizeof(float2), 256);
+    l.nint = off;
+    off = align_up(off + static_cast<size_t>(B) * sizeof(int), 256);
+    l.tint = off;
+    off = align_up(off + static_cast<size_t>(B) * kMaxTreeNodes * sizeof(int), 256);
+    l.resid = off;
+    off = align_up(off + static_cast<size_t>(B) * g.n_sub * sizeof(float), 256);
+    l.total = off;
+    return l;
+}
+
+bool g_tree_init[kMaxDevices] = {};
+std::mutex g_tree_mu;
+
+// stats_kernel's tree modes in this translation unit: the opt-in dynamic
+// shared memory, once per device.
+template <int DT, int MODE>
+bool tree_stats_attr(int smem_optin_raw) {
+    cudaFuncAttributes fa{};
+    if (!cuda_ok(cudaFuncGetAttributes(&fa, stats_kernel<DT, MODE>), "cudaFuncGetAttributes")) return false;
+    return cuda_ok(cudaFuncSetAttribute(stats_kernel<DT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        smem_optin_raw - static_cast<int>(fa.sharedSizeBytes)),
+                   "cudaFuncSetAttribute(stats_kernel tree)");
+}
+
+DeviceState *tree_device_state(int *dev_out) {
+    DeviceState *st = device_state(dev_out);
+    if (!st) return nullptr;
+    std::lock_guard<std::mutex> lock(g_tree_mu);
+    if (!g_tree_init[*dev_out]) {
+        int optin = 0;
+        if (!cuda_ok(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, *dev_out),
+                     "cudaDeviceGetAttribute"))
+            return nullptr;
+        if (!tree_stats_attr<SPEC_F32, kModeTree>(optin) || !tree_stats_attr<SPEC_F32, kModeTreeDraft>(optin) ||
+            !tree_stats_attr<SPEC_BF16, kModeTree>(optin) || !tree_stats_attr<SPEC_BF16, kModeTreeDraft>(optin))
+            return nullptr;
+        g_tree_init[*dev_out] = true;
+    }
+    return st;
+}
+
+int check_tree_args(int B, int N, int V, int dtype) {
+    const int rc = check_common(B, V, dtype);
+    if (rc != SPEC_OK) return rc;
+    if (N < B || static_cast<int64_t>(N) > static_cast<int64_t>(B) * kMaxTreeNodes) return SPEC_ERR_INVALID_ARG;
+    return SPEC_OK;
+}
+
+template <int DT, bool VERIFY>
+int launch_tree(const void *target, const void *draft, const int32_t *node_offsets, const int32_t *parent,
+                const int32_t *tokens, const float *u_accept, const float *u_resample, const float *u_draft,
+                const float *temperature, int B, int N, const Geometry &g, int32_t *out_tokens, int32_t *out_num,
+                int32_t *out_last, DeviceState &st, cudaStream_t stream) {
+    const TreeWsLayout l = tree_ws_layout(B, N, g);
+    void *ws = get_internal_ws(st, l.total);
+    if (!ws) return SPEC_ERR_CUDA;
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    int *counters = reinterpret_cast<int *>(w);
+    float2 *part = reinterpret_cast<float2 *>(w + l.part);
+    int *nint = reinterpret_cast<int *>(w + l.nint);
+    int *tint = reinterpret_cast<int *>(w + l.tint);
+    float *resid = reinterpret_cast<float *>(w + l.resid);
+    int ns, per_sm;
+    size_t smem;
+    pick_ring(st, B, &ns, &smem, &per_sm);
+    if (ns == 0) return SPEC_ERR_INVALID_ARG;
+    // setup, then stats_kernel launched plainly: its prologue reads the
+    // setup's tables before waiting on anything
+    if (!cuda_ok(launch_k(false, tree_setup_kernel, dim3((B * 32 + 255) / 256), dim3(256), 0, stream, node_offsets,
+                          parent, B, N, nint, tint),
+                 "launch tree_setup_kernel"))
+        return SPEC_ERR_CUDA;
+    const cudaError_t e =
+        VERIFY ? launch_k(false, stats_kernel<DT, kModeTree>, dim3(st.sms * per_sm), dim3(kThreads), smem, stream,
+                          target, draft, temperature, node_offsets, B, g, ns, part, counters,
+                          static_cast<int *>(nullptr), static_cast<const int *>(nint), static_cast<const int *>(tint), N)
+               : launch_k(false, stats_kernel<DT, kModeTreeDraft>, dim3(st.sms * per_sm), dim3(kThreads), smem,
+                          stream, draft, draft, temperature, node_offsets, B, g, ns, part, counters,
+                          static_cast<int *>(nullptr), static_cast<const int *>(nint), static_cast<const int *>(tint), N);
+    if (!cuda_ok(e, "launch stats_kernel (tree)")) return SPEC_ERR_CUDA;
+    if (VERIFY) {
+        if (!cuda_ok(launch_k(true, tree_walk_kernel<DT>, dim3(B), dim3(kWalkThreads), 0, stream, target, draft,
+                              node_offsets, parent, tokens, u_accept, u_resample, temperature, B, N, g,
+                              static_cast<const float2 *>(part), static_cast<const int *>(nint), resid, counters,
+                              out_tokens, out_num, out_last),
+                     "launch tree_walk_kernel"))
+            return SPEC_ERR_CUDA;
+    } else {
+        const int grid = std::max(1, std::min(st.sms * 8, (N + 7) / 8));
+        if (!cuda_ok(launch_k(true, tree_draft_select_kernel<DT>, dim3(grid), dim3(256), (B + 1) * sizeof(int),
+                              stream, draft, node_offsets, parent, temperature, u_draft, B, N, g,
+                              static_cast<const float2 *>(part), static_cast<const int *>(nint), out_tokens,
+                              counters),
+                     "launch tree_draft_select_kernel"))
+            return SPEC_ERR_CUDA;
+    }
+    return SPEC_OK;
+}
+
+}  // namespace specv
+
+using namespace specv;
+
+extern "C" {
+
+int spec_tree_verify(const void *target_logits, const void *draft_logits, const int32_t *node_offsets,
+                     const int32_t *parent, const int32_t *tokens, const float *u_accept, const float *u_resample,
+                     const float *temperature, int B, int N, int V, int dtype, int32_t *out_tokens,
+                     int32_t *out_num_accepted, int32_t *out_last_node, void *stream) {
+    int rc = check_tree_args(B, N, V, dtype);
+    if (rc != SPEC_OK) return rc;
+    if (B == 0) return SPEC_OK;
+    if (!target_logits || !draft_logits || !node_offsets || !parent || !tokens || !u_accept || !u_resample ||
+        !temperature || !out_tokens || !out_num_accepted)
+        return SPEC_ERR_INVALID_ARG;
+    if (!aligned16(target_logits) || !aligned16(draft_logits)) return SPEC_ERR_ALIGNMENT;
+    Geometry g;
+    make_geometry(V, dtype, &g);
+    int dev;
+    DeviceState *st = tree_device_state(&dev);
+    if (!st) return SPEC_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == SPEC_F32)
+        return launch_tree<SPEC_F32, true>(target_logits, draft_logits, node_offsets, parent, tokens, u_accept,
+                                           u_resample, nullptr, temperature, B, N, g, out_tokens, out_num_accepted,
+                                           out_last_node, *st, s);
+    return launch_tree<SPEC_BF16, true>(target_logits, draft_logits, node_offsets, parent, tokens, u_accept,
+                                        u_resample, nullptr, temperature, B, N, g, out_tokens, out_num_accepted,
+                                        out_last_node, *st, s);
+}
+
+int spec_tree_draft_sample(const void *draft_logits, const int32_t *node_offsets, const int32_t *parent,
+                           const float *temperature, const float *u_draft, int B, int N, int V, int dtype,
+                           int32_t *out_tokens, void *stream) {
+    int rc = check_tree_args(B, N, V, dtype);
+    if (rc != SPEC_OK) return rc;
+    if (B == 0) return SPEC_OK;
+    if (!draft_logits || !node_offsets || !parent || !temperature || !u_draft || !out_tokens)
+        return SPEC_ERR_INVALID_ARG;
+    if (!aligned16(draft_logits)) return SPEC_ERR_ALIGNMENT;
+    Geometry g;
+    make_geometry(V, dtype, &g);
+    int dev;
+    DeviceState *st = tree_device_state(&dev);
+    if (!st) return SPEC_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == SPEC_F32)
+        return launch_tree<SPEC_F32, false>(nullptr, draft_logits, node_offsets, parent, nullptr, nullptr, nullptr,
+                                            u_draft, temperature, B, N, g, out_tokens, nullptr, nullptr, *st, s);
+    return launch_tree<SPEC_BF16, false>(nullptr, draft_logits, node_offsets, parent, nullptr, nullptr, nullptr,
+                                         u_draft, temperature, B, N, g, out_tokens, nullptr, nullptr, *st, s);
+}
+
+}  // extern "C"

@@ -32,7 +32,7 @@ def test_header_declares_expected_entry_points():
     for n in ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",
               "spec_round_host", "spec_workspace_bytes", "spec_workspace_status",
               "spec_status_string", "spec_abi_version", "spec_draft_sample_lse", "spec_verify_lse",
-              "spec_round"):
+              "spec_round", "spec_tree_verify", "spec_tree_draft_sample"):
         assert n in names
 
 
@@ -100,3 +100,21 @@ def test_fused_round_host_argument_errors(lib):
     assert lib.spec_round(fake, fake, fake, fake, fake, fake, 4, fake, 1000, 5, fake, fake, fake, None) == -1
     assert lib.spec_round(fake, fake, fake, fake, fake, fake, 4, fake, 1001, 1, fake, fake, fake, None) == -2
     assert lib.spec_round(None, None, None, None, None, None, 0, None, 1000, 0, None, None, None, None) == 0
+
+
+def test_tree_host_argument_errors(lib):
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)  # never dereferenced: validation fails first
+    # N outside [B, 64 B], null pointer, bad dtype; B == 0 is a no-op
+    assert lib.spec_tree_verify(fake, fake, fake, fake, fake, fake, fake, fake, 4, 3, 1000, 0, fake, fake,
+                                None, None) == -1
+    assert lib.spec_tree_verify(fake, fake, fake, fake, fake, fake, fake, fake, 4, 257, 1000, 0, fake, fake,
+                                None, None) == -1
+    assert lib.spec_tree_verify(fake, fake, None, fake, fake, fake, fake, fake, 4, 8, 1000, 0, fake, fake,
+                                None, None) == -1
+    assert lib.spec_tree_verify(fake, fake, fake, fake, fake, fake, fake, fake, 4, 8, 1000, 7, fake, fake,
+                                None, None) == -1
+    assert lib.spec_tree_verify(None, None, None, None, None, None, None, None, 0, 0, 1000, 0, None, None,
+                                None, None) == 0
+    assert lib.spec_tree_draft_sample(fake, fake, fake, fake, fake, 4, 3, 1000, 0, fake, None) == -1
+    assert lib.spec_tree_draft_sample(fake, fake, fake, fake, fake, 4, 8, 1001, 1, fake, None) == -2
