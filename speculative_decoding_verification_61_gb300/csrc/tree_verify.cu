@@ -103,7 +103,8 @@ struct TreeWalkSmem {
     float zt[kMaxTreeNodes];    // the current node's target logit at each child's token
     float zd[kMaxTreeNodes];    // and its draft logit
     int path[kMaxTreeNodes];    // accepted tokens
-    float invZ[kMaxTreeNodes];  // 1 / Z of each residual level at the current node
+    double t;                   // residual level of the current p at the node (0: p itself)
+    float S;                    // its mass S(t)
     double Lt, Ld;              // log2-domain log-sum-exp of the current node's rows
     float M;                    // max of the current target row (z * c)
     float lth, ltl, ldh, ldl;   // Lt and Ld as fp32 hi/lo pairs
@@ -114,68 +115,86 @@ struct TreeWalkSmem {
     int token;                  // the drawn token
 };
 
-// Probability of one element at residual level L of the current node:
-// p_0 = 2^(zt c - Lt), q = 2^(zd c - Ld), p_(i+1) = max(0, p_i - q) / Z_(i+1)
-// (1 / Z from invZ).  Operations are pinned, so that a candidate's test,
-// the passes and the final scan compute identical bits.
-__device__ __forceinline__ float tree_level_p(float zt, float zd, float c, float lth, float ltl, float ldh,
-                                              float ldl, const float *invZ, int L, float *q_out) {
-    const float at = __fsub_rn(__fmaf_rn(zt, c, -lth), ltl);
-    const float ad = __fsub_rn(__fmaf_rn(zd, c, -ldh), ldl);
-    float p = ex2(at);
-    const float q = ex2(ad);
-    for (int i = 0; i < L; ++i) p = __fmul_rn(fmaxf(__fsub_rn(p, q), 0.0f), invZ[i]);
-    *q_out = q;
-    return p;
+// The residual chain in closed form.  With a = p and b = q of the node,
+// t_0 = 0 and S(t) = sum_v max(0, a_v - t b_v), the distribution after k
+// rejections is p_k = max(0, a - t_k b) / S(t_k), t_(k+1) = t_k + S(t_k)
+// (induction on norm(max(0, p_(k-1) - q)); p_0 = a, S(0) = 1, t_1 = 1).
+// One element's a and b at the node; operations pinned, so that a
+// candidate's test, the passes and the final scan compute identical bits.
+__device__ __forceinline__ void tree_pq(float zt, float zd, float c, float lth, float ltl, float ldh, float ldl,
+                                        float *a, float *bq) {
+    *a = ex2(__fsub_rn(__fmaf_rn(zt, c, -lth), ltl));
+    *bq = ex2(__fsub_rn(__fmaf_rn(zd, c, -ldh), ldl));
 }
 
-// Weight of one element: the residual max(0, p_L - q) (p_only: p_L itself).
+// Weight of one element at level t: max(0, a - t b) (t = 0: a itself).
 struct TreeWeight {
-    float c, lth, ltl, ldh, ldl;
-    const float *invZ;
-    int L;
-    bool p_only;
+    float c, lth, ltl, ldh, ldl, t;
     __device__ __forceinline__ float operator()(float zt, float zd) const {
-        float q;
-        const float p = tree_level_p(zt, zd, c, lth, ltl, ldh, ldl, invZ, L, &q);
-        return p_only ? p : fmaxf(__fsub_rn(p, q), 0.0f);
+        float pa, pb;
+        tree_pq(zt, zd, c, lth, ltl, ldh, ldl, &pa, &pb);
+        return fmaxf(__fmaf_rn(-t, pb, pa), 0.0f);
     }
 };
 
 // One pass of the whole block over the current node's two rows: the mass of
-// W over every sub-chunk, to rm[sc] (warp w takes sub-chunks w, w + 16, ...).
+// W over every sub-chunk, to rm[sc].  Warp w takes sub-chunks w, w + 16,
+// ...; the loads of its next sub-chunk are issued before the current one is
+// reduced, so that they overlap.  (Not inlined: the walk's state would
+// otherwise share its registers.)
 template <int DT>
-__device__ void tree_pass(const unsigned char *rt, const unsigned char *rd, const Geometry &g, const TreeWeight &W,
+__device__ __noinline__ void tree_pass(const unsigned char *rt, const unsigned char *rd, const Geometry &g, const TreeWeight &W,
                           float *rm) {
     using E = Elem<DT>;
     const int lane = lane_id();
-    for (int sc = warp_id(); sc < g.n_sub; sc += kWalkWarps) {
+    auto load = [&](int sc, uint4 (&xt)[4], uint4 (&xd)[4]) -> int {
         int a, e1;
         sub_range(g, sc, &a, &e1);
         const int nvec = (e1 - a) / E::kPerVec;  // <= 128
         const uint4 *pt = reinterpret_cast<const uint4 *>(rt + static_cast<int64_t>(a) * E::kBytes);
         const uint4 *pd = reinterpret_cast<const uint4 *>(rd + static_cast<int64_t>(a) * E::kBytes);
-        uint4 xt4[4], xd4[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int i = lane + 32 * j;
             if (i < nvec) {
-                xt4[j] = ld_stream(pt + i);
-                xd4[j] = ld_stream(pd + i);
+                xt[j] = ld_stream(pt + i);
+                xd[j] = ld_stream(pd + i);
             }
         }
+        return nvec;
+    };
+    auto mass = [&](const uint4 (&xt)[4], const uint4 (&xd)[4], int nvec) -> float {
         float acc = 0.0f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             if (lane + 32 * j >= nvec) continue;
             float x1[E::kPerVec], x2[E::kPerVec];
-            E::unpack(xt4[j], x1);
-            E::unpack(xd4[j], x2);
+            E::unpack(xt[j], x1);
+            E::unpack(xd[j], x2);
 #pragma unroll
             for (int q = 0; q < E::kPerVec; ++q) acc += W(x1[q], x2[q]);
         }
-        const float sum = warp_sum_f(acc);
+        return warp_sum_f(acc);
+    };
+    int sc = warp_id();
+    if (sc >= g.n_sub) return;
+    uint4 ct[4], cd[4];
+    int nc = load(sc, ct, cd);
+    for (;;) {
+        const int sn = sc + kWalkWarps;
+        uint4 nt[4], nd[4];
+        int nn = 0;
+        if (sn < g.n_sub) nn = load(sn, nt, nd);
+        const float sum = mass(ct, cd, nc);
         if (lane == 0) rm[sc] = sum;
+        if (sn >= g.n_sub) break;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            ct[j] = nt[j];
+            cd[j] = nd[j];
+        }
+        nc = nn;
+        sc = sn;
     }
 }
 
@@ -337,8 +356,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
         // the children in order
         const unsigned char *rt = static_cast<const unsigned char *>(target) + urow * rb;
         const unsigned char *rd = static_cast<const unsigned char *>(draft) + urow * rb;
-        const TreeWeight base{c, sm.lth, sm.ltl, sm.ldh, sm.ldl, sm.invZ, 0, false};
-        int L = 0, j = 0, next = -1;
+        const TreeWeight base{c, sm.lth, sm.ltl, sm.ldh, sm.ldl, 0.0f};
+        if (tid == 0) {
+            sm.t = 0.0;  // p itself
+            sm.S = 1.0f;
+        }
+        int j = 0, next = -1;
         bool zero_last = false;
         for (unsigned long long rest = kids; rest; rest &= rest - 1ull, ++j) {
             const int ch = __ffsll(static_cast<long long>(rest)) - 1;
@@ -358,9 +381,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
                         alpha = lr >= 0.0 ? 1.0f : exp2f(static_cast<float>(lr));
                     }
                 } else {
-                    float q;
-                    const float px = tree_level_p(zt, zd, c, sm.lth, sm.ltl, sm.ldh, sm.ldl, sm.invZ, L, &q);
-                    alpha = (zd == -INFINITY || q == 0.0f) ? (px > 0.0f ? 1.0f : 0.0f) : fminf(1.0f, px / q);
+                    // p_k(x) / q(x) = max(0, a - t b) / (S b) at the current level
+                    float pa, pb;
+                    tree_pq(zt, zd, c, sm.lth, sm.ltl, sm.ldh, sm.ldl, &pa, &pb);
+                    const float num = fmaxf(__fmaf_rn(-static_cast<float>(sm.t), pb, pa), 0.0f);
+                    alpha = (zd == -INFINITY || pb == 0.0f) ? (num > 0.0f ? 1.0f : 0.0f)
+                                                            : fminf(1.0f, num / (sm.S * pb));
                 }
                 sm.next = u_accept[g0 + ch] < alpha ? ch : -1;
             }
@@ -369,7 +395,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
                 next = sm.next;
                 break;
             }
-            // rejected: one pass over u's rows for the residual at level L
+            // rejected: the next level t' = t + S(t), and one pass over u's
+            // rows for S(t') and its per-sub-chunk masses
             if (j == 0 && warp == 0 && SPEC_RESID_PREFETCH) {
                 // both rows to L2 in 32 KB bulk prefetches: the later passes hit L2
                 constexpr int64_t kPiece = 32768;
@@ -377,24 +404,23 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
                 for (int64_t off = static_cast<int64_t>(lane >> 1) * kPiece; off < rb; off += 16 * kPiece)
                     bulk_prefetch_l2(r0 + off, static_cast<uint32_t>(min(kPiece, rb - off)));
             }
+            const double tn = sm.t + static_cast<double>(sm.S);
             TreeWeight W = base;
-            W.L = L;
+            W.t = static_cast<float>(tn);
             tree_pass<DT>(rt, rd, g, W, rm);
             __syncthreads();
             if (warp == 0) {
-                const float Z = warp_total(rm, g.n_sub);
+                const float Sn = warp_total(rm, g.n_sub);
                 if (lane == 0) {
-                    sm.zpos = Z > 0.0f;
-                    if (Z > 0.0f) sm.invZ[L] = __frcp_rn(Z);
+                    sm.zpos = Sn > 0.0f;
+                    if (Sn > 0.0f) {
+                        sm.t = tn;
+                        sm.S = Sn;
+                    }
                 }
             }
             __syncthreads();
-            if (sm.zpos) {
-                ++L;
-                zero_last = false;
-            } else {
-                zero_last = true;  // p stays as it was (the residual mass rounded to 0)
-            }
+            zero_last = !sm.zpos;  // a mass that rounded to 0 leaves p as it was
         }
         if (next >= 0) {
             if (tid == 0) sm.path[nacc] = sm.tok[next];
@@ -403,29 +429,36 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
             __syncthreads();
             continue;
         }
-        // every child rejected: draw from the last residual (after a mass
-        // that rounded to 0, from p at the current level)
+        // every child rejected: draw from p_k = max(0, a - t b) / S at the
+        // current level, whose masses the last pass left in rm (after a
+        // mass that rounded to 0, they are computed again; at t = 0 the
+        // draw is the bonus draw from the row's partials)
         TreeWeight W = base;
-        if (zero_last) {
-            W.L = L;
-            W.p_only = true;
+        W.t = static_cast<float>(sm.t);
+        const bool from_partials = zero_last && sm.t == 0.0;
+        if (zero_last && !from_partials) {
             tree_pass<DT>(rt, rd, g, W, rm);
             __syncthreads();
-        } else {
-            W.L = L - 1;
         }
         if (warp == 0) {
-            float w[kPartCache];
-#pragma unroll
-            for (int q = 0; q < kPartCache; ++q) w[q] = (lane + 32 * q < g.n_sub) ? __ldcg(rm + lane + 32 * q) : 0.0f;
-            auto wfar = [&](int i) -> float { return __ldcg(rm + i); };
-            F2 before, Z, tgt;
-            const int sc = warp_locate(g.n_sub, w, wfar, u_resample[urow], &before, &Z, &tgt);
             int tk = -1;
-            if (sc >= 0) {
-                int a, e1;
-                sub_range(g, sc, &a, &e1);
-                tk = warp_scan_elems<DT>(rt, rd, a, e1, W, before, tgt);
+            if (from_partials) {
+                const float2 *pr = part + urow * g.n_sub;
+                float2 pc[kPartCache];
+                load_parts(pr, g.n_sub, pc);
+                tk = warp_draw_row<DT>(target, urow, pr, pc, g, c, sm.M, u_resample[urow]);
+            } else {
+                float w[kPartCache];
+#pragma unroll
+                for (int q = 0; q < kPartCache; ++q) w[q] = (lane + 32 * q < g.n_sub) ? __ldcg(rm + lane + 32 * q) : 0.0f;
+                auto wfar = [&](int i) -> float { return __ldcg(rm + i); };
+                F2 before, Z, tgt;
+                const int sc = warp_locate(g.n_sub, w, wfar, u_resample[urow], &before, &Z, &tgt);
+                if (sc >= 0) {
+                    int a, e1;
+                    sub_range(g, sc, &a, &e1);
+                    tk = warp_scan_elems<DT>(rt, rd, a, e1, W, before, tgt);
+                }
             }
             if (lane == 0) sm.token = tk;
         }
