@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--tree", type=int, default=1, help="also time the tree verify workload (0: skip)")
+    ap.add_argument("--vocab-shard", default="2,4,8",
+                    help="rank counts of the vocab-sharded verify to time ('' to skip)")
     return ap.parse_args()
 
 
@@ -296,6 +298,90 @@ def measure_tree(torch, sv, dev, reps, warmup):
                      "spec_tree_draft_sample (setup + stats_kernel tree-draft mode + tree_draft_select_kernel)"}
 
 
+def measure_vocab_shard(torch, sv, dev, reps, warmup, Gs):
+    """One rank's share of the vocab-sharded verify on the 512-sequence ragged
+    workload (V = 128256, bf16, T = 1) with the vocabulary split over G
+    ranks.  The G ranks are emulated on this GPU: every rank's columns are
+    cut out once, the gathered records and masses (the inputs of decide and
+    draw) come from one untimed pass over all ranks, then each rank's three
+    calls (spec_shard_stats, spec_shard_decide, spec_shard_draw) are timed
+    with CUDA events, the ranks interleaved so that a rank's columns leave
+    L2 before its next run.  On G GPUs the ranks run in parallel: the
+    slowest rank's time is the step's, plus two all-gathers and one
+    all-reduce that are not measured here."""
+    import workloads
+    from speculative_decoding_verification_61_gb300.vocab_shard import VocabShardVerifier, even_bounds
+    w = workloads.make_config(5)
+    d = to_device(w, torch, dev)
+    toks = sv.spec_draft_sample(d["dl"], d["T"], d["ud"], d["ko"])
+    ab = workloads.algorithmic_bytes(w)
+    stream = torch.cuda.current_stream()
+    out = {}
+    for G in Gs:
+        bounds = even_bounds(w.V, G)
+        vs = [VocabShardVerifier(bounds, r, w.B, sv.BF16, dev) for r in range(G)]
+        cols = [(d["tl"][:, a:b].contiguous(), d["dl"][:, a:b].contiguous()) for a, b in zip(bounds, bounds[1:])]
+        recs = torch.stack([v.stats(t, q, toks, d["T"], d["ko"]) for v, (t, q) in zip(vs, cols)])
+        outs = [v.decide(recs, d["ua"]) for v in vs]
+        mass = torch.stack([o[2] for o in outs])
+        tok_out = [o[0] for o in outs]
+
+        def rank_call(r):
+            v, (t, q) = vs[r], cols[r]
+            v.stats(t, q, toks, d["T"], d["ko"])
+            v.decide(recs, d["ua"])
+            v.draw(mass, d["ur"], tok_out[r])
+        for _ in range(max(3, warmup)):
+            for r in range(G):
+                rank_call(r)
+        torch.cuda.synchronize()
+        # each rank's calls as one CUDA graph (what a serving loop replays),
+        # and issued one by one from Python (host-bound at small widths)
+        graphs = []
+        for r in range(G):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                rank_call(r)
+            graphs.append(g)
+        torch.cuda.synchronize()
+
+        def timed(run):
+            ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(G)]
+                  for _ in range(reps)]
+            for i in range(reps):
+                for r in range(G):
+                    ev[i][r][0].record(stream)
+                    run(r)
+                    ev[i][r][1].record(stream)
+            torch.cuda.synchronize()
+            return [statistics.mean(ev[i][r][0].elapsed_time(ev[i][r][1]) for i in range(reps)) for r in range(G)]
+        per_rank_eager = timed(rank_call)
+        for _ in range(3):
+            for r in range(G):
+                graphs[r].replay()
+        per_rank = timed(lambda r: graphs[r].replay())
+        worst = max(per_rank)
+        Vs_max = max(b - a for a, b in zip(bounds, bounds[1:]))
+        rows_rec = w.rows_target + w.rows_draft
+        # the rank's columns of every needed row once, one row-equivalent of
+        # them per sampled sequence for the draw, its records out and all
+        # ranks' records in
+        rank_bytes = (w.elem_bytes * Vs_max * (ab["rows_needed"] + ab["sampled_sequences"]) +
+                      16 * rows_rec * (1 + G) + 16 * w.B * (1 + G))
+        gbs = rank_bytes / (worst * 1e-3) / 1e9
+        out[str(G)] = {"ranks": G, "columns_per_rank": Vs_max, "rank_ms_max": round(worst, 5),
+                       "rank_ms_mean": round(statistics.mean(per_rank), 5),
+                       "rank_ms_max_eager": round(max(per_rank_eager), 5), "rank_bytes": int(rank_bytes),
+                       "rank_gbs": gbs, "rank_frac_of_8tbs": gbs / 8000.0,
+                       "rows_per_s_without_exchanges": rows_rec / (worst * 1e-3)}
+        del vs, cols, recs, outs, mass, tok_out, graphs
+    del d
+    return {"workload": w.name, "by_ranks": out,
+            "calls": "per rank, replayed as one CUDA graph (rank_ms_*; issued from Python: rank_ms_max_eager): "
+                     "spec_shard_stats (ticket reset + stats_kernel shard mode + shard_row_kernel), "
+                     "spec_shard_decide (shard_decide_kernel), spec_shard_draw (shard_draw_kernel); exchanges not timed"}
+
+
 def adaptive_k_timing(torch, sv, dev, B=4096, reps=1000):
     """Device time of one adaptive-k update (spec_adapt_update) for B
     sequences, the round-to-round step of a serving loop."""
@@ -479,6 +565,9 @@ def main():
 
     adapt = adaptive_k_timing(torch, sv, dev) if rank == 0 else None
     tree = measure_tree(torch, sv, dev, max(50, args.steps // 4), args.warmup) if rank == 0 and args.tree else None
+    shard_gs = [int(x) for x in args.vocab_shard.split(",") if x.strip()]
+    vshard = (measure_vocab_shard(torch, sv, dev, max(20, args.steps // 20), args.warmup, shard_gs)
+              if rank == 0 and shard_gs else None)
 
     e2e_line = None
     if rank == 0 and args.e2e_steps > 0:
@@ -532,6 +621,7 @@ def main():
         "other_workloads": extra,
         "adaptive_k": adapt,
         "tree_verify": tree,
+        "vocab_sharded_verify": vshard,
     }
     print(json.dumps(line))
     if world > 1:

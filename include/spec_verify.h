@@ -322,6 +322,98 @@ int spec_tree_draft_sample(const void *draft_logits, const int32_t *node_offsets
                            int32_t *out_tokens, void *stream);
 
 /*
+ * Vocab-sharded verify.  The vocabulary is split over G ranks (as when a
+ * tensor-parallel LM head leaves each GPU the logits of its own columns):
+ * rank r holds columns [V_r, V_{r+1}) of every target and draft row, with
+ * shard_bounds = {V_0 = 0 < V_1 < ... < V_G = V}.  The result is that of
+ * spec_verify on the whole rows (operations (a)-(d) at the top of this
+ * file); only the floating-point order of the sums differs.  One verify is
+ * three calls per rank with two exchanges between them, which the caller
+ * makes (an all-gather each, e.g. NCCL).  (docs.ifdog.com "投机解码",
+ * 实践要点, names the extra synchronisation of multi-GPU tensor parallelism
+ * as a cost; the split below is this library's design, not the pages'.)
+ *
+ *   1. spec_shard_stats  -> out_stats, one record per row of this shard;
+ *      all-gather: all_stats = the G ranks' out_stats, rank-major.
+ *   2. spec_shard_decide -> every rank combines the G records of each row
+ *      in rank order (so all ranks take the same decisions): accept test,
+ *      n_b, the accepted prefix, the greedy token; for a draw, this rank's
+ *      share of its mass: out_mass [B][2] = { mass of the distribution to
+ *      draw from (the residual max(0, p_j - q_j) at j = n_b, or p_{k_b}),
+ *      mass of p at position n_b } over this rank's columns;
+ *      all-gather: all_mass = the G ranks' out_mass, rank-major.
+ *   3. spec_shard_draw   -> Z = sum of the G masses (in rank order), target
+ *      u * Z; the rank whose columns hold the crossing of the cumulative
+ *      mass draws inside its columns and writes the token; the others leave
+ *      -1 in that slot.  If Z is 0 the draw uses the second mass, i.e. p
+ *      (as spec_verify does).
+ *   The caller then combines out_tokens over ranks with an element-wise
+ *   maximum (all-reduce MAX): accepted tokens and greedy tokens are equal
+ *   on every rank, and the drawn token is -1 everywhere but on its owner.
+ *   out_num_accepted is equal on every rank after step 2.
+ *
+ * The three calls of one verify must use the same workspace (device,
+ * 256-byte aligned, spec_shard_workspace_bytes(B, V_{r+1} - V_r, dtype)
+ * bytes, owned by the caller, zero-filled before its first use so that its
+ * status word reads SPEC_OK), unmodified in between, and the same B,
+ * k_offsets, temperature, shard_bounds and rank.
+ *
+ *   target_shard  [R_t, Vs]   rank r's columns of the target rows, row-major
+ *                             (Vs = V_{r+1} - V_r); draft_shard [R_d, Vs]
+ *   draft_tokens, u_accept, u_resample, temperature, k_offsets: as for
+ *                             spec_verify (global token ids), the same on
+ *                             every rank
+ *   shard_bounds  HOST int32 [G+1], 1 <= G <= SPEC_MAX_SHARDS, 0 <= rank < G;
+ *                             every shard width (V_{r+1} - V_r) a multiple
+ *                             of 4 (fp32) or 8 (bf16)
+ *   out_stats     spec_shard_stat_t [R_t + R_d]: target row t at index t,
+ *                             draft row d at index R_t + d
+ *   all_stats     spec_shard_stat_t [G][R_t + R_d], 16-byte aligned
+ *   out_mass      double [B][2];  all_mass double [G][B][2], 16-byte aligned
+ *   out_tokens, out_num_accepted: as for spec_verify
+ * Errors: as for spec_verify (data errors mark their sequence on every
+ * rank; an invalid k_offsets array fails the call on the device), plus
+ * SPEC_ERR_INVALID_ARG for bad shard_bounds / G / rank or a NULL
+ * workspace, SPEC_ERR_WORKSPACE for a small one.
+ */
+#define SPEC_MAX_SHARDS 64
+
+/* One row's statistics over one shard's columns (16 bytes).
+ *   sampled row: m = max over the columns of z * log2(e) / T (-inf when
+ *     every column is -inf), s = sum of 2^(z * log2(e) / T - m) (0 then;
+ *     NaN when a column holds NaN or +inf), zx = the logit of the row's
+ *     drafted token if this shard holds that column (else 0), arg = 0;
+ *   greedy row: m = the largest logit, arg = global column of its first
+ *     occurrence (-1 when a column holds NaN), s = zx = 0;
+ *   a row the verify does not need: m = -inf, s = NaN, zx = 0, arg = -1. */
+typedef struct {
+    float m;
+    float s;
+    float zx;
+    int32_t arg;
+} spec_shard_stat_t;
+
+size_t spec_shard_workspace_bytes(int B, int Vs, int dtype);
+
+int spec_shard_stats(const void *target_shard, const void *draft_shard,
+                     const int32_t *draft_tokens, const float *temperature, int B,
+                     const int32_t *k_offsets, const int32_t *shard_bounds, int G, int rank,
+                     int dtype, spec_shard_stat_t *out_stats, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
+int spec_shard_decide(const void *target_shard, const void *draft_shard,
+                      const spec_shard_stat_t *all_stats, const int32_t *draft_tokens,
+                      const float *u_accept, const float *temperature, int B,
+                      const int32_t *k_offsets, const int32_t *shard_bounds, int G, int rank,
+                      int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
+                      double *out_mass, void *workspace, size_t workspace_bytes, void *stream);
+
+int spec_shard_draw(const void *target_shard, const void *draft_shard, const double *all_mass,
+                    const float *u_resample, int B, const int32_t *k_offsets,
+                    const int32_t *shard_bounds, int G, int rank, int dtype,
+                    int32_t *out_tokens, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Adaptive draft length (sxl-space.tk "【大模型】- 推测解码", 自适应推测解码:
  * AdaptiveSpeculativeDecoder.adapt_k), per sequence and on the device.
  *

@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     F32,
     MAX_B,
     MAX_K,
+    MAX_SHARDS,
     MAX_TREE_NODES,
     MAX_V,
     SPEC_ERRORS,
@@ -25,10 +26,15 @@ from ._binding import (  # noqa: F401
     lib,
     lib_path,
     noalloc_bytes,
+    shard_workspace,
+    shard_workspace_bytes,
     spec_draft_sample,
     spec_draft_sample_lse,
     spec_round,
     spec_round_host,
+    spec_shard_decide,
+    spec_shard_draw,
+    spec_shard_stats,
     spec_tree_draft_sample,
     spec_tree_verify,
     spec_verify,

@@ -10,6 +10,7 @@ _LIB_PATH = os.path.join(PKG, "_build", "libspecverify.so")
 F32, BF16 = 0, 1
 MAX_K, MAX_B, MAX_V = 32, 4096, 1 << 24
 MAX_TREE_NODES = 64
+MAX_SHARDS = 64
 ABI_VERSION = 1
 SPEC_ERRORS = {0: "SPEC_OK", -1: "SPEC_ERR_INVALID_ARG", -2: "SPEC_ERR_ALIGNMENT",
                -3: "SPEC_ERR_CUDA", -4: "SPEC_ERR_TIMEOUT", -5: "SPEC_ERR_WORKSPACE"}
@@ -20,7 +21,8 @@ EXPORTS = ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sam
            "spec_status_string", "spec_abi_version", "spec_last_error", "spec_verify_noalloc",
            "spec_noalloc_bytes", "spec_adapt_state_bytes", "spec_adapt_init", "spec_adapt_update",
            "spec_draft_sample_lse", "spec_verify_lse", "spec_round", "spec_tree_verify",
-           "spec_tree_draft_sample")
+           "spec_tree_draft_sample", "spec_shard_workspace_bytes", "spec_shard_stats",
+           "spec_shard_decide", "spec_shard_draw")
 
 
 class SpecError(RuntimeError):
@@ -64,6 +66,11 @@ def lib():
     L.spec_round.argtypes = [vp, vp, vp, vp, vp, vp, ip, vp, ip, ip, vp, vp, vp, vp]
     L.spec_tree_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ip, ip, ip, ip, vp, vp, vp, vp]
     L.spec_tree_draft_sample.argtypes = [vp, vp, vp, vp, vp, ip, ip, ip, ip, vp, vp]
+    L.spec_shard_workspace_bytes.argtypes = [ip, ip, ip]
+    L.spec_shard_workspace_bytes.restype = sz
+    L.spec_shard_stats.argtypes = [vp, vp, vp, vp, ip, vp, vp, ip, ip, ip, vp, vp, sz, vp]
+    L.spec_shard_decide.argtypes = [vp, vp, vp, vp, vp, vp, ip, vp, vp, ip, ip, ip, vp, vp, vp, vp, sz, vp]
+    L.spec_shard_draw.argtypes = [vp, vp, vp, vp, ip, vp, vp, ip, ip, ip, vp, vp, sz, vp]
     L.spec_workspace_bytes.argtypes = [ip, ip, ip]
     L.spec_workspace_bytes.restype = sz
     L.spec_noalloc_bytes.argtypes = [ip, ip, ip]
@@ -85,7 +92,7 @@ def lib():
     for name in ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",
                  "spec_round_host", "spec_workspace_status", "spec_abi_version",
                  "spec_draft_sample_lse", "spec_verify_lse", "spec_round", "spec_tree_verify",
-                 "spec_tree_draft_sample"):
+                 "spec_tree_draft_sample", "spec_shard_stats", "spec_shard_decide", "spec_shard_draw"):
         getattr(L, name).restype = ip
     _lib = L
     return L
@@ -392,6 +399,112 @@ def spec_round_host(target_logits, draft_logits, u_draft, u_accept, u_resample, 
                                _stream(stream))
     _raise(rc, "spec_round_host")
     return out_draft_tokens, out_tokens, out_num_accepted
+
+
+# ------------------------------------------------------- vocab-sharded verify
+def _bounds(shard_bounds):
+    b = [int(x) for x in shard_bounds]
+    return (ctypes.c_int32 * len(b))(*b), len(b) - 1
+
+
+def _ws_args(workspace):
+    _check_dev("workspace", workspace)
+    return _p(workspace), workspace.numel() * workspace.element_size()
+
+
+def shard_workspace_bytes(B: int, Vs: int, dtype: int) -> int:
+    """Workspace bytes of one rank's vocab-sharded verify (Vs columns)."""
+    return int(lib().spec_shard_workspace_bytes(B, Vs, dtype))
+
+
+def shard_workspace(B: int, Vs: int, dtype: int, device="cuda"):
+    """A zero-filled workspace tensor for spec_shard_* (the caching
+    allocator's blocks are 512-byte aligned; the zeros clear the status
+    word that workspace_status reads)."""
+    import torch
+    n = shard_workspace_bytes(B, Vs, dtype)
+    if n == 0:
+        raise ValueError(f"invalid shard workspace arguments B={B}, Vs={Vs}, dtype={dtype}")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def spec_shard_stats(target_shard, draft_shard, draft_tokens, temperature, k_offsets, shard_bounds, rank,
+                     workspace, out_stats=None, stream=None):
+    """Step 1 of the vocab-sharded verify on this rank's columns.  Returns
+    the row records as int32 [R_t + R_d, 4] (fields m, s, zx as float bits,
+    then arg)."""
+    import torch
+    B = temperature.numel()
+    dt = _dtype_code(target_shard)
+    for name, t in (("target_shard", target_shard), ("draft_shard", draft_shard)):
+        _check_dev(name, t, target_shard.dtype)
+    _check_dev("draft_tokens", draft_tokens, torch.int32)
+    _check_dev("temperature", temperature, torch.float32)
+    _check_dev("k_offsets", k_offsets, torch.int32)
+    rows = target_shard.shape[0] + draft_shard.shape[0]
+    if out_stats is None:
+        out_stats = torch.empty((rows, 4), dtype=torch.int32, device=target_shard.device)
+    bounds, G = _bounds(shard_bounds)
+    wp, wb = _ws_args(workspace)
+    rc = lib().spec_shard_stats(_p(target_shard), _p(draft_shard), _p(draft_tokens), _p(temperature), B,
+                                _p(k_offsets), bounds, G, rank, dt, _p(out_stats), wp, wb, _stream(stream))
+    _raise(rc, "spec_shard_stats")
+    return out_stats
+
+
+def spec_shard_decide(target_shard, draft_shard, all_stats, draft_tokens, u_accept, temperature, k_offsets,
+                      shard_bounds, rank, workspace, out_tokens=None, out_num_accepted=None, out_mass=None,
+                      stream=None):
+    """Step 2: the decision from the gathered records (all_stats: the G
+    ranks' records, rank-major).  Returns (out_tokens [R_t] int32,
+    out_num_accepted [B] int32, out_mass [B, 2] float64)."""
+    import torch
+    B = temperature.numel()
+    dt = _dtype_code(target_shard)
+    bounds, G = _bounds(shard_bounds)
+    R_t, R_d = target_shard.shape[0], draft_shard.shape[0]
+    _check_dev("all_stats", all_stats, torch.int32)
+    if all_stats.numel() != G * (R_t + R_d) * 4:
+        raise ValueError("all_stats must hold G * (R_t + R_d) records")
+    for name, t in (("draft_tokens", draft_tokens), ("k_offsets", k_offsets)):
+        _check_dev(name, t, torch.int32)
+    for name, t in (("u_accept", u_accept), ("temperature", temperature)):
+        _check_dev(name, t, torch.float32)
+    dev = target_shard.device
+    if out_tokens is None:
+        out_tokens = torch.empty(R_t, dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_mass is None:
+        out_mass = torch.empty((B, 2), dtype=torch.float64, device=dev)
+    wp, wb = _ws_args(workspace)
+    rc = lib().spec_shard_decide(_p(target_shard), _p(draft_shard), _p(all_stats), _p(draft_tokens), _p(u_accept),
+                                 _p(temperature), B, _p(k_offsets), bounds, G, rank, dt, _p(out_tokens),
+                                 _p(out_num_accepted), _p(out_mass), wp, wb, _stream(stream))
+    _raise(rc, "spec_shard_decide")
+    return out_tokens, out_num_accepted, out_mass
+
+
+def spec_shard_draw(target_shard, draft_shard, all_mass, u_resample, k_offsets, shard_bounds, rank, workspace,
+                    out_tokens, stream=None):
+    """Step 3: the draw by the rank owning the crossing (all_mass: the G
+    ranks' out_mass, rank-major).  Writes the drawn token into out_tokens
+    on that rank; returns out_tokens."""
+    import torch
+    B = k_offsets.numel() - 1
+    dt = _dtype_code(target_shard)
+    bounds, G = _bounds(shard_bounds)
+    _check_dev("all_mass", all_mass, torch.float64)
+    if all_mass.numel() != G * B * 2:
+        raise ValueError("all_mass must hold G * B * 2 values")
+    _check_dev("u_resample", u_resample, torch.float32)
+    _check_dev("k_offsets", k_offsets, torch.int32)
+    _check_dev("out_tokens", out_tokens, torch.int32)
+    wp, wb = _ws_args(workspace)
+    rc = lib().spec_shard_draw(_p(target_shard), _p(draft_shard), _p(all_mass), _p(u_resample), B, _p(k_offsets),
+                               bounds, G, rank, dt, _p(out_tokens), wp, wb, _stream(stream))
+    _raise(rc, "spec_shard_draw")
+    return out_tokens
 
 
 def workspace_bytes(B: int, V: int, dtype: int) -> int:

@@ -132,7 +132,8 @@ enum StatsMode : int {
     kModeTarget = 2,     // target rows only (verify with the draft rows' lse given)
     kModeTree = 3,       // tree verify: every node's target row, plus the draft rows of
                          // the internal nodes of sampled sequences
-    kModeTreeDraft = 4   // tree drafting: the draft rows of internal nodes
+    kModeTreeDraft = 4,  // tree drafting: the draft rows of internal nodes
+    kModeShard = 5       // vocab-sharded verify: as kModeVerify, over one shard's columns
 };
 
 // Nodes per sequence of a tree call, and the per-sequence tables the tree
@@ -594,25 +595,28 @@ static __device__ int warp_combine_arg(const float2 *p, int n) {
     return a.i == INT_MAX ? -1 : a.i;
 }
 
-// Warp-level locate over n non-negative weights (sub-chunk masses): total
-// Z, target = u * Z, and the first i whose cumulative mass exceeds the
-// target, with the mass before it.  If rounding leaves no such i, the last
-// i with positive weight.  Returns -1 if every weight is 0.  Weight i is
-// cache[j] of lane i % 32 for i = lane + 32 j < 32 * kPartCache, wfar(i)
-// beyond.
+// warp_locate: warp-level locate over n non-negative weights (sub-chunk
+// masses): total Z, target = u * Z, and the first i whose cumulative mass
+// exceeds the target, with the mass before it.  If rounding leaves no such
+// i, the last i with positive weight.  Returns -1 if every weight is 0.
+// Weight i is cache[j] of lane i % 32 for i = lane + 32 j < 32 * kPartCache,
+// wfar(i) beyond.  It is warp_total (Z as an unevaluated pair, the same bits
+// on every call with the same weights) followed by warp_locate_at (the scan
+// against a given target).
 template <class WF>
-__device__ int warp_locate(int n, const float (&cache)[kPartCache], WF wfar, float u, F2 *before, F2 *total,
-                           F2 *target_out) {
+__device__ F2 warp_total(int n, const float (&cache)[kPartCache], WF wfar) {
     const int lane = lane_id();
-    constexpr int kCache = kPartCache;
     Acc2 acc;
 #pragma unroll
-    for (int j = 0; j < kCache; ++j) acc.add(cache[j]);
-    for (int j = kCache; 32 * j < n; ++j) acc.add((lane + 32 * j < n) ? wfar(lane + 32 * j) : 0.0f);
-    const F2 tot = f2_two_sum(warp_sum_f(acc.hi), warp_sum_f(acc.lo));
-    const F2 target = f2_scale(u, tot);
-    *total = tot;
-    *target_out = target;
+    for (int j = 0; j < kPartCache; ++j) acc.add(cache[j]);
+    for (int j = kPartCache; 32 * j < n; ++j) acc.add((lane + 32 * j < n) ? wfar(lane + 32 * j) : 0.0f);
+    return f2_two_sum(warp_sum_f(acc.hi), warp_sum_f(acc.lo));
+}
+
+template <class WF>
+__device__ int warp_locate_at(int n, const float (&cache)[kPartCache], WF wfar, F2 target, F2 *before) {
+    const int lane = lane_id();
+    constexpr int kCache = kPartCache;
     F2 carry{0.0f, 0.0f}, last_before{0.0f, 0.0f};
     int last = -1;
     for (int j = 0; 32 * j < n; ++j) {
@@ -639,6 +643,16 @@ __device__ int warp_locate(int n, const float (&cache)[kPartCache], WF wfar, flo
     }
     *before = last_before;
     return last;
+}
+
+template <class WF>
+__device__ int warp_locate(int n, const float (&cache)[kPartCache], WF wfar, float u, F2 *before, F2 *total,
+                           F2 *target_out) {
+    const F2 tot = warp_total(n, cache, wfar);
+    const F2 target = f2_scale(u, tot);
+    *total = tot;
+    *target_out = target;
+    return warp_locate_at(n, cache, wfar, target, before);
 }
 
 #ifndef SPEC_RESID_PREFETCH

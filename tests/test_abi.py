@@ -32,7 +32,8 @@ def test_header_declares_expected_entry_points():
     for n in ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",
               "spec_round_host", "spec_workspace_bytes", "spec_workspace_status",
               "spec_status_string", "spec_abi_version", "spec_draft_sample_lse", "spec_verify_lse",
-              "spec_round", "spec_tree_verify", "spec_tree_draft_sample"):
+              "spec_round", "spec_tree_verify", "spec_tree_draft_sample", "spec_shard_workspace_bytes",
+              "spec_shard_stats", "spec_shard_decide", "spec_shard_draw"):
         assert n in names
 
 
@@ -118,3 +119,45 @@ def test_tree_host_argument_errors(lib):
                                 None, None) == 0
     assert lib.spec_tree_draft_sample(fake, fake, fake, fake, fake, 4, 3, 1000, 0, fake, None) == -1
     assert lib.spec_tree_draft_sample(fake, fake, fake, fake, fake, 4, 8, 1001, 1, fake, None) == -2
+
+
+def test_shard_host_argument_errors(lib):
+    """The vocab-sharded calls check bounds, G, rank, widths and the
+    workspace on the host before touching the device."""
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)  # never dereferenced: validation fails first
+
+    def bounds(*b):
+        return (ctypes.c_int32 * len(b))(*b)
+
+    ws_need = lib.spec_shard_workspace_bytes(4, 504, 1)
+    assert ws_need > 0 and ws_need % 256 == 0
+    assert lib.spec_shard_workspace_bytes(4, 501, 1) == 0   # bf16 width not a multiple of 8
+    assert lib.spec_shard_workspace_bytes(4, 0, 1) == 0
+    ok = bounds(0, 496, 1000)
+    ws = vp(1 << 24)  # 256-byte aligned, never dereferenced here
+
+    def stats(b, G, rank, dtype=1, ws_ptr=ws, ws_bytes=1 << 30, first=fake):
+        return lib.spec_shard_stats(first, fake, fake, fake, 4, fake, b, G, rank, dtype, fake, ws_ptr, ws_bytes,
+                                    None)
+
+    assert stats(None, 2, 0) == -1                      # no bounds
+    assert stats(ok, 0, 0) == -1 and stats(ok, 65, 0) == -1   # G outside [1, 64]
+    assert stats(ok, 2, 2) == -1 and stats(ok, 2, -1) == -1   # rank outside [0, G)
+    assert stats(bounds(8, 496, 1000), 2, 0) == -1      # must start at 0
+    assert stats(bounds(0, 496, 496), 2, 0) == -1       # an empty shard
+    assert stats(bounds(0, 500, 1000), 2, 0) == -2      # width 500: not a multiple of 8 (bf16)
+    assert stats(bounds(0, 500, 1000), 2, 0, dtype=0) != -2   # ... but of 4 (fp32): passes that check
+    assert stats(ok, 2, 0, dtype=3) == -1               # bad dtype
+    assert stats(ok, 2, 0, ws_ptr=None) == -1           # the workspace is required
+    assert stats(ok, 2, 0, ws_bytes=16) == -5           # too small
+    assert stats(ok, 2, 0, ws_ptr=vp((1 << 24) + 16)) == -2   # not 256-byte aligned
+    assert stats(ok, 2, 0, first=None) == -1            # a null logit pointer
+    assert stats(ok, 2, 0, first=vp((1 << 20) + 4)) == -2     # unaligned logits
+    assert lib.spec_shard_decide(fake, fake, None, fake, fake, fake, 4, fake, ok, 2, 0, 1, fake, fake, fake, ws,
+                                 1 << 30, None) == -1   # no gathered records
+    assert lib.spec_shard_draw(fake, fake, None, fake, 4, fake, ok, 2, 1, 1, fake, ws, 1 << 30, None) == -1
+    assert lib.spec_shard_draw(fake, fake, fake, fake, 4, fake, ok, 2, 1, 1, fake, ws, 16, None) == -5
+    # B = 0 is a no-op that still checks the shard arguments
+    assert lib.spec_shard_draw(None, None, None, None, 0, None, ok, 2, 1, 1, None, None, 0, None) == 0
+    assert lib.spec_shard_draw(None, None, None, None, 0, None, ok, 2, 2, 1, None, None, 0, None) == -1
