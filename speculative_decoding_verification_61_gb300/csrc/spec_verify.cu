@@ -74,11 +74,14 @@ struct ResolveSmem {
     float lth, ltl, ldh, ldl, u;
 };
 
+#ifndef SPEC_RESOLVE_THREADS
+#define SPEC_RESOLVE_THREADS 256
+#endif
 #ifndef SPEC_RESOLVE_MIN_BLOCKS
 #define SPEC_RESOLVE_MIN_BLOCKS 4
 #endif
 template <int DT>
-__global__ void __launch_bounds__(256, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
+__global__ void __launch_bounds__(SPEC_RESOLVE_THREADS, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
     const void *__restrict__ target, const void *__restrict__ draft,
     const int32_t *__restrict__ tokens, const float *__restrict__ u_accept,
     const float *__restrict__ u_resample, const float *__restrict__ temperature,
@@ -362,6 +365,13 @@ __global__ void __launch_bounds__(256, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
         const void *rd = static_cast<const unsigned char *>(draft) + drow * V * static_cast<int64_t>(E::kBytes);
         auto W = [&](float a1, float a2) -> float { return resid_weight(a1, a2, c, lth, ltl, ldh, ldl); };
         token = warp_scan_elems<DT>(rt, rd, a, e1, W, before, tgt);
+    } else {
+        // every residual weight rounded to 0: p at position n is drawn with
+        // the same uniform instead
+        const float2 *pr = ws.part + trow * g.n_sub;
+        float2 pc[kPartCache];
+        load_parts(pr, g.n_sub, pc);
+        token = warp_draw_row<DT>(target, trow, pr, pc, g, c, sm.M[n], sm.u);
     }
     if (lane == 0) {
         out_tokens[trow] = token;
@@ -645,7 +655,7 @@ int launch_verify(const void *target, const void *draft, const double *draft_lse
                               target, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, w.seqcnt,
                               nullptr, nullptr, 0);
     if (!cuda_ok(e1, "launch stats_kernel") ||
-        !cuda_ok(launch_k(true, resolve_kernel<DT>, dim3(B * nsplit), dim3(256), 0, stream, target, draft, tokens,
+        !cuda_ok(launch_k(true, resolve_kernel<DT>, dim3(B * nsplit), dim3(SPEC_RESOLVE_THREADS), 0, stream, target, draft, tokens,
                           u_accept, u_resample, temperature, k_offsets, draft_lse2, B, g, nsplit, w, out_tokens,
                           out_num, aux),
                  "launch resolve_kernel"))

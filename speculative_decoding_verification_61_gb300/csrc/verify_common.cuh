@@ -527,6 +527,10 @@ __device__ __forceinline__ double lse2(float M, float S) {
     return static_cast<double>(M) + static_cast<double>(e) + static_cast<double>(log2f(m));
 }
 
+#ifndef SPEC_ARG_BATCH
+#define SPEC_ARG_BATCH 1
+#endif
+
 // Sub-chunk partials a lane holds in registers: p[lane + 32 j], j < 8, so
 // rows of up to 256 sub-chunks take one memory round trip; the rest of a
 // longer row is read again where needed.
@@ -585,9 +589,21 @@ static __device__ bool warp_combine_soft(const float2 *p, int n, float *M_out, f
 }
 
 // Arg-max over the n sub-chunk partials of one row; -1 if a NaN was seen.
+// The first 32 * kPartCache partials arrive in one round trip (load_parts);
+// the merge is order-free (largest value, lowest index, NaN wins).
 static __device__ int warp_combine_arg(const float2 *p, int n) {
+    const int lane = lane_id();
     ArgPart a{-INFINITY, INT_MAX};
-    for (int i = lane_id(); i < n; i += 32) {
+#if SPEC_ARG_BATCH
+    float2 c[kPartCache];
+    load_parts(p, n, c);
+#pragma unroll
+    for (int j = 0; j < kPartCache; ++j)
+        if (lane + 32 * j < n) a = arg_merge(a, ArgPart{c[j].x, __float_as_int(c[j].y)});
+    for (int i = lane + 32 * kPartCache; i < n; i += 32) {
+#else
+    for (int i = lane; i < n; i += 32) {
+#endif
         const float2 v = __ldcg(p + i);
         a = arg_merge(a, ArgPart{v.x, __float_as_int(v.y)});
     }
