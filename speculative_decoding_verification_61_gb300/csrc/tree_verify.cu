@@ -51,13 +51,16 @@ namespace specv {
 // gets nint = -1; otherwise nint = its internal nodes (nodes with a child)
 // and tint[b * kMaxTreeNodes + j] = the j-th of them (global index,
 // ascending).  Sequences whose node count is out of range are left to the
-// whole-call check of the other kernels.
+// whole-call check of the other kernels.  pair[b] (if given) is zeroed for
+// the walk.
 __global__ void __launch_bounds__(256) tree_setup_kernel(const int *__restrict__ node_offsets,
                                                          const int *__restrict__ parent, int B, int N,
-                                                         int *__restrict__ nint, int *__restrict__ tint) {
+                                                         int *__restrict__ nint, int *__restrict__ tint,
+                                                         int *__restrict__ pair) {
     const int b = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = lane_id();
     if (b >= B) return;
+    if (lane == 0 && pair) pair[b] = 0;  // the walk's meeting counter of this tree
     const int g0 = node_offsets[b];
     const int n = node_offsets[b + 1] - g0;
     if (n < 1 || n > kMaxTreeNodes || g0 < 0 || g0 + n > N) {
@@ -94,22 +97,38 @@ __global__ void __launch_bounds__(256) tree_setup_kernel(const int *__restrict__
 }
 
 // ================================================================== walk
+#ifndef SPEC_TREE_PACKED
+#define SPEC_TREE_PACKED 1
+#endif
+// CTAs per tree: with 2, a tree is walked by a cluster of two CTAs on two
+// SMs; both take every decision (from the same data, so the same one) and
+// each makes half of every pass over the node's rows.
+#ifndef SPEC_TREE_CTAS
+#define SPEC_TREE_CTAS 2
+#endif
+constexpr int kTreeCtas = SPEC_TREE_CTAS;
+static_assert(kTreeCtas == 1 || kTreeCtas == 2, "one or two CTAs per tree");
 constexpr int kWalkThreads = 512;
 constexpr int kWalkWarps = kWalkThreads / 32;
 
 struct TreeWalkSmem {
     int par[kMaxTreeNodes];     // local parent of each node (-1: root)
     int tok[kMaxTreeNodes];     // drafted token of each node
-    float zt[kMaxTreeNodes];    // the current node's target logit at each child's token
-    float zd[kMaxTreeNodes];    // and its draft logit
+    // per node i, from the prologue (read only when the walk visits i)
+    float zt[kMaxTreeNodes];    // i's token's logit in its parent's target row
+    float zd[kMaxTreeNodes];    // and in its parent's draft row
+    float ua[kMaxTreeNodes];    // u_accept of i
+    double Lt[kMaxTreeNodes];   // log2-domain log-sum-exp of i's target row
+    double Ld[kMaxTreeNodes];   // and of its draft row (internal nodes)
+    float M[kMaxTreeNodes];     // max of i's target row (z * c)
+    float lth[kMaxTreeNodes], ltl[kMaxTreeNodes];  // Lt as an fp32 hi/lo pair
+    float ldh[kMaxTreeNodes], ldl[kMaxTreeNodes];  // Ld likewise
+    int am[kMaxTreeNodes];      // greedy: arg-max of i's target row
+    int ok[kMaxTreeNodes];      // i's target row is valid
+    int okd[kMaxTreeNodes];     // i's draft row is valid (or not needed)
     int path[kMaxTreeNodes];    // accepted tokens
     double t;                   // residual level of the current p at the node (0: p itself)
     float S;                    // its mass S(t)
-    double Lt, Ld;              // log2-domain log-sum-exp of the current node's rows
-    float M;                    // max of the current target row (z * c)
-    float lth, ltl, ldh, ldl;   // Lt and Ld as fp32 hi/lo pairs
-    int am;                     // greedy: arg-max of the current target row
-    int ok, okd;                // the current node's rows are valid
     int next;                   // accepted child (local index) or -1
     int zpos;                   // the last residual mass was > 0
     int token;                  // the drawn token
@@ -137,6 +156,21 @@ struct TreeWeight {
     }
 };
 
+// TreeWeight on two elements at once in packed fp32: lane for lane the same
+// operations (x - y is rounded exactly as x + (-y)), so the same bits.
+struct TreeWeight2 {
+    float2 c2, nlth2, nltl2, nldh2, nldl2, nt2;
+    __device__ __forceinline__ explicit TreeWeight2(const TreeWeight &w)
+        : c2(make_float2(w.c, w.c)), nlth2(make_float2(-w.lth, -w.lth)), nltl2(make_float2(-w.ltl, -w.ltl)),
+          nldh2(make_float2(-w.ldh, -w.ldh)), nldl2(make_float2(-w.ldl, -w.ldl)), nt2(make_float2(-w.t, -w.t)) {}
+    __device__ __forceinline__ float2 operator()(float2 zt, float2 zd) const {
+        const float2 at = fadd2(ffma2(zt, c2, nlth2), nltl2);
+        const float2 ad = fadd2(ffma2(zd, c2, nldh2), nldl2);
+        const float2 w = ffma2(nt2, make_float2(ex2(ad.x), ex2(ad.y)), make_float2(ex2(at.x), ex2(at.y)));
+        return make_float2(fmaxf(w.x, 0.0f), fmaxf(w.y, 0.0f));
+    }
+};
+
 // One pass of the whole block over the current node's two rows: the mass of
 // W over every sub-chunk, to rm[sc].  Warp w takes sub-chunks w, w + 16,
 // ...; the loads of its next sub-chunk are issued before the current one is
@@ -144,7 +178,7 @@ struct TreeWeight {
 // otherwise share its registers.)
 template <int DT>
 __device__ __noinline__ void tree_pass(const unsigned char *rt, const unsigned char *rd, const Geometry &g, const TreeWeight &W,
-                          float *rm) {
+                          float *rm, int sc_begin, int sc_end) {
     using E = Elem<DT>;
     const int lane = lane_id();
     auto load = [&](int sc, uint4 (&xt)[4], uint4 (&xd)[4]) -> int {
@@ -163,6 +197,22 @@ __device__ __noinline__ void tree_pass(const unsigned char *rt, const unsigned c
         }
         return nvec;
     };
+#if SPEC_TREE_PACKED
+    const TreeWeight2 W2(W);
+    auto mass = [&](const uint4 (&xt)[4], const uint4 (&xd)[4], int nvec) -> float {
+        float2 acc0 = make_float2(0.0f, 0.0f), acc1 = acc0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (lane + 32 * j >= nvec) continue;
+#pragma unroll
+            for (int p = 0; p < E::kPairs; ++p) {
+                const float2 w2 = W2(E::pair(xt[j], p), E::pair(xd[j], p));
+                if (p & 1) acc1 = fadd2(acc1, w2); else acc0 = fadd2(acc0, w2);
+            }
+        }
+        return warp_sum_f((acc0.x + acc0.y) + (acc1.x + acc1.y));
+    };
+#else
     auto mass = [&](const uint4 (&xt)[4], const uint4 (&xd)[4], int nvec) -> float {
         float acc = 0.0f;
 #pragma unroll
@@ -176,18 +226,19 @@ __device__ __noinline__ void tree_pass(const unsigned char *rt, const unsigned c
         }
         return warp_sum_f(acc);
     };
-    int sc = warp_id();
-    if (sc >= g.n_sub) return;
+#endif
+    int sc = sc_begin + warp_id();
+    if (sc >= sc_end) return;
     uint4 ct[4], cd[4];
     int nc = load(sc, ct, cd);
     for (;;) {
         const int sn = sc + kWalkWarps;
         uint4 nt[4], nd[4];
         int nn = 0;
-        if (sn < g.n_sub) nn = load(sn, nt, nd);
+        if (sn < sc_end) nn = load(sn, nt, nd);
         const float sum = mass(ct, cd, nc);
         if (lane == 0) rm[sc] = sum;
-        if (sn >= g.n_sub) break;
+        if (sn >= sc_end) break;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             ct[j] = nt[j];
@@ -196,6 +247,48 @@ __device__ __noinline__ void tree_pass(const unsigned char *rt, const unsigned c
         nc = nn;
         sc = sn;
     }
+    // this warp's masses visible to the other CTA of the tree before the meeting
+    if (kTreeCtas > 1 && lane == 0) __threadfence();
+}
+
+__device__ __forceinline__ unsigned cluster_ctarank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Meeting point of a tree's CTAs after a pass (a no-op with one CTA): each
+// CTA adds one to the tree's counter once its masses are written and
+// fenced, then waits until the counter reaches `target` (every CTA of the
+// tree has added for this pass).  The wait is bounded: on a time-out the
+// status word gets SPEC_ERR_TIMEOUT and false is returned.  The counter is
+// in global memory, so no CTA ever touches the other's shared memory.
+__device__ bool tree_meet(int *cnt, int target, int *status, int *s_flag) {
+    __syncthreads();  // this CTA's masses are written (each writer fenced them)
+    if (kTreeCtas == 1) return true;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(cnt, 1);
+        const uint64_t t0 = global_timer_ns();
+        bool ok = true;
+        while (ld_acquire_gpu(cnt) < target) {
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                ok = false;
+                set_status(status, SPEC_ERR_TIMEOUT);
+                break;
+            }
+            __nanosleep(64);
+        }
+        *s_flag = ok;
+    }
+    __syncthreads();
+    return *s_flag != 0;
 }
 
 // The total of the n masses rm[0 .. n) by one warp (fixed order: lane l
@@ -216,12 +309,16 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
     const void *__restrict__ target, const void *__restrict__ draft, const int *__restrict__ node_offsets,
     const int *__restrict__ parent, const int32_t *__restrict__ tokens, const float *__restrict__ u_accept,
     const float *__restrict__ u_resample, const float *__restrict__ temperature, int B, int N, Geometry g,
-    const float2 *__restrict__ part, const int *__restrict__ nint, float *__restrict__ resid,
-    int *__restrict__ counters, int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_num,
-    int32_t *__restrict__ out_last) {
+    const float2 *__restrict__ part, const int *__restrict__ nint, const int *__restrict__ tint,
+    float *__restrict__ resid, int *__restrict__ pair, int *__restrict__ counters, int32_t *__restrict__ out_tokens,
+    int32_t *__restrict__ out_num, int32_t *__restrict__ out_last) {
     using E = Elem<DT>;
     __shared__ TreeWalkSmem sm;
-    const int b = blockIdx.x;
+    __shared__ int s_meet;
+    // CTA cr of the tree's cluster (0 with one CTA per tree); CTA 0 draws
+    // and writes the outputs
+    const int cr = kTreeCtas > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int b = blockIdx.x / kTreeCtas;
     const int lane = lane_id(), warp = warp_id(), tid = threadIdx.x;
 
     // --- inputs only (written before this call) --------------------------
@@ -241,7 +338,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
     bad = __syncthreads_or(bad);
     if (bad) {
         grid_dependency_wait();
-        if (tid == 0) {
+        if (tid == 0 && cr == 0) {
             out_num[b] = -1;
             if (out_last) out_last[b] = -1;
             if (b == 0) set_status(counters + kStatus, SPEC_ERR_INVALID_ARG);
@@ -251,6 +348,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
     const int g0 = node_offsets[b], n = node_offsets[b + 1] - g0;
     const float c = temp_scale(temperature[b]);
     const bool greedy = c == 0.0f;
+    // a greedy walk makes no pass: CTA 0 does it alone
+    if (greedy && cr != 0) return;
     const int V = g.V;
     bool tokbad = false;
     if (tid < n) {
@@ -265,8 +364,99 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
 
     bool err = (c != c) || tokbad || nint[b] < 0;
     int u = 0, nacc = 0, final_token = -1;
-    float *rm = resid + static_cast<int64_t>(b) * g.n_sub;
+    // per-sub-chunk masses, two buffers used in turn by successive passes
+    // (a CTA may start the next pass while the other still reads the last)
+    float *const rm_base = resid + static_cast<int64_t>(b) * 2 * g.n_sub;
+    int passes = 0;
+    float *rm = rm_base;
+    // this CTA's share of every pass: a contiguous half of the sub-chunks
+    const int half = (g.n_sub + kTreeCtas - 1) / kTreeCtas;
+    const int sc0 = min(g.n_sub, cr * half), sc1 = min(g.n_sub, sc0 + half);
+    int *const meet_cnt = pair + b;
+    auto pass = [&](const unsigned char *prt, const unsigned char *prd, const TreeWeight &W) -> bool {
+        rm = rm_base + (passes & 1) * g.n_sub;
+        tree_pass<DT>(prt, prd, g, W, rm, sc0, sc1);
+        ++passes;
+        return tree_meet(meet_cnt, kTreeCtas * passes, counters + kStatus, &s_meet);
+    };
     const int64_t rb = static_cast<int64_t>(V) * E::kBytes;
+
+    // --- prologue: the statistics of every node's rows (the n target rows,
+    // then the internal nodes' draft rows; each warp takes two rows at a
+    // time, both rows' partials loaded before either is combined) and every
+    // child's logits at its token, so that the walk itself only tests
+    if (!err) {
+        if (tid < n) {
+            sm.ua[tid] = u_accept[g0 + tid];
+            // a leaf's draft row is not needed; an internal node's okd is
+            // written by its row's combine below (no other write, no race)
+            bool internal = false;
+            for (int i = tid + 1; i < n; ++i) internal |= sm.par[i] == tid;
+            if (!internal) sm.okd[tid] = 1;
+            if (!greedy && tid > 0) {
+                const int64_t prow = g0 + sm.par[tid];
+                sm.zt[tid] = E::load1(target, prow * V + sm.tok[tid]);
+                sm.zd[tid] = E::load1(draft, prow * V + sm.tok[tid]);
+            }
+        }
+        const int items = n + (greedy ? 0 : nint[b]);
+        // partials of item k: target row of node k, or the draft row of the
+        // (k - n)-th internal node
+        auto item_part = [&](int k) -> const float2 * {
+            const int64_t slot = k < n ? static_cast<int64_t>(g0) + k
+                                       : static_cast<int64_t>(N) + tint[b * kMaxTreeNodes + (k - n)];
+            return part + slot * g.n_sub;
+        };
+        auto store_soft = [&](int k, bool ok, float M, float S) {
+            if (lane != 0) return;
+            if (k < n) {
+                sm.ok[k] = ok;
+                if (ok) {
+                    const double Lt = lse2(M, S);
+                    sm.M[k] = M;
+                    sm.Lt[k] = Lt;
+                    sm.lth[k] = static_cast<float>(Lt);
+                    sm.ltl[k] = static_cast<float>(Lt - static_cast<double>(sm.lth[k]));
+                }
+            } else {
+                const int i = tint[b * kMaxTreeNodes + (k - n)] - g0;
+                sm.okd[i] = ok;
+                if (ok) {
+                    const double Ld = lse2(M, S);
+                    sm.Ld[i] = Ld;
+                    sm.ldh[i] = static_cast<float>(Ld);
+                    sm.ldl[i] = static_cast<float>(Ld - static_cast<double>(sm.ldh[i]));
+                }
+            }
+        };
+        if (greedy) {
+            for (int k = warp; k < n; k += kWalkWarps) {
+                const int am = warp_combine_arg(item_part(k), g.n_sub);
+                if (lane == 0) {
+                    sm.am[k] = am;
+                    sm.ok[k] = am >= 0;
+                }
+            }
+        } else {
+            for (int k0 = warp; k0 < items; k0 += 2 * kWalkWarps) {
+                const int k1 = k0 + kWalkWarps;
+                float2 ca[kPartCache], cb[kPartCache];
+                const float2 *pa = item_part(k0);
+                const float2 *pb = k1 < items ? item_part(k1) : pa;
+                load_parts(pa, g.n_sub, ca);
+                if (k1 < items) load_parts(pb, g.n_sub, cb);
+                float M, S;
+                bool ok = combine_soft(ca, pa, g.n_sub, &M, &S);
+                store_soft(k0, ok, M, S);
+                if (k1 < items) {
+                    ok = combine_soft(cb, pb, g.n_sub, &M, &S);
+                    store_soft(k1, ok, M, S);
+                }
+            }
+        }
+        __syncthreads();
+    }
+
     for (int step = 0; !err && step < n; ++step) {
         const int64_t urow = g0 + u;
         // children of u, in ascending node order (the same mask in every warp)
@@ -274,57 +464,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
         const unsigned long long kids = (static_cast<unsigned long long>(__ballot_sync(0xffffffffu, pa1 == u)) << 32) |
                                         __ballot_sync(0xffffffffu, pa0 == u);
         const bool leaf = kids == 0ull;
-        // statistics of u's rows; its children's logits at their tokens
-        if (warp == 0) {
-            const float2 *pr = part + urow * g.n_sub;
-            if (greedy) {
-                const int am = warp_combine_arg(pr, g.n_sub);
-                if (lane == 0) {
-                    sm.am = am;
-                    sm.ok = am >= 0;
-                }
-            } else {
-                float M, S;
-                const bool ok = warp_combine_soft(pr, g.n_sub, &M, &S);
-                if (lane == 0) {
-                    sm.ok = ok;
-                    if (ok) {
-                        const double Lt = lse2(M, S);
-                        sm.M = M;
-                        sm.Lt = Lt;
-                        sm.lth = static_cast<float>(Lt);
-                        sm.ltl = static_cast<float>(Lt - static_cast<double>(sm.lth));
-                    }
-                }
-            }
-        } else if (warp == 1) {
-            bool ok = true;
-            if (!greedy && !leaf) {
-                float M, S;
-                ok = warp_combine_soft(part + (static_cast<int64_t>(N) + urow) * g.n_sub, g.n_sub, &M, &S);
-                if (lane == 0 && ok) {
-                    const double Ld = lse2(M, S);
-                    sm.Ld = Ld;
-                    sm.ldh = static_cast<float>(Ld);
-                    sm.ldl = static_cast<float>(Ld - static_cast<double>(sm.ldh));
-                }
-            }
-            if (lane == 0) sm.okd = ok;
-        } else if (warp == 2 && !greedy) {
-            for (int i = lane; i < n; i += 32)
-                if ((kids >> i) & 1ull) {
-                    sm.zt[i] = E::load1(target, urow * V + sm.tok[i]);
-                    sm.zd[i] = E::load1(draft, urow * V + sm.tok[i]);
-                }
-        }
-        __syncthreads();
-        if (!sm.ok || !sm.okd) {
+        if (!sm.ok[u] || (!greedy && !leaf && !sm.okd[u])) {
             err = true;
             break;
         }
         if (greedy) {
             // the first child whose token is argmax p
-            const int am = sm.am;
+            const int am = sm.am[u];
             const int t0 = lane < n ? sm.tok[lane] : -1, t1 = lane + 32 < n ? sm.tok[lane + 32] : -1;
             const unsigned long long match =
                 kids & ((static_cast<unsigned long long>(__ballot_sync(0xffffffffu, t1 == am)) << 32) |
@@ -342,11 +488,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
         }
         if (leaf) {
             // bonus token from p_u, as the chain's bonus draw
-            if (warp == 0) {
+            if (warp == 0 && cr == 0) {
                 const float2 *pr = part + urow * g.n_sub;
                 float2 pc[kPartCache];
                 load_parts(pr, g.n_sub, pc);
-                const int tk = warp_draw_row<DT>(target, urow, pr, pc, g, c, sm.M, u_resample[urow]);
+                const int tk = warp_draw_row<DT>(target, urow, pr, pc, g, c, sm.M[u], u_resample[urow]);
                 if (lane == 0) sm.token = tk;
             }
             __syncthreads();
@@ -356,7 +502,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
         // the children in order
         const unsigned char *rt = static_cast<const unsigned char *>(target) + urow * rb;
         const unsigned char *rd = static_cast<const unsigned char *>(draft) + urow * rb;
-        const TreeWeight base{c, sm.lth, sm.ltl, sm.ldh, sm.ldl, 0.0f};
+        const TreeWeight base{c, sm.lth[u], sm.ltl[u], sm.ldh[u], sm.ldl[u], 0.0f};
         if (tid == 0) {
             sm.t = 0.0;  // p itself
             sm.S = 1.0f;
@@ -377,18 +523,18 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
                     } else {
                         const double cd = static_cast<double>(c);
                         const double lr =
-                            (static_cast<double>(zt) * cd - sm.Lt) - (static_cast<double>(zd) * cd - sm.Ld);
+                            (static_cast<double>(zt) * cd - sm.Lt[u]) - (static_cast<double>(zd) * cd - sm.Ld[u]);
                         alpha = lr >= 0.0 ? 1.0f : exp2f(static_cast<float>(lr));
                     }
                 } else {
                     // p_k(x) / q(x) = max(0, a - t b) / (S b) at the current level
                     float pa, pb;
-                    tree_pq(zt, zd, c, sm.lth, sm.ltl, sm.ldh, sm.ldl, &pa, &pb);
+                    tree_pq(zt, zd, c, sm.lth[u], sm.ltl[u], sm.ldh[u], sm.ldl[u], &pa, &pb);
                     const float num = fmaxf(__fmaf_rn(-static_cast<float>(sm.t), pb, pa), 0.0f);
                     alpha = (zd == -INFINITY || pb == 0.0f) ? (num > 0.0f ? 1.0f : 0.0f)
                                                             : fminf(1.0f, num / (sm.S * pb));
                 }
-                sm.next = u_accept[g0 + ch] < alpha ? ch : -1;
+                sm.next = sm.ua[ch] < alpha ? ch : -1;
             }
             __syncthreads();
             if (sm.next >= 0) {
@@ -397,18 +543,25 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
             }
             // rejected: the next level t' = t + S(t), and one pass over u's
             // rows for S(t') and its per-sub-chunk masses
-            if (j == 0 && warp == 0 && SPEC_RESID_PREFETCH) {
-                // both rows to L2 in 32 KB bulk prefetches: the later passes hit L2
+            if (j == 0 && warp == 0 && SPEC_RESID_PREFETCH && sc0 < sc1) {
+                // this CTA's half of both rows to L2 in 32 KB bulk prefetches
+                // (sub-chunk bounds are 16-byte aligned): the later passes hit L2
+                int e_lo, e_hi, unused;
+                sub_range(g, sc0, &e_lo, &unused);
+                sub_range(g, sc1 - 1, &unused, &e_hi);
+                const int64_t lo = static_cast<int64_t>(e_lo) * E::kBytes, hi = static_cast<int64_t>(e_hi) * E::kBytes;
                 constexpr int64_t kPiece = 32768;
                 const unsigned char *r0 = (lane & 1) ? rd : rt;
-                for (int64_t off = static_cast<int64_t>(lane >> 1) * kPiece; off < rb; off += 16 * kPiece)
-                    bulk_prefetch_l2(r0 + off, static_cast<uint32_t>(min(kPiece, rb - off)));
+                for (int64_t off = lo + static_cast<int64_t>(lane >> 1) * kPiece; off < hi; off += 16 * kPiece)
+                    bulk_prefetch_l2(r0 + off, static_cast<uint32_t>(min(kPiece, hi - off)));
             }
             const double tn = sm.t + static_cast<double>(sm.S);
             TreeWeight W = base;
             W.t = static_cast<float>(tn);
-            tree_pass<DT>(rt, rd, g, W, rm);
-            __syncthreads();
+            if (!pass(rt, rd, W)) {
+                err = true;
+                break;
+            }
             if (warp == 0) {
                 const float Sn = warp_total(rm, g.n_sub);
                 if (lane == 0) {
@@ -422,6 +575,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
             __syncthreads();
             zero_last = !sm.zpos;  // a mass that rounded to 0 leaves p as it was
         }
+        if (err) break;
         if (next >= 0) {
             if (tid == 0) sm.path[nacc] = sm.tok[next];
             ++nacc;
@@ -436,17 +590,17 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
         TreeWeight W = base;
         W.t = static_cast<float>(sm.t);
         const bool from_partials = zero_last && sm.t == 0.0;
-        if (zero_last && !from_partials) {
-            tree_pass<DT>(rt, rd, g, W, rm);
-            __syncthreads();
+        if (zero_last && !from_partials && !pass(rt, rd, W)) {
+            err = true;
+            break;
         }
-        if (warp == 0) {
+        if (warp == 0 && cr == 0) {
             int tk = -1;
             if (from_partials) {
                 const float2 *pr = part + urow * g.n_sub;
                 float2 pc[kPartCache];
                 load_parts(pr, g.n_sub, pc);
-                tk = warp_draw_row<DT>(target, urow, pr, pc, g, c, sm.M, u_resample[urow]);
+                tk = warp_draw_row<DT>(target, urow, pr, pc, g, c, sm.M[u], u_resample[urow]);
             } else {
                 float w[kPartCache];
 #pragma unroll
@@ -466,7 +620,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
         final_token = sm.token;
         break;
     }
-    // outputs: the accepted path, the drawn token, then -1
+    // outputs (CTA 0): the accepted path, the drawn token, then -1
+    if (cr != 0) return;
     for (int i = tid; i < n; i += blockDim.x) {
         int32_t o = -1;
         if (!err) o = i < nacc ? sm.path[i] : (i == nacc ? final_token : -1);
@@ -538,11 +693,12 @@ __global__ void __launch_bounds__(256) tree_draft_select_kernel(
 
 // ================================================================== host side
 struct TreeWsLayout {
-    size_t part, nint, tint, resid, total;
+    size_t part, nint, tint, resid, pair, total;
 };
 
 // Counters (the common 256-byte block) | partials of N target and N draft
-// rows | nint [B] | tint [B * kMaxTreeNodes] | residual masses [B * n_sub].
+// rows | nint [B] | tint [B * kMaxTreeNodes] | residual masses, two buffers
+// [B * 2 * n_sub] | the walk's meeting counters [B].
 TreeWsLayout tree_ws_layout(int B, int N, const Geometry &g) {
     TreeWsLayout l;
     size_t off = kCountersBytes;
@@ -553,7 +709,9 @@ TreeWsLayout tree_ws_layout(int B, int N, const Geometry &g) {
     l.tint = off;
     off = align_up(off + static_cast<size_t>(B) * kMaxTreeNodes * sizeof(int), 256);
     l.resid = off;
-    off = align_up(off + static_cast<size_t>(B) * g.n_sub * sizeof(float), 256);
+    off = align_up(off + static_cast<size_t>(B) * 2 * g.n_sub * sizeof(float), 256);
+    l.pair = off;
+    off = align_up(off + static_cast<size_t>(B) * sizeof(int), 256);
     l.total = off;
     return l;
 }
@@ -610,6 +768,7 @@ int launch_tree(const void *target, const void *draft, const int32_t *node_offse
     int *nint = reinterpret_cast<int *>(w + l.nint);
     int *tint = reinterpret_cast<int *>(w + l.tint);
     float *resid = reinterpret_cast<float *>(w + l.resid);
+    int *pair = reinterpret_cast<int *>(w + l.pair);
     int ns, per_sm;
     size_t smem;
     pick_ring(st, B, &ns, &smem, &per_sm);
@@ -617,7 +776,7 @@ int launch_tree(const void *target, const void *draft, const int32_t *node_offse
     // setup, then stats_kernel launched plainly: its prologue reads the
     // setup's tables before waiting on anything
     if (!cuda_ok(launch_k(false, tree_setup_kernel, dim3((B * 32 + 255) / 256), dim3(256), 0, stream, node_offsets,
-                          parent, B, N, nint, tint),
+                          parent, B, N, nint, tint, VERIFY ? pair : static_cast<int *>(nullptr)),
                  "launch tree_setup_kernel"))
         return SPEC_ERR_CUDA;
     const cudaError_t e =
@@ -629,10 +788,26 @@ int launch_tree(const void *target, const void *draft, const int32_t *node_offse
                           static_cast<int *>(nullptr), static_cast<const int *>(nint), static_cast<const int *>(tint), N);
     if (!cuda_ok(e, "launch stats_kernel (tree)")) return SPEC_ERR_CUDA;
     if (VERIFY) {
-        if (!cuda_ok(launch_k(true, tree_walk_kernel<DT>, dim3(B), dim3(kWalkThreads), 0, stream, target, draft,
-                              node_offsets, parent, tokens, u_accept, u_resample, temperature, B, N, g,
-                              static_cast<const float2 *>(part), static_cast<const int *>(nint), resid, counters,
-                              out_tokens, out_num, out_last),
+        // kTreeCtas CTAs per tree as one cluster (co-scheduled), launched
+        // with programmatic dependent launch after stats_kernel
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(B * kTreeCtas);
+        cfg.blockDim = dim3(kWalkThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = kTreeCtas;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = kTreeCtas > 1 ? 2 : 1;
+        if (!cuda_ok(cudaLaunchKernelEx(&cfg, tree_walk_kernel<DT>, target, draft, node_offsets, parent, tokens,
+                                        u_accept, u_resample, temperature, B, N, g, static_cast<const float2 *>(part),
+                                        static_cast<const int *>(nint), static_cast<const int *>(tint), resid, pair,
+                                        counters, out_tokens, out_num, out_last),
                      "launch tree_walk_kernel"))
             return SPEC_ERR_CUDA;
     } else {
