@@ -236,6 +236,31 @@ def measure(w, steps, warmup, torch, sv, dev, sampler=None, barrier=None, fused=
                 verify_ms_median=statistics.median(ver), mean_accepted=n_acc)
 
 
+def measure_round(w, steps, warmup, torch, sv, dev):
+    """Device time of spec_round (draft pass + verify pass in one call) on
+    the same batch, CUDA events on the launching stream; ms per call."""
+    d = to_device(w, torch, dev)
+    toks = torch.empty(w.rows_draft, dtype=torch.int32, device=dev)
+    out_t = torch.empty(w.rows_target, dtype=torch.int32, device=dev)
+    out_n = torch.empty(w.B, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        sv.spec_round(d["tl"], d["dl"], d["ud"], d["ua"], d["ur"], d["T"], d["ko"], out_draft_tokens=toks,
+                      out_tokens=out_t, out_num_accepted=out_n)
+    for _ in range(max(3, warmup)):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    del d
+    return e0.elapsed_time(e1) / steps
+
+
 class _Null:
     def __enter__(self):
         return self
@@ -541,6 +566,9 @@ def main():
 
     # the separate calls on the same batch: spec_verify streams the draft rows again
     sep = measure(w, max(50, args.steps // 4), args.warmup, torch, sv, dev, fused=False) if rank == 0 else None
+    # the same round as one call (spec_round: the verify's streaming pass
+    # starts beside the draft pass's epilogue)
+    rnd_ms = measure_round(w, max(50, args.steps // 4), args.warmup, torch, sv, dev) if rank == 0 else None
 
     extra = {}
     for c in [int(x) for x in args.extra_configs.split(",") if x.strip()] if rank == 0 else []:
@@ -605,7 +633,10 @@ def main():
                         "spec_verify_ms": sep["verify_ms"],
                         "spec_verify_gbs": gbs(ab["verify"], sep["verify_ms"]),
                         "spec_verify_frac_of_8tbs": gbs(ab["verify"], sep["verify_ms"]) / 8000.0,
-                        "spec_draft_sample_ms": sep["draft_ms"]}},
+                        "spec_draft_sample_ms": sep["draft_ms"]},
+                    "spec_round": None if rnd_ms is None else {
+                        "ms": rnd_ms, "rows_per_s": rows / (rnd_ms * 1e-3),
+                        "gbs": step_bytes / (rnd_ms * 1e-3) / 1e9}},
         "roofline": {"bound": "hbm", "kernel": "spec_verify_lse (all its launches: stats_kernel over the "
                                                "target rows + resolve_kernel)",
                      "achieved": verify_lse_gbs, "peak": peak, "unit": "GB/s",
