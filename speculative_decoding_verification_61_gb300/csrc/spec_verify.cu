@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
             if (s_kofs[mid] <= r) lo = mid; else hi = mid - 1;
         }
         const float c = temp_scale(temperature[lo]);
-        const float2 *pr = part + (static_cast<int64_t>(kMaxK + 1) * B + r) * g.n_sub;  // draft-mode slots
+        const float2 *pr = part + static_cast<int64_t>(r) * g.n_sub;
         int token = -1;
         double L = NAN;
         if (c == 0.0f) {

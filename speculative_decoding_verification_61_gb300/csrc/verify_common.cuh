@@ -152,10 +152,9 @@ constexpr int kMaxTreeNodes = SPEC_MAX_TREE_NODES;
 //                nodes, then the draft rows of its internal nodes if b is
 //                sampled; nothing for a bad temperature or parent array;
 //   tree-draft:  the draft rows of b's internal nodes.
-// Partials go to slot row r for target row r, R + r for draft row r (R =
-// R_t in verify mode and the node count N in tree mode), 33 B + r for draft
-// row r in draft mode (clear of every target slot), and r for draft row r
-// in tree-draft mode.
+// Partials go to slot row r (target row r, and draft rows in draft mode) or
+// R + r (draft row r otherwise), R = R_t in verify mode and the node count
+// N in tree mode; tree-draft mode uses slot r for draft row r.
 // Units are taken by tickets (unit_batch).  One lane of warp 8 is the
 // producer: it waits for a free ring slot and issues the bulk copy of the
 // next unit into it.  Warps 0..7 consume: warp w owns the w-th 2 KB
@@ -224,23 +223,15 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
     }
     if (tid == 0) s_rowpre[B] = total_rows;
     // everything above only read the inputs; from here on the workspace is
-    // written, so the previous kernel on the stream must have finished.
-    // Target mode writes nothing the draft epilogue before it reads (the
-    // draft partials sit in other slots), so it streams beside it and waits
-    // only at its end: it still completes after its predecessor, and so
-    // the kernel after it sees both.
-    constexpr bool kLateWait = MODE == kModeTarget;
-    if (!kLateWait) grid_dependency_wait();
+    // written, so the previous kernel on the stream must have finished
+    grid_dependency_wait();
     const bool any_bad = __syncthreads_or(bad);
     if (MODE == kModeVerify || MODE == kModeTarget)
         for (int i = blockIdx.x * kThreads + tid; i < B; i += gridDim.x * kThreads) seqcnt[i] = 0;
     // the next kernel may be scheduled as soon as SMs free up; it waits for
     // this grid's completion before it reads anything written here
     grid_launch_dependents();
-    if (any_bad) {
-        if (kLateWait) grid_dependency_wait();
-        return;
-    }
+    if (any_bad) return;
 
     if (tid == 0) {
         for (int s = 0; s < ns; ++s) {
@@ -302,12 +293,9 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
                             slot_row = s_kofs[B] + row;
                         }
                     } else if (DRAFT) {
-                        // above every target row's slot: a target pass may
-                        // write its partials while the draft epilogue still
-                        // reads these
                         row = s_kofs[b] + l;
                         base_ptr = draft;
-                        slot_row = static_cast<int64_t>(kMaxK + 1) * B + row;
+                        slot_row = row;
                     } else if (l <= k) {
                         row = static_cast<int64_t>(s_kofs[b]) + b + l;
                         base_ptr = target;
@@ -443,7 +431,6 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
     }
     // the last CTA out resets the ticket counters for the next launch on the
     // stream (the library zeroes them once when it allocates a workspace)
-    if (kLateWait) grid_dependency_wait();
     __syncthreads();
     if (tid == 0 && atomic_add_acq_rel_gpu(counters + kDone, 1) == static_cast<int>(gridDim.x) - 1) {
         counters[kTicket] = 0;
