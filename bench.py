@@ -1,14 +1,15 @@
 #!/usr/bin/env python
 """Benchmark of the speculative-decoding sampling round on one GB300.
 
-One step = spec_draft_sample_lse (draft-side softmax + multinomial over
-every draft row, keeping each row's normaliser) + spec_verify_lse (softmax
-of every target row, accept test, first rejection, residual or bonus draw,
-with the draft rows' normalisers from the first call) on the ragged
-adaptive-k batch (B = 512 sequences, k_b uniform in 1..10, V = 128256,
-bf16 logits, T = 1).  Inputs are resident in HBM and larger than L2 (no
-flush needed).  The standalone spec_verify (which streams the draft rows
-again) is timed on the same batch beside it.
+One step = spec_round: the draft-side softmax + multinomial over every
+draft row, keeping each row's normaliser (the pass of spec_draft_sample_lse),
+then the softmax of every target row, accept test, first rejection and
+residual or bonus draw with those normalisers (the pass of spec_verify_lse),
+in one call, on the ragged adaptive-k batch (B = 512 sequences, k_b uniform
+in 1..10, V = 128256, bf16 logits, T = 1).  Inputs are resident in HBM and
+larger than L2 (no flush needed).  The same round as two calls (each pass
+timed by itself) and the standalone spec_verify (which streams the draft
+rows again) are timed on the same batch beside it.
 
 metric: verified logit rows/s (R_t + R_d rows per step) and achieved HBM
 GB/s of algorithmic bytes (every logit row once, plus one row-equivalent
@@ -59,7 +60,7 @@ def parse():
     return ap.parse_args()
 
 
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "spec_verify_lse_traffic_B512_ragged_k1to10_V128256_bf16.txt")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "spec_round_traffic_B512_ragged_k1to10_V128256_bf16.txt")
 
 
 # the sources of the kernels a verify call launches
@@ -79,7 +80,7 @@ def kernel_source_hash() -> str:
 
 
 def measured_traffic(workload: str):
-    """DRAM bytes per spec_verify_lse call from the committed ncu summary, if
+    """DRAM bytes per spec_round call from the committed ncu summary, if
     it was taken on this workload with the current kernel sources; else None."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
@@ -178,11 +179,13 @@ def to_device(w, torch, dev):
                 ud=t(w.u_draft), T=t(w.temperature), ko=t(w.k_offsets))
 
 
-def measure(w, steps, warmup, torch, sv, dev, sampler=None, barrier=None, fused=True):
-    """Device-resident timing of draft sample + verify with CUDA events on
-    the launching stream.  fused: spec_draft_sample_lse + spec_verify_lse
-    (each row read once); else spec_draft_sample + spec_verify.  Returns
-    per-step, per-call times (ms)."""
+def measure(w, steps, warmup, torch, sv, dev, sampler=None, barrier=None, mode="fused"):
+    """Device-resident timing of one sampling round with CUDA events on the
+    launching stream.  mode "round": spec_round (both passes in one call);
+    "fused": spec_draft_sample_lse + spec_verify_lse (each row read once);
+    "separate": spec_draft_sample + spec_verify.  Returns per-step and
+    per-call times (ms; in round mode the draft slot is empty)."""
+    fused = mode == "fused"
     d = to_device(w, torch, dev)
     toks = torch.empty(w.rows_draft, dtype=torch.int32, device=dev)
     lse2 = torch.empty(max(w.rows_draft, 1), dtype=torch.float64, device=dev)
@@ -191,13 +194,18 @@ def measure(w, steps, warmup, torch, sv, dev, sampler=None, barrier=None, fused=
     stream = torch.cuda.current_stream()
 
     def draft():
+        if mode == "round":
+            return
         if fused:
             sv.spec_draft_sample_lse(d["dl"], d["T"], d["ud"], d["ko"], out_draft_tokens=toks, out_draft_lse2=lse2)
         else:
             sv.spec_draft_sample(d["dl"], d["T"], d["ud"], d["ko"], out_draft_tokens=toks)
 
     def verify():
-        if fused:
+        if mode == "round":
+            sv.spec_round(d["tl"], d["dl"], d["ud"], d["ua"], d["ur"], d["T"], d["ko"], out_draft_tokens=toks,
+                          out_tokens=out_t, out_num_accepted=out_n)
+        elif fused:
             sv.spec_verify_lse(d["tl"], d["dl"], lse2, toks, d["ua"], d["ur"], d["T"], d["ko"], out_tokens=out_t,
                                out_num_accepted=out_n)
         else:
@@ -234,31 +242,6 @@ def measure(w, steps, warmup, torch, sv, dev, sampler=None, barrier=None, fused=
     del d
     return dict(step_ms=total / steps, draft_ms=statistics.mean(draft), verify_ms=statistics.mean(ver),
                 verify_ms_median=statistics.median(ver), mean_accepted=n_acc)
-
-
-def measure_round(w, steps, warmup, torch, sv, dev):
-    """Device time of spec_round (draft pass + verify pass in one call) on
-    the same batch, CUDA events on the launching stream; ms per call."""
-    d = to_device(w, torch, dev)
-    toks = torch.empty(w.rows_draft, dtype=torch.int32, device=dev)
-    out_t = torch.empty(w.rows_target, dtype=torch.int32, device=dev)
-    out_n = torch.empty(w.B, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def call():
-        sv.spec_round(d["tl"], d["dl"], d["ud"], d["ua"], d["ur"], d["T"], d["ko"], out_draft_tokens=toks,
-                      out_tokens=out_t, out_num_accepted=out_n)
-    for _ in range(max(3, warmup)):
-        call()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        call()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    del d
-    return e0.elapsed_time(e1) / steps
 
 
 class _Null:
@@ -550,7 +533,7 @@ def main():
     w = workloads.make_config(args.config)
     ab = workloads.algorithmic_bytes(w)
     sampler = ClockSampler(local, enabled=(rank == 0 and not args.no_clocks))
-    m = measure(w, args.steps, args.warmup, torch, sv, dev, sampler=sampler, barrier=barrier, fused=True)
+    m = measure(w, args.steps, args.warmup, torch, sv, dev, sampler=sampler, barrier=barrier, mode="round")
     step_ms = m["step_ms"]
     if world > 1:
         import torch.distributed as dist
@@ -561,22 +544,21 @@ def main():
     value = world * rows / (step_ms * 1e-3)
     step_bytes = ab["verify_lse"] + ab["draft_sample"]
     gbs = lambda nbytes, ms: nbytes / (ms * 1e-3) / 1e9  # noqa: E731
-    verify_lse_gbs = gbs(ab["verify_lse"], m["verify_ms"])
-    draft_gbs = gbs(ab["draft_sample"], m["draft_ms"])
+    step_gbs = gbs(step_bytes, step_ms)
 
-    # the separate calls on the same batch: spec_verify streams the draft rows again
-    sep = measure(w, max(50, args.steps // 4), args.warmup, torch, sv, dev, fused=False) if rank == 0 else None
-    # the same round as one call (spec_round: the verify's streaming pass
-    # starts beside the draft pass's epilogue)
-    rnd_ms = measure_round(w, max(50, args.steps // 4), args.warmup, torch, sv, dev) if rank == 0 else None
+    # the same round as two calls (each pass timed by itself), and the
+    # separate calls (spec_verify streams the draft rows again)
+    reps = max(50, args.steps // 4)
+    two = measure(w, reps, args.warmup, torch, sv, dev, mode="fused") if rank == 0 else None
+    sep = measure(w, reps, args.warmup, torch, sv, dev, mode="separate") if rank == 0 else None
 
     extra = {}
     for c in [int(x) for x in args.extra_configs.split(",") if x.strip()] if rank == 0 else []:
         wc = workloads.make_config(c)
         abc = workloads.algorithmic_bytes(wc)
         reps = max(50, args.steps // 4)
-        mc = measure(wc, reps, args.warmup, torch, sv, dev, fused=False)
-        mf = measure(wc, reps, args.warmup, torch, sv, dev, fused=True)
+        mc = measure(wc, reps, args.warmup, torch, sv, dev, mode="separate")
+        mf = measure(wc, reps, args.warmup, torch, sv, dev, mode="fused")
         extra[wc.name] = {
             "verify_ms": round(mc["verify_ms"], 5), "draft_sample_ms": round(mc["draft_ms"], 5),
             "verify_rows_per_s": (wc.rows_target + wc.rows_draft) / (mc["verify_ms"] * 1e-3),
@@ -618,33 +600,37 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Zipf-like logits + Gaussian noise)",
         "config": {"workload": w.name, "B": w.B, "V": w.V, "k": "uniform 1..10 per sequence",
                    "temperature": 1.0, "rows_target": w.rows_target, "rows_draft": w.rows_draft,
-                   "step": "spec_draft_sample_lse + spec_verify_lse", "l2": "inputs > L2 (no flush)",
+                   "step": "spec_round (the draft pass of spec_draft_sample_lse and the verify pass of "
+                           "spec_verify_lse in one call)", "l2": "inputs > L2 (no flush)",
                    "parallelism": f"replicas x{world}"},
         "hbm_gbs": step_bytes / (step_ms * 1e-3) / 1e9,
         "frac_of_8tbs": step_bytes / (step_ms * 1e-3) / 8e12,
         "bytes_per_step": step_bytes,
-        "kernels": {"spec_verify_lse_ms": m["verify_ms"], "spec_verify_lse_gbs": verify_lse_gbs,
-                    "spec_verify_lse_frac_of_8tbs": verify_lse_gbs / 8000.0,
-                    "spec_draft_sample_lse_ms": m["draft_ms"], "spec_draft_sample_lse_gbs": draft_gbs,
-                    "mean_accepted": m["mean_accepted"],
+        "kernels": {"mean_accepted": m["mean_accepted"],
+                    "two_calls": None if two is None else {
+                        "step": "spec_draft_sample_lse + spec_verify_lse",
+                        "step_ms": two["step_ms"], "rows_per_s": rows / (two["step_ms"] * 1e-3),
+                        "spec_verify_lse_ms": two["verify_ms"],
+                        "spec_verify_lse_gbs": gbs(ab["verify_lse"], two["verify_ms"]),
+                        "spec_verify_lse_frac_of_peak": gbs(ab["verify_lse"], two["verify_ms"]) / peak,
+                        "spec_draft_sample_lse_ms": two["draft_ms"],
+                        "spec_draft_sample_lse_gbs": gbs(ab["draft_sample"], two["draft_ms"])},
                     "separate_calls": None if sep is None else {
                         "step_ms": sep["step_ms"],
                         "rows_per_s": rows / (sep["step_ms"] * 1e-3),
                         "spec_verify_ms": sep["verify_ms"],
                         "spec_verify_gbs": gbs(ab["verify"], sep["verify_ms"]),
                         "spec_verify_frac_of_8tbs": gbs(ab["verify"], sep["verify_ms"]) / 8000.0,
-                        "spec_draft_sample_ms": sep["draft_ms"]},
-                    "spec_round": None if rnd_ms is None else {
-                        "ms": rnd_ms, "rows_per_s": rows / (rnd_ms * 1e-3),
-                        "gbs": step_bytes / (rnd_ms * 1e-3) / 1e9}},
-        "roofline": {"bound": "hbm", "kernel": "spec_verify_lse (all its launches: stats_kernel over the "
-                                               "target rows + resolve_kernel)",
-                     "achieved": verify_lse_gbs, "peak": peak, "unit": "GB/s",
-                     "frac": verify_lse_gbs / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
-                     "traffic": measured_traffic(w.name), "algorithmic_bytes_per_launch": ab["verify_lse"],
-                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the call's kernels "
-                                       "(profiles/, null unless taken with the current kernel sources)"},
-        # per step: stats_kernel + draft_select_kernel, stats_kernel + resolve_kernel
+                        "spec_draft_sample_ms": sep["draft_ms"]}},
+        "roofline": {"bound": "hbm",
+                     "kernel": "spec_round, all four launches (stats_kernel over the draft rows, draft_select_kernel, "
+                               "stats_kernel over the target rows, resolve_kernel), timed as the step",
+                     "achieved": step_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": step_gbs / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": measured_traffic(w.name), "algorithmic_bytes_per_launch": step_bytes,
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the round's four "
+                                       "kernels (profiles/, null unless taken with the current kernel sources)"},
+        # per step (spec_round): stats_kernel + draft_select_kernel, stats_kernel + resolve_kernel
         "gpu_launches": 4 * args.steps,
         "cpu_baseline": cpu,
         "e2e": e2e_line,
