@@ -224,20 +224,28 @@ def measure(w, steps, warmup, torch, sv, dev, sampler=None, barrier=None, mode="
     ctx = sampler if sampler is not None else _Null()
     with ctx:
         t0.record(stream)
-        for i in range(steps):
-            e = ev[i]
-            e[0].record(stream)
-            draft()
-            e[1].record(stream)
-            verify()
-            e[2].record(stream)
+        if mode == "round":
+            # one call per step: only the bracketing events
+            for _ in range(steps):
+                verify()
+        else:
+            for i in range(steps):
+                e = ev[i]
+                e[0].record(stream)
+                draft()
+                e[1].record(stream)
+                verify()
+                e[2].record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
     if barrier:
         barrier()
     total = t0.elapsed_time(t1)
-    draft = [e[0].elapsed_time(e[1]) for e in ev]
-    ver = [e[1].elapsed_time(e[2]) for e in ev]
+    if mode == "round":
+        draft, ver = [0.0], [total / steps]
+    else:
+        draft = [e[0].elapsed_time(e[1]) for e in ev]
+        ver = [e[1].elapsed_time(e[2]) for e in ev]
     n_acc = out_n.float().mean().item()
     del d
     return dict(step_ms=total / steps, draft_ms=statistics.mean(draft), verify_ms=statistics.mean(ver),
