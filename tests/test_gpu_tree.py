@@ -78,6 +78,7 @@ CASES = [
     dict(B=4, shape=[2, 2, 2, 2, 2], V=1000, dtype="f32", temperature=1.0),     # 63 nodes
     dict(B=16, shape=[1, 1, 1, 1], V=20000, dtype="bf16", temperature=1.0),     # a chain
     dict(B=9, shape="random_6", V=8, dtype="f32", temperature=1.0),              # tiny vocabulary
+    dict(B=200, shape=[2, 2], V=4096, dtype="bf16", temperature=1.0, sigma_d=2.0),  # 400 CTAs: several waves of clusters
 ]
 
 
