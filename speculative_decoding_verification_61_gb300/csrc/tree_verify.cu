@@ -178,7 +178,7 @@ struct TreeWeight2 {
 // otherwise share its registers.)
 template <int DT>
 __device__ __noinline__ void tree_pass(const unsigned char *rt, const unsigned char *rd, const Geometry &g, const TreeWeight &W,
-                          float *rm, int sc_begin, int sc_end) {
+                          float *rm, int sc_begin, int sc_end, float2 *wpart) {
     using E = Elem<DT>;
     const int lane = lane_id();
     auto load = [&](int sc, uint4 (&xt)[4], uint4 (&xd)[4]) -> int {
@@ -228,7 +228,11 @@ __device__ __noinline__ void tree_pass(const unsigned char *rt, const unsigned c
     };
 #endif
     int sc = sc_begin + warp_id();
-    if (sc >= sc_end) return;
+    if (sc >= sc_end) {
+        if (lane == 0) wpart[warp_id()] = make_float2(0.0f, 0.0f);
+        return;
+    }
+    Acc2 wacc;  // this warp's masses in sub-chunk order (lane 0)
     uint4 ct[4], cd[4];
     int nc = load(sc, ct, cd);
     for (;;) {
@@ -237,7 +241,10 @@ __device__ __noinline__ void tree_pass(const unsigned char *rt, const unsigned c
         int nn = 0;
         if (sn < sc_end) nn = load(sn, nt, nd);
         const float sum = mass(ct, cd, nc);
-        if (lane == 0) rm[sc] = sum;
+        if (lane == 0) {
+            rm[sc] = sum;
+            wacc.add(sum);
+        }
         if (sn >= sc_end) break;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -247,8 +254,11 @@ __device__ __noinline__ void tree_pass(const unsigned char *rt, const unsigned c
         nc = nn;
         sc = sn;
     }
-    // this warp's masses visible to the other CTA of the tree before the meeting
-    if (kTreeCtas > 1 && lane == 0) __threadfence();
+    if (lane == 0) {
+        wpart[warp_id()] = make_float2(wacc.hi, wacc.lo);
+        // this warp's masses visible to the other CTA of the tree before the meeting
+        if (kTreeCtas > 1) __threadfence();
+    }
 }
 
 __device__ __forceinline__ unsigned cluster_ctarank() {
@@ -263,40 +273,45 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
     return v;
 }
 
-// Meeting point of a tree's CTAs after a pass (a no-op with one CTA): each
-// CTA adds one to the tree's counter once its masses are written and
-// fenced, then waits until the counter reaches `target` (every CTA of the
-// tree has added for this pass).  The wait is bounded: on a time-out the
-// status word gets SPEC_ERR_TIMEOUT and false is returned.  The counter is
-// in global memory, so no CTA ever touches the other's shared memory.
-__device__ bool tree_meet(int *cnt, int target, int *status, int *s_flag) {
-    __syncthreads();  // this CTA's masses are written (each writer fenced them)
-    if (kTreeCtas == 1) return true;
-    if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(cnt, 1);
-        const uint64_t t0 = global_timer_ns();
-        bool ok = true;
-        while (ld_acquire_gpu(cnt) < target) {
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-                ok = false;
-                set_status(status, SPEC_ERR_TIMEOUT);
-                break;
-            }
-            __nanosleep(64);
-        }
-        *s_flag = ok;
+// Meeting point of a tree's CTAs after a pass, run by thread 0 of each CTA
+// once the CTA's masses and warp partials are written: the CTA's partial
+// T_cr = its warps' partials added in order; with two CTAs it publishes T_cr
+// (ptot: this pass's two slots), adds one to the tree's counter and waits
+// (bounded) until the counter reaches `target`, then S = T_0 + T_1 added
+// in rank order, so both CTAs get the same bits.  On a time-out the status
+// word gets SPEC_ERR_TIMEOUT and false is returned.  Counter and partials
+// are in global memory: no CTA touches the other's shared memory.
+__device__ bool tree_meet_sum(int *cnt, int target, float2 *ptot, int cr, const float2 *wpart, int *status,
+                              float *S_out) {
+    Acc2 part;
+    for (int w = 0; w < kWalkWarps; ++w) {
+        part.add(wpart[w].x);
+        part.add(wpart[w].y);
     }
-    __syncthreads();
-    return *s_flag != 0;
-}
-
-// The total of the n masses rm[0 .. n) by one warp (fixed order: lane l
-// adds its masses l, l + 32, ... with compensation, then the two warp sums).
-__device__ __forceinline__ float warp_total(const float *rm, int n) {
-    Acc2 acc;
-    for (int i = lane_id(); i < n; i += 32) acc.add(__ldcg(rm + i));
-    return __fadd_rn(warp_sum_f(acc.hi), warp_sum_f(acc.lo));
+    if (kTreeCtas == 1) {
+        *S_out = part.value();
+        return true;
+    }
+    const float2 mine = make_float2(part.hi, part.lo);
+    ptot[cr] = mine;
+    __threadfence();
+    atomicAdd(cnt, 1);
+    const uint64_t t0 = global_timer_ns();
+    while (ld_acquire_gpu(cnt) < target) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            set_status(status, SPEC_ERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(64);
+    }
+    Acc2 tot;
+    for (int r = 0; r < kTreeCtas; ++r) {
+        const float2 v = r == cr ? mine : __ldcg(ptot + r);
+        tot.add(v.x);
+        tot.add(v.y);
+    }
+    *S_out = tot.value();
+    return true;
 }
 
 // Block per sequence.  Partials: target row g at slot g, draft row g at
@@ -310,11 +325,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
     const int *__restrict__ parent, const int32_t *__restrict__ tokens, const float *__restrict__ u_accept,
     const float *__restrict__ u_resample, const float *__restrict__ temperature, int B, int N, Geometry g,
     const float2 *__restrict__ part, const int *__restrict__ nint, const int *__restrict__ tint,
-    float *__restrict__ resid, int *__restrict__ pair, int *__restrict__ counters, int32_t *__restrict__ out_tokens,
+    float *__restrict__ resid, int *__restrict__ pair, float2 *__restrict__ ptot, int *__restrict__ counters,
+    int32_t *__restrict__ out_tokens,
     int32_t *__restrict__ out_num, int32_t *__restrict__ out_last) {
     using E = Elem<DT>;
     __shared__ TreeWalkSmem sm;
-    __shared__ int s_meet;
+    __shared__ int s_meet;                   // the last meeting succeeded (thread 0 writes)
+    __shared__ float2 s_wpart[kWalkWarps];   // the last pass's warp partials
     // CTA cr of the tree's cluster (0 with one CTA per tree); CTA 0 draws
     // and writes the outputs
     const int cr = kTreeCtas > 1 ? static_cast<int>(cluster_ctarank()) : 0;
@@ -373,11 +390,18 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
     const int half = (g.n_sub + kTreeCtas - 1) / kTreeCtas;
     const int sc0 = min(g.n_sub, cr * half), sc1 = min(g.n_sub, sc0 + half);
     int *const meet_cnt = pair + b;
-    auto pass = [&](const unsigned char *prt, const unsigned char *prd, const TreeWeight &W) -> bool {
+    float2 *const ptot_b = ptot + static_cast<int64_t>(b) * 2 * kTreeCtas;
+    // One pass over the node's rows at level W.t; afterwards thread 0 holds
+    // the pass's whole mass in *S0 and s_meet says whether the meeting of
+    // the tree's CTAs succeeded (published by the caller's next barrier).
+    auto pass = [&](const unsigned char *prt, const unsigned char *prd, const TreeWeight &W, float *S0) {
         rm = rm_base + (passes & 1) * g.n_sub;
-        tree_pass<DT>(prt, prd, g, W, rm, sc0, sc1);
+        tree_pass<DT>(prt, prd, g, W, rm, sc0, sc1, s_wpart);
         ++passes;
-        return tree_meet(meet_cnt, kTreeCtas * passes, counters + kStatus, &s_meet);
+        __syncthreads();  // this CTA's masses and warp partials are written
+        if (tid == 0)
+            s_meet = tree_meet_sum(meet_cnt, kTreeCtas * passes, ptot_b + (passes & 1) * kTreeCtas, cr, s_wpart,
+                                   counters + kStatus, S0);
     };
     const int64_t rb = static_cast<int64_t>(V) * E::kBytes;
 
@@ -503,40 +527,43 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
         const unsigned char *rt = static_cast<const unsigned char *>(target) + urow * rb;
         const unsigned char *rd = static_cast<const unsigned char *>(draft) + urow * rb;
         const TreeWeight base{c, sm.lth[u], sm.ltl[u], sm.ldh[u], sm.ldl[u], 0.0f};
+        // the accept test of child ch, the jj-th tried (thread 0): its index
+        // if accepted, else -1
+        auto test = [&](int ch, int jj) -> int {
+            const float zt = sm.zt[ch], zd = sm.zd[ch];
+            float alpha;
+            if (jj == 0) {
+                // the first candidate: the log-domain ratio of the chain verify
+                if (zt == -INFINITY) {
+                    alpha = 0.0f;
+                } else if (zd == -INFINITY) {
+                    alpha = 1.0f;
+                } else {
+                    const double cd = static_cast<double>(c);
+                    const double lr =
+                        (static_cast<double>(zt) * cd - sm.Lt[u]) - (static_cast<double>(zd) * cd - sm.Ld[u]);
+                    alpha = lr >= 0.0 ? 1.0f : exp2f(static_cast<float>(lr));
+                }
+            } else {
+                // p_k(x) / q(x) = max(0, a - t b) / (S b) at the current level
+                float pa, pb;
+                tree_pq(zt, zd, c, sm.lth[u], sm.ltl[u], sm.ldh[u], sm.ldl[u], &pa, &pb);
+                const float num = fmaxf(__fmaf_rn(-static_cast<float>(sm.t), pb, pa), 0.0f);
+                alpha = (zd == -INFINITY || pb == 0.0f) ? (num > 0.0f ? 1.0f : 0.0f)
+                                                        : fminf(1.0f, num / (sm.S * pb));
+            }
+            return sm.ua[ch] < alpha ? ch : -1;
+        };
+        unsigned long long rest = kids;  // the children not yet tried, lowest first
         if (tid == 0) {
             sm.t = 0.0;  // p itself
             sm.S = 1.0f;
+            sm.next = test(__ffsll(static_cast<long long>(rest)) - 1, 0);
         }
+        __syncthreads();
         int j = 0, next = -1;
         bool zero_last = false;
-        for (unsigned long long rest = kids; rest; rest &= rest - 1ull, ++j) {
-            const int ch = __ffsll(static_cast<long long>(rest)) - 1;
-            if (tid == 0) {
-                const float zt = sm.zt[ch], zd = sm.zd[ch];
-                float alpha;
-                if (j == 0) {
-                    // the first candidate: the log-domain ratio of the chain verify
-                    if (zt == -INFINITY) {
-                        alpha = 0.0f;
-                    } else if (zd == -INFINITY) {
-                        alpha = 1.0f;
-                    } else {
-                        const double cd = static_cast<double>(c);
-                        const double lr =
-                            (static_cast<double>(zt) * cd - sm.Lt[u]) - (static_cast<double>(zd) * cd - sm.Ld[u]);
-                        alpha = lr >= 0.0 ? 1.0f : exp2f(static_cast<float>(lr));
-                    }
-                } else {
-                    // p_k(x) / q(x) = max(0, a - t b) / (S b) at the current level
-                    float pa, pb;
-                    tree_pq(zt, zd, c, sm.lth[u], sm.ltl[u], sm.ldh[u], sm.ldl[u], &pa, &pb);
-                    const float num = fmaxf(__fmaf_rn(-static_cast<float>(sm.t), pb, pa), 0.0f);
-                    alpha = (zd == -INFINITY || pb == 0.0f) ? (num > 0.0f ? 1.0f : 0.0f)
-                                                            : fminf(1.0f, num / (sm.S * pb));
-                }
-                sm.next = sm.ua[ch] < alpha ? ch : -1;
-            }
-            __syncthreads();
+        for (;;) {
             if (sm.next >= 0) {
                 next = sm.next;
                 break;
@@ -558,22 +585,27 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
             const double tn = sm.t + static_cast<double>(sm.S);
             TreeWeight W = base;
             W.t = static_cast<float>(tn);
-            if (!pass(rt, rd, W)) {
+            float Sn = 0.0f;
+            pass(rt, rd, W, &Sn);
+            rest &= rest - 1ull;
+            ++j;
+            if (tid == 0 && s_meet) {
+                // the new level (a mass that rounded to 0 leaves p as it was),
+                // then the next child's test at it
+                sm.zpos = Sn > 0.0f;
+                if (Sn > 0.0f) {
+                    sm.t = tn;
+                    sm.S = Sn;
+                }
+                sm.next = rest ? test(__ffsll(static_cast<long long>(rest)) - 1, j) : -1;
+            }
+            __syncthreads();
+            if (!s_meet) {
                 err = true;
                 break;
             }
-            if (warp == 0) {
-                const float Sn = warp_total(rm, g.n_sub);
-                if (lane == 0) {
-                    sm.zpos = Sn > 0.0f;
-                    if (Sn > 0.0f) {
-                        sm.t = tn;
-                        sm.S = Sn;
-                    }
-                }
-            }
-            __syncthreads();
-            zero_last = !sm.zpos;  // a mass that rounded to 0 leaves p as it was
+            zero_last = !sm.zpos;
+            if (!rest) break;
         }
         if (err) break;
         if (next >= 0) {
@@ -590,9 +622,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
         TreeWeight W = base;
         W.t = static_cast<float>(sm.t);
         const bool from_partials = zero_last && sm.t == 0.0;
-        if (zero_last && !from_partials && !pass(rt, rd, W)) {
-            err = true;
-            break;
+        if (zero_last && !from_partials) {
+            float unused;
+            pass(rt, rd, W, &unused);
+            __syncthreads();
+            if (!s_meet) {
+                err = true;
+                break;
+            }
         }
         if (warp == 0 && cr == 0) {
             int tk = -1;
@@ -693,12 +730,13 @@ __global__ void __launch_bounds__(256) tree_draft_select_kernel(
 
 // ================================================================== host side
 struct TreeWsLayout {
-    size_t part, nint, tint, resid, pair, total;
+    size_t part, nint, tint, resid, pair, ptot, total;
 };
 
 // Counters (the common 256-byte block) | partials of N target and N draft
 // rows | nint [B] | tint [B * kMaxTreeNodes] | residual masses, two buffers
-// [B * 2 * n_sub] | the walk's meeting counters [B].
+// [B * 2 * n_sub] | the walk's meeting counters [B] | the CTAs' partial masses
+// of a pass [B * 2 * kTreeCtas] (fp32 hi/lo pairs).
 TreeWsLayout tree_ws_layout(int B, int N, const Geometry &g) {
     TreeWsLayout l;
     size_t off = kCountersBytes;
@@ -712,6 +750,8 @@ TreeWsLayout tree_ws_layout(int B, int N, const Geometry &g) {
     off = align_up(off + static_cast<size_t>(B) * 2 * g.n_sub * sizeof(float), 256);
     l.pair = off;
     off = align_up(off + static_cast<size_t>(B) * sizeof(int), 256);
+    l.ptot = off;
+    off = align_up(off + static_cast<size_t>(B) * 2 * kTreeCtas * sizeof(float2), 256);
     l.total = off;
     return l;
 }
@@ -769,6 +809,7 @@ int launch_tree(const void *target, const void *draft, const int32_t *node_offse
     int *tint = reinterpret_cast<int *>(w + l.tint);
     float *resid = reinterpret_cast<float *>(w + l.resid);
     int *pair = reinterpret_cast<int *>(w + l.pair);
+    float2 *ptot = reinterpret_cast<float2 *>(w + l.ptot);
     int ns, per_sm;
     size_t smem;
     pick_ring(st, B, &ns, &smem, &per_sm);
@@ -807,7 +848,7 @@ int launch_tree(const void *target, const void *draft, const int32_t *node_offse
         if (!cuda_ok(cudaLaunchKernelEx(&cfg, tree_walk_kernel<DT>, target, draft, node_offsets, parent, tokens,
                                         u_accept, u_resample, temperature, B, N, g, static_cast<const float2 *>(part),
                                         static_cast<const int *>(nint), static_cast<const int *>(tint), resid, pair,
-                                        counters, out_tokens, out_num, out_last),
+                                        ptot, counters, out_tokens, out_num, out_last),
                      "launch tree_walk_kernel"))
             return SPEC_ERR_CUDA;
     } else {
