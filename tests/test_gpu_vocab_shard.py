@@ -226,3 +226,41 @@ def test_verify_vocab_sharded_nccl_world_of_one(sv, tmp_path):
     ora = oracle.verify(w.target_logits, w.draft_logits, toks_np, w.u_accept, w.u_resample, w.temperature,
                         w.k_offsets)
     compare_verify(w, got.cpu().numpy(), num.cpu().numpy(), None, ora)
+
+
+def test_vocab_shard_statistical_marginal(sv):
+    """2^14 copies of one sequence (k = 1, V = 64, low acceptance so that most
+    tokens come from the residual) split over three uneven ranks: the first
+    emitted token follows p (chi-square), whichever rank drew it."""
+    from scipy.special import softmax
+    from scipy.stats import chisquare
+    calls, B, V = 4, 4096, 64
+    rng = np.random.default_rng(17)
+    t = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    dr = (t + rng.standard_normal(V) * 1.5).astype(np.float32)
+    bounds = [0, 24, 40, 64]
+    urng = np.random.Generator(np.random.Philox(33))
+    first = []
+    for _ in range(calls):
+        w = workloads.Workload(name="shared_seq", B=B, V=V, dtype="f32",
+                               k_offsets=np.arange(B + 1, dtype=np.int32), temperature=np.ones(B, np.float32),
+                               target_logits=np.tile(t, (2 * B, 1)), draft_logits=np.tile(dr, (B, 1)),
+                               u_accept=workloads.uniforms(urng, B), u_resample=workloads.uniforms(urng, 2 * B),
+                               u_draft=workloads.uniforms(urng, B))
+        d = to_device(w)
+        toks = sv.spec_draft_sample(d["draft_logits"], d["temperature"], d["u_draft"], d["k_offsets"])
+        got, num, per_rank = lockstep(w, d, toks, bounds)
+        check_one_owner(w, per_rank, num)
+        first.append(got.reshape(B, 2)[:, 0])
+    first = np.concatenate(first)
+    p0 = softmax(t.astype(np.float64))
+    counts = np.bincount(first, minlength=V)
+    e = p0 * len(first)
+    keep = e > 5
+    c2 = np.append(counts[keep], counts[~keep].sum()).astype(np.float64)
+    e2 = np.append(e[keep], e[~keep].sum())
+    _, pval = chisquare(c2, e2 * c2.sum() / e2.sum())
+    assert pval > 1e-4
+    # the draws really came from every rank
+    owners = {int(np.searchsorted(bounds, x, side="right")) - 1 for x in first}
+    assert owners == {0, 1, 2}
