@@ -300,7 +300,9 @@ int spec_verify_noalloc(const void *target_logits, const void *draft_logits,
  * SPEC_ERR_INVALID_ARG).  Host errors: SPEC_ERR_INVALID_ARG for null
  * pointers or N outside [B, B * SPEC_MAX_TREE_NODES], plus the errors of
  * spec_verify.  Uses the library-owned workspace (calls ordered on one
- * stream, as for spec_verify).
+ * stream, as for spec_verify).  Each tree is walked by a cluster of two
+ * CTAs (thread-block clusters); a device-side wait between them that runs
+ * out (2 s) marks the tree -1 and sets SPEC_ERR_TIMEOUT in the status word.
  */
 int spec_tree_verify(const void *target_logits, const void *draft_logits,
                      const int32_t *node_offsets, const int32_t *parent,
