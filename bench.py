@@ -452,45 +452,61 @@ def e2e(w, steps, torch, sv):
     return ms, h2d, d2h
 
 
-def cpu_baseline(w, seconds, nthreads):
+class OracleSample:
     """The oracle as it stands, on host cores, on the first n sequences of
-    the workload (n sized for about `seconds` of CPU time)."""
-    import oracle
-    import workloads
+    the workload: draft sample + verify of that sub-batch is one step."""
 
-    def sub(n):
+    def __init__(self, w, nthreads, n):
+        import workloads
+        self.w, self.nthreads = w, nthreads
+        self.n = n = int(min(w.B, max(1, n)))
         ko = w.k_offsets[:n + 1].copy()
         R_d, R_t = int(ko[-1]), int(ko[-1]) + n
-        return workloads.Workload(name=w.name, B=n, V=w.V, dtype=w.dtype, k_offsets=ko,
-                                  temperature=w.temperature[:n].copy(),
-                                  target_logits=w.target_logits[:R_t], draft_logits=w.draft_logits[:R_d],
-                                  u_accept=w.u_accept[:R_d], u_resample=w.u_resample[:R_t],
-                                  u_draft=w.u_draft[:R_d])
+        self.s = workloads.Workload(name=w.name, B=n, V=w.V, dtype=w.dtype, k_offsets=ko,
+                                    temperature=w.temperature[:n].copy(),
+                                    target_logits=w.target_logits[:R_t], draft_logits=w.draft_logits[:R_d],
+                                    u_accept=w.u_accept[:R_d], u_resample=w.u_resample[:R_t],
+                                    u_draft=w.u_draft[:R_d])
+        self.rows = self.s.rows_target + self.s.rows_draft
 
-    def run(s):
+    def step(self):
+        import oracle
+        s = self.s
         t = time.perf_counter()
-        ds = oracle.draft_sample(s.draft_logits, s.temperature, s.u_draft, s.k_offsets, nthreads=nthreads)
+        ds = oracle.draft_sample(s.draft_logits, s.temperature, s.u_draft, s.k_offsets, nthreads=self.nthreads)
         oracle.verify(s.target_logits, s.draft_logits, ds.tokens, s.u_accept, s.u_resample, s.temperature,
-                      s.k_offsets, nthreads=nthreads)
+                      s.k_offsets, nthreads=self.nthreads)
         return time.perf_counter() - t
 
-    n = min(w.B, max(nthreads, 4))
-    t = run(sub(n))
-    n = int(min(w.B, max(1, n * seconds / max(t, 1e-3))))
-    s = sub(n)
-    reps = 1
-    t = run(s)
+    @classmethod
+    def sized(cls, w, nthreads, seconds):
+        """A sample whose step takes about `seconds` (at least one sequence
+        per thread)."""
+        probe = cls(w, nthreads, max(nthreads, 4))
+        t = probe.step()
+        return cls(w, nthreads, max(probe.n, probe.n * seconds / max(t, 1e-3)))
+
+    def describe(self, reps, t):
+        return (f"first {self.n} of {self.w.B} sequences of {self.w.name} x{reps} ({self.rows * reps} rows), "
+                f"draft sample + verify, fp64 C oracle, OpenMP over sequences, {t:.1f} s")
+
+
+def cpu_baseline(w, seconds, nthreads):
+    """The oracle on a bounded sample of the workload, about `seconds` of CPU time."""
+    smp = OracleSample.sized(w, nthreads, seconds)
+    reps, t = 1, smp.step()
     while t * (reps + 1) / reps < seconds and reps < 64:
-        t += run(s)
+        t += smp.step()
         reps += 1
-    rows = (s.rows_target + s.rows_draft) * reps
-    return dict(value=rows / t, unit=UNIT, cores=nthreads, kind="oracle",
-                sample=f"first {n} of {w.B} sequences of {w.name} x{reps} ({rows} rows), draft sample + "
-                       f"verify, fp64 C oracle, OpenMP over sequences, {t:.1f} s")
+    return dict(value=smp.rows * reps / t, unit=UNIT, cores=nthreads, kind="oracle", sample=smp.describe(reps, t))
 
 
 # ------------------------------------------------------------------ main
 def run_reference(args):
+    """The reference arm: the fp64 oracle timed on the host cores, rank 0
+    only.  One step = draft sample + verify of a fixed sample of the
+    workload, sized once so that the W + K steps take about two minutes in
+    all (at least one sequence per thread)."""
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
@@ -498,11 +514,12 @@ def run_reference(args):
     import workloads
     w = workloads.make_config(args.config)
     nthreads = oracle.cores()
-    per_step = max(1.0, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
+    per_step = min(args.cpu_seconds if args.cpu_seconds > 0 else 15.0, 120.0 / max(1, args.steps + args.warmup))
+    smp = OracleSample.sized(w, nthreads, per_step)
     for _ in range(args.warmup):
-        cpu_baseline(w, per_step / 4, nthreads)
-    vals = [cpu_baseline(w, per_step, nthreads) for _ in range(args.steps)]
-    v = statistics.median(x["value"] for x in vals)
+        smp.step()
+    times = [smp.step() for _ in range(args.steps)]
+    v = smp.rows / statistics.median(times)
     rows_step = w.rows_target + w.rows_draft
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * rows_step / v,
@@ -510,7 +527,7 @@ def run_reference(args):
             "data": "synthetic (seeded Zipf-like logits)",
             "config": {"workload": w.name, "B": w.B, "V": w.V, "k": "uniform 1..10", "logits": w.dtype},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": nthreads, "kind": "oracle",
-                             "sample": vals[-1]["sample"]},
+                             "sample": smp.describe(args.steps, sum(times)) + " (median step)"},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
