@@ -469,6 +469,14 @@ const char *spec_status_string(int status);
 /* SPEC_VERIFY_ABI_VERSION of the loaded library. */
 int spec_abi_version(void);
 
+/* Frees the library-owned device buffers of every device (the workspaces of
+ * the entry points without a workspace argument, and the staging buffer of
+ * spec_round_host), after waiting for each such device.  Later calls
+ * allocate them again.  Must not run while another thread calls the
+ * library or during stream capture.  Returns SPEC_OK, or SPEC_ERR_CUDA if a
+ * device could not be synchronised (its buffers are then kept). */
+int spec_shutdown(void);
+
 /* Description of the last CUDA failure (the call and the CUDA error name)
  * seen by the calling thread, or "" if none.  Static per-thread storage. */
 const char *spec_last_error(void);

@@ -28,6 +28,7 @@ from ._binding import (  # noqa: F401
     noalloc_bytes,
     shard_workspace,
     shard_workspace_bytes,
+    shutdown,
     spec_draft_sample,
     spec_draft_sample_lse,
     spec_round,

@@ -22,7 +22,7 @@ EXPORTS = ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sam
            "spec_noalloc_bytes", "spec_adapt_state_bytes", "spec_adapt_init", "spec_adapt_update",
            "spec_draft_sample_lse", "spec_verify_lse", "spec_round", "spec_tree_verify",
            "spec_tree_draft_sample", "spec_shard_workspace_bytes", "spec_shard_stats",
-           "spec_shard_decide", "spec_shard_draw")
+           "spec_shard_decide", "spec_shard_draw", "spec_shutdown")
 
 
 class SpecError(RuntimeError):
@@ -79,6 +79,8 @@ def lib():
     L.spec_status_string.argtypes = [ip]
     L.spec_status_string.restype = ctypes.c_char_p
     L.spec_abi_version.argtypes = []
+    L.spec_shutdown.argtypes = []
+    L.spec_shutdown.restype = ip
     L.spec_verify_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, ip, vp, ip, ip, vp, vp, vp]
     L.spec_verify_noalloc.restype = ip
     L.spec_last_error.argtypes = []
@@ -505,6 +507,12 @@ def spec_shard_draw(target_shard, draft_shard, all_mass, u_resample, k_offsets, 
                                bounds, G, rank, dt, _p(out_tokens), wp, wb, _stream(stream))
     _raise(rc, "spec_shard_draw")
     return out_tokens
+
+
+def shutdown():
+    """Free the library-owned device buffers (they are allocated again on
+    the next call that needs them)."""
+    _raise(lib().spec_shutdown(), "spec_shutdown")
 
 
 def workspace_bytes(B: int, V: int, dtype: int) -> int:

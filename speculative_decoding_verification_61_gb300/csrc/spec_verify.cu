@@ -981,6 +981,29 @@ const char *spec_status_string(int status) {
 
 int spec_abi_version(void) { return SPEC_VERIFY_ABI_VERSION; }
 
+int spec_shutdown(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    int rc = SPEC_OK;
+    for (int d = 0; d < kMaxDevices; ++d) {
+        DeviceState &st = g_dev[d];
+        if (!st.ws && !st.stage) continue;
+        if (!cuda_ok(cudaSetDevice(d), "cudaSetDevice") || !cuda_ok(cudaDeviceSynchronize(), "cudaDeviceSynchronize")) {
+            rc = SPEC_ERR_CUDA;
+            continue;
+        }
+        if (st.ws) cudaFree(st.ws);
+        if (st.stage) cudaFree(st.stage);
+        st.ws = nullptr;
+        st.ws_bytes = 0;
+        st.stage = nullptr;
+        st.stage_bytes = 0;
+    }
+    if (prev >= 0) cudaSetDevice(prev);
+    return rc;
+}
+
 const char *spec_last_error(void) { return g_last_error; }
 
 }  // extern "C"

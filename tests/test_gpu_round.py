@@ -114,3 +114,29 @@ def test_bad_normaliser_marks_only_its_sequence(sv):
     for b in keep:
         assert (t1[b * 4:(b + 1) * 4] == t0[b * 4:(b + 1) * 4]).all()
 
+
+
+def test_shutdown_frees_and_calls_allocate_again():
+    """spec_shutdown frees the library-owned workspace and staging buffer;
+    the next calls allocate them again and give the same outputs."""
+    import speculative_decoding_verification_61_gb300 as sv
+    w = workloads.make_case(B=16, k="ragged_1_10", V=20000, dtype="bf16", temperature="odd_greedy", seed=61)
+    d = to_device(w)
+    args = (d["target_logits"], d["draft_logits"], d["u_draft"], d["u_accept"], d["u_resample"], d["temperature"],
+            d["k_offsets"])
+    a = [x.clone() for x in sv.spec_round(*args)]
+    h = lambda x: x.cpu().pin_memory()  # noqa: E731
+    ah = sv.spec_round_host(*(h(x) for x in args))
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    sv.shutdown()
+    assert torch.cuda.mem_get_info()[0] > free0  # the buffers went back to the device
+    b = sv.spec_round(*args)
+    bh = sv.spec_round_host(*(h(x) for x in args))
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    for x, y in zip(ah, bh):
+        assert torch.equal(x, y)
+    for x, y in zip(a, ah):
+        assert torch.equal(x.cpu(), y)
