@@ -26,6 +26,7 @@ from ._binding import (  # noqa: F401
     lib,
     lib_path,
     noalloc_bytes,
+    selfcheck_wait_timeout,
     shard_workspace,
     shard_workspace_bytes,
     shutdown,

@@ -22,7 +22,7 @@ EXPORTS = ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sam
            "spec_noalloc_bytes", "spec_adapt_state_bytes", "spec_adapt_init", "spec_adapt_update",
            "spec_draft_sample_lse", "spec_verify_lse", "spec_round", "spec_tree_verify",
            "spec_tree_draft_sample", "spec_shard_workspace_bytes", "spec_shard_stats",
-           "spec_shard_decide", "spec_shard_draw", "spec_shutdown")
+           "spec_shard_decide", "spec_shard_draw", "spec_shutdown", "spec_selfcheck_wait_timeout")
 
 
 class SpecError(RuntimeError):
@@ -81,6 +81,8 @@ def lib():
     L.spec_abi_version.argtypes = []
     L.spec_shutdown.argtypes = []
     L.spec_shutdown.restype = ip
+    L.spec_selfcheck_wait_timeout.argtypes = [vp, sz, vp]
+    L.spec_selfcheck_wait_timeout.restype = ip
     L.spec_verify_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, ip, vp, ip, ip, vp, vp, vp]
     L.spec_verify_noalloc.restype = ip
     L.spec_last_error.argtypes = []
@@ -507,6 +509,13 @@ def spec_shard_draw(target_shard, draft_shard, all_mass, u_resample, k_offsets, 
                                bounds, G, rank, dt, _p(out_tokens), wp, wb, _stream(stream))
     _raise(rc, "spec_shard_draw")
     return out_tokens
+
+
+def selfcheck_wait_timeout(workspace, stream=None):
+    """Run the device-side bounded waits until they give up (about 4 s);
+    afterwards workspace_status(workspace) is SPEC_ERR_TIMEOUT."""
+    wp, wb = _ws_args(workspace)
+    _raise(lib().spec_selfcheck_wait_timeout(wp, wb, _stream(stream)), "spec_selfcheck_wait_timeout")
 
 
 def shutdown():

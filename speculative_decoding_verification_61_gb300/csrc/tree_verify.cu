@@ -670,6 +670,29 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
     }
 }
 
+// ================================================================== self-check
+// The bounded device-side waits, made to run out on purpose: one thread
+// waits on an mbarrier that nothing arrives at (as a ring slot whose copy
+// never lands), then meets on a counter that no other CTA completes (as a
+// tree whose other CTA never arrives).  Each wait gives up after its limit
+// and the status word gets SPEC_ERR_TIMEOUT; the kernel then returns.
+__global__ void selfcheck_wait_kernel(int *counters, int *never) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    const bool mbar_ok = mbar_wait_bounded(&bar, 0);
+    if (!mbar_ok) set_status(counters + kStatus, SPEC_ERR_TIMEOUT);
+    float2 wpart[kWalkWarps] = {};
+    // the partials' slots are global memory, as in the walk: words 16..19
+    float2 *ptot = reinterpret_cast<float2 *>(counters + 16);
+    float S;
+    // a count the single arrival of this CTA never reaches
+    const bool meet_ok = tree_meet_sum(never, 2 * kTreeCtas, ptot, 0, wpart, counters + kStatus, &S);
+    counters[8] = (mbar_ok ? 0 : 1) | (meet_ok ? 0 : 2);  // which waits gave up
+    *never = 0;
+}
+
 // ================================================================== drafting
 // Warp per node (grid-stride): a non-root node's token from its parent's
 // draft row (partials at slot parent, stats_kernel tree-draft mode):
@@ -893,6 +916,17 @@ int spec_tree_verify(const void *target_logits, const void *draft_logits, const 
     return launch_tree<SPEC_BF16, true>(target_logits, draft_logits, node_offsets, parent, tokens, u_accept,
                                         u_resample, nullptr, temperature, B, N, g, out_tokens, out_num_accepted,
                                         out_last_node, *st, s);
+}
+
+int spec_selfcheck_wait_timeout(void *workspace, size_t workspace_bytes, void *stream) {
+    if (!workspace) return SPEC_ERR_INVALID_ARG;
+    if (workspace_bytes < kCountersBytes) return SPEC_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return SPEC_ERR_ALIGNMENT;
+    int *counters = static_cast<int *>(workspace);
+    // words 8 (result), 9 (the counter nothing completes) and 16..19 (the
+    // meeting's partial slots) of the counters block
+    selfcheck_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(counters, counters + 9);
+    return cuda_ok(cudaGetLastError(), "launch selfcheck_wait_kernel") ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 int spec_tree_draft_sample(const void *draft_logits, const int32_t *node_offsets, const int32_t *parent,

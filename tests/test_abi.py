@@ -33,7 +33,8 @@ def test_header_declares_expected_entry_points():
               "spec_round_host", "spec_workspace_bytes", "spec_workspace_status",
               "spec_status_string", "spec_abi_version", "spec_draft_sample_lse", "spec_verify_lse",
               "spec_round", "spec_tree_verify", "spec_tree_draft_sample", "spec_shard_workspace_bytes",
-              "spec_shard_stats", "spec_shard_decide", "spec_shard_draw"):
+              "spec_shard_stats", "spec_shard_decide", "spec_shard_draw", "spec_shutdown",
+              "spec_selfcheck_wait_timeout"):
         assert n in names
 
 
@@ -161,3 +162,10 @@ def test_shard_host_argument_errors(lib):
     # B = 0 is a no-op that still checks the shard arguments
     assert lib.spec_shard_draw(None, None, None, None, 0, None, ok, 2, 1, 1, None, None, 0, None) == 0
     assert lib.spec_shard_draw(None, None, None, None, 0, None, ok, 2, 2, 1, None, None, 0, None) == -1
+
+
+def test_selfcheck_host_argument_errors(lib):
+    vp = ctypes.c_void_p
+    assert lib.spec_selfcheck_wait_timeout(None, 256, None) == -1
+    assert lib.spec_selfcheck_wait_timeout(vp(1 << 20), 64, None) == -5
+    assert lib.spec_selfcheck_wait_timeout(vp((1 << 20) + 4), 256, None) == -2
