@@ -211,7 +211,13 @@ int spec_round(const void *target_logits, const void *draft_logits, const float 
  * returns after the stream has finished.  All pointers are host pointers
  * (pinned memory gives full copy bandwidth); k_offsets [B+1] is read on the
  * host to size the copies.  Uses a library-owned device staging area that
- * grows on demand (synchronous cudaMalloc).
+ * grows on demand (synchronous cudaMalloc).  The draft-side inputs are
+ * copied first on `stream`; the target logits follow on a library-owned
+ * second stream of the device (ordered after everything enqueued on
+ * `stream` before the call), so the draft pass runs while they are still
+ * crossing the host link.  The staging area and that stream are shared by
+ * all callers on a device: calls must not overlap (one host thread at a
+ * time per device).
  */
 int spec_round_host(const void *target_logits_host, const void *draft_logits_host,
                     const float *u_draft_host, const float *u_accept_host,

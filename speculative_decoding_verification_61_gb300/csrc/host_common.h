@@ -22,6 +22,8 @@ struct DeviceState {
     size_t ws_bytes = 0;
     void *stage = nullptr;
     size_t stage_bytes = 0;
+    cudaStream_t host_stream = nullptr;       // spec_round_host's second copy stream
+    cudaEvent_t host_ev[2] = {nullptr, nullptr};
 };
 
 constexpr int kMaxDevices = 64;

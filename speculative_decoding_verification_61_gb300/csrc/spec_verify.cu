@@ -781,9 +781,12 @@ int draft_call(const void *draft_logits, const float *temperature, const float *
 
 // One round on device buffers: the draft pass (tokens and the draft rows'
 // lse2, kept in the workspace), then the verify pass over the target rows.
+// before_verify (optional): an event the verify pass waits for (the host
+// entry's copy of the target logits); the draft pass does not wait for it.
 int round_call(const void *target_logits, const void *draft_logits, const float *u_draft, const float *u_accept,
                const float *u_resample, const float *temperature, int B, const int32_t *k_offsets, int V, int dtype,
-               int32_t *out_draft_tokens, int32_t *out_tokens, int32_t *out_num_accepted, void *stream) {
+               int32_t *out_draft_tokens, int32_t *out_tokens, int32_t *out_num_accepted, void *stream,
+               cudaEvent_t before_verify = nullptr) {
     int rc = check_common(B, V, dtype);
     if (rc != SPEC_OK) return rc;
     if (B == 0) return SPEC_OK;
@@ -802,20 +805,25 @@ int round_call(const void *target_logits, const void *draft_logits, const float 
     if (!ws) return rc;
     double *lse2 = reinterpret_cast<double *>(static_cast<unsigned char *>(ws) + l.lse2);
     const spec_verify_aux_t a{};
+    // the verify pass chains to the draft pass by programmatic dependent
+    // launch, unless it has to wait for an event first
+    const bool chained = before_verify == nullptr;
     if (dtype == SPEC_F32) {
         rc = launch_draft<SPEC_F32>(draft_logits, temperature, u_draft, B, k_offsets, g, out_draft_tokens, lse2, ws,
                                     l, *st, s);
         if (rc != SPEC_OK) return rc;
+        if (!chained && !cuda_ok(cudaStreamWaitEvent(s, before_verify, 0), "cudaStreamWaitEvent")) return SPEC_ERR_CUDA;
         return launch_verify<SPEC_F32>(target_logits, draft_logits, lse2, out_draft_tokens, u_accept, u_resample,
                                        temperature, B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st, s,
-                                       true);
+                                       chained);
     }
     rc = launch_draft<SPEC_BF16>(draft_logits, temperature, u_draft, B, k_offsets, g, out_draft_tokens, lse2, ws, l,
                                  *st, s);
     if (rc != SPEC_OK) return rc;
+    if (!chained && !cuda_ok(cudaStreamWaitEvent(s, before_verify, 0), "cudaStreamWaitEvent")) return SPEC_ERR_CUDA;
     return launch_verify<SPEC_BF16>(target_logits, draft_logits, lse2, out_draft_tokens, u_accept, u_resample,
                                     temperature, B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st, s,
-                                    true);
+                                    chained);
 }
 
 }  // namespace specv
@@ -924,19 +932,45 @@ int spec_round_host(const void *target_logits_host, const void *draft_logits_hos
     }
     unsigned char *d = static_cast<unsigned char *>(st->stage);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaMemcpyAsync(d + o_t, target_logits_host, R_t * V * es, cudaMemcpyHostToDevice, s);
-    if (R_d) cudaMemcpyAsync(d + o_d, draft_logits_host, R_d * V * es, cudaMemcpyHostToDevice, s);
+    // The draft pass needs only the draft logits: they go first, and the
+    // draft pass runs while the target logits cross the host link on a
+    // second stream (started after the draft copy, so that the two copies
+    // do not share the link); the verify pass waits for that copy.
+    cudaStream_t s2;
+    cudaEvent_t ev_draft, ev_target;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!st->host_stream) {
+            if (!cuda_ok(cudaStreamCreateWithFlags(&st->host_stream, cudaStreamNonBlocking), "cudaStreamCreate") ||
+                !cuda_ok(cudaEventCreateWithFlags(&st->host_ev[0], cudaEventDisableTiming), "cudaEventCreate") ||
+                !cuda_ok(cudaEventCreateWithFlags(&st->host_ev[1], cudaEventDisableTiming), "cudaEventCreate"))
+                return SPEC_ERR_CUDA;
+        }
+        s2 = st->host_stream;
+        ev_draft = st->host_ev[0];
+        ev_target = st->host_ev[1];
+    }
+    cudaMemcpyAsync(d + o_k, k_offsets_host, (B + 1) * 4, cudaMemcpyHostToDevice, s);
+    cudaMemcpyAsync(d + o_T, temperature_host, B * 4, cudaMemcpyHostToDevice, s);
     if (R_d) cudaMemcpyAsync(d + o_ud, u_draft_host, R_d * 4, cudaMemcpyHostToDevice, s);
+    if (R_d) cudaMemcpyAsync(d + o_d, draft_logits_host, R_d * V * es, cudaMemcpyHostToDevice, s);
     if (R_d) cudaMemcpyAsync(d + o_ua, u_accept_host, R_d * 4, cudaMemcpyHostToDevice, s);
     cudaMemcpyAsync(d + o_ur, u_resample_host, R_t * 4, cudaMemcpyHostToDevice, s);
-    cudaMemcpyAsync(d + o_T, temperature_host, B * 4, cudaMemcpyHostToDevice, s);
-    cudaMemcpyAsync(d + o_k, k_offsets_host, (B + 1) * 4, cudaMemcpyHostToDevice, s);
+    if (!cuda_ok(cudaEventRecord(ev_draft, s), "cudaEventRecord") ||
+        !cuda_ok(cudaStreamWaitEvent(s2, ev_draft, 0), "cudaStreamWaitEvent"))
+        return SPEC_ERR_CUDA;
+    cudaMemcpyAsync(d + o_t, target_logits_host, R_t * V * es, cudaMemcpyHostToDevice, s2);
+    if (!cuda_ok(cudaEventRecord(ev_target, s2), "cudaEventRecord")) return SPEC_ERR_CUDA;
     rc = round_call(d + o_t, d + o_d, reinterpret_cast<const float *>(d + o_ud),
                     reinterpret_cast<const float *>(d + o_ua), reinterpret_cast<const float *>(d + o_ur),
                     reinterpret_cast<const float *>(d + o_T), B, reinterpret_cast<const int32_t *>(d + o_k), V, dtype,
                     reinterpret_cast<int32_t *>(d + o_xd), reinterpret_cast<int32_t *>(d + o_ot),
-                    reinterpret_cast<int32_t *>(d + o_on), stream);
-    if (rc != SPEC_OK) return rc;
+                    reinterpret_cast<int32_t *>(d + o_on), stream, ev_target);
+    if (rc != SPEC_OK) {
+        cudaStreamWaitEvent(s, ev_target, 0);  // the staging buffer stays in use until the copy lands
+        cudaStreamSynchronize(s);
+        return rc;
+    }
     if (R_d) cudaMemcpyAsync(out_draft_tokens_host, d + o_xd, R_d * 4, cudaMemcpyDeviceToHost, s);
     cudaMemcpyAsync(out_tokens_host, d + o_ot, R_t * 4, cudaMemcpyDeviceToHost, s);
     cudaMemcpyAsync(out_num_accepted_host, d + o_on, B * 4, cudaMemcpyDeviceToHost, s);
