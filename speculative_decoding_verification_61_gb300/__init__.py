@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     MAX_SHARDS,
     MAX_TREE_NODES,
     MAX_V,
+    NOALLOC_SCRATCH_BYTES,
     SPEC_ERRORS,
     SpecError,
     exported_symbols,

@@ -11,6 +11,7 @@ F32, BF16 = 0, 1
 MAX_K, MAX_B, MAX_V = 32, 4096, 1 << 24
 MAX_TREE_NODES = 64
 MAX_SHARDS = 64
+NOALLOC_SCRATCH_BYTES = 48 << 20  # spec_verify_noalloc's fixed scratch array
 ABI_VERSION = 1
 SPEC_ERRORS = {0: "SPEC_OK", -1: "SPEC_ERR_INVALID_ARG", -2: "SPEC_ERR_ALIGNMENT",
                -3: "SPEC_ERR_CUDA", -4: "SPEC_ERR_TIMEOUT", -5: "SPEC_ERR_WORKSPACE"}
@@ -529,7 +530,7 @@ def workspace_bytes(B: int, V: int, dtype: int) -> int:
 
 
 def noalloc_bytes(B: int, V: int, dtype: int) -> int:
-    """Scratch a spec_verify_noalloc call uses (refused above MAX_NOALLOC_SCRATCH)."""
+    """Scratch a spec_verify_noalloc call uses (refused above NOALLOC_SCRATCH_BYTES)."""
     return int(lib().spec_noalloc_bytes(B, V, dtype))
 
 

@@ -27,6 +27,26 @@ def declared_functions():
     return sorted(set(re.findall(r"\b(spec_[a-z_]+)\s*\(", src)))
 
 
+def test_binding_constants_match_the_header():
+    """The binding's limits are the header's #defines (the library checks
+    arguments against the latter)."""
+    import speculative_decoding_verification_61_gb300 as sv
+    src = open(HEADER).read()
+
+    def define(name):
+        m = re.search(r"#define\s+" + name + r"\s+(.+?)\s*(/\*|$)", src, flags=re.M)
+        assert m, name
+        return int(eval(m.group(1).replace("(size_t)", ""), {}))  # integer arithmetic only
+
+    assert define("SPEC_MAX_K") == sv.MAX_K
+    assert define("SPEC_MAX_B") == sv.MAX_B
+    assert define("SPEC_MAX_V") == sv.MAX_V
+    assert define("SPEC_MAX_TREE_NODES") == sv.MAX_TREE_NODES
+    assert define("SPEC_MAX_SHARDS") == sv.MAX_SHARDS
+    assert define("SPEC_NOALLOC_SCRATCH_BYTES") == sv.NOALLOC_SCRATCH_BYTES
+    assert define("SPEC_VERIFY_ABI_VERSION") == sv.ABI_VERSION
+
+
 def test_header_declares_expected_entry_points():
     names = declared_functions()
     for n in ("spec_verify", "spec_verify_ex", "spec_draft_sample", "spec_draft_sample_ex",

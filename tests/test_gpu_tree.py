@@ -79,6 +79,8 @@ CASES = [
     dict(B=16, shape=[1, 1, 1, 1], V=20000, dtype="bf16", temperature=1.0),     # a chain
     dict(B=9, shape="random_6", V=8, dtype="f32", temperature=1.0),              # tiny vocabulary
     dict(B=200, shape=[2, 2], V=4096, dtype="bf16", temperature=1.0, sigma_d=2.0),  # 400 CTAs: several waves of clusters
+    dict(B=8, shape=[63], V=4096, dtype="f32", temperature=1.0, sigma_d=3.0),   # 64 nodes (the most): 63 candidates at the root
+    dict(B=4096, shape=[2], V=64, dtype="bf16", temperature="odd_greedy"),      # the most sequences per call
 ]
 
 

@@ -111,6 +111,7 @@ CASES = [
     (dict(B=40, k=6, V=3000, dtype="f32", temperature=1.0, sigma_d=0.05), "even2"),        # high acceptance
     (dict(B=7, k=5, V=4096, dtype="bf16", temperature=1.0), [0, 4096]),                    # one rank
     (dict(B=20, k="ragged_1_10", V=2048, dtype="bf16", temperature="odd_greedy"), "even16"),  # 16 ranks of 128 columns
+    (dict(B=10, k="ragged_1_10", V=4096, dtype="bf16", temperature="odd_greedy"), "even64"),  # the most ranks: 64 of 64 columns
 ]
 
 
