@@ -209,3 +209,38 @@ def test_statistical_marginal_on_gpu():
     assert pval > 1e-4
     Z0 = np.maximum(0, p0 - q0).sum()
     assert abs(acc0.mean() - (1 - Z0)) < 5 * np.sqrt(Z0 * (1 - Z0) / N)
+
+
+def test_owned_workspace_shared_across_shapes_and_the_tree_verify():
+    """The library-owned workspace serves calls of any B and V and the tree
+    verify too, laid out differently each time; the per-sequence counters
+    in its fixed header must still start every chain call at zero.  Each
+    call must equal the same call on a fresh zero-filled caller workspace,
+    bit for bit."""
+    import speculative_decoding_verification_61_gb300 as sv
+    cases = [dict(B=3, k=[2, 5, 1], V=60000, dtype="bf16", seed=61),
+             dict(B=300, k="ragged_1_10", V=1000, dtype="f32", seed=62, temperature="odd_greedy"),
+             dict(B=3, k=[2, 5, 1], V=60000, dtype="bf16", seed=63)]
+    tw = workloads.make_tree_case(B=40, shape=[3, 2], V=20000, dtype="bf16", seed=64)
+
+    def tdev(a):
+        x = torch.from_numpy(np.ascontiguousarray(a))
+        return (x.view(torch.bfloat16) if a.dtype == np.uint16 else x).cuda()
+
+    for i, c in enumerate(cases):
+        w = workloads.make_case(**c)
+        d = to_device(w)
+        toks = gpu_draft_sample(d)
+        args = (d["target_logits"], d["draft_logits"], toks, d["u_accept"], d["u_resample"], d["temperature"],
+                d["k_offsets"])
+        t0, n0 = sv.spec_verify(*args)
+        ws = torch.zeros(sv.workspace_bytes(w.B, w.V, sv.BF16 if w.dtype == "bf16" else sv.F32),
+                         dtype=torch.uint8, device="cuda")
+        t1, n1 = sv.spec_verify(*args, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(t0, t1) and torch.equal(n0, n1), i
+        # a tree verify between chain calls, on the same library-owned workspace
+        tok = np.where(tw.parent < 0, 0, 1).astype(np.int32)
+        sv.spec_tree_verify(tdev(tw.target_logits), tdev(tw.draft_logits), tdev(tw.node_offsets), tdev(tw.parent),
+                            tdev(tok), tdev(tw.u_accept), tdev(tw.u_resample), tdev(tw.temperature))
+    assert sv.workspace_status() == 0
