@@ -140,3 +140,15 @@ def test_shutdown_frees_and_calls_allocate_again():
         assert torch.equal(x, y)
     for x, y in zip(a, ah):
         assert torch.equal(x.cpu(), y)
+
+
+def test_graft_entry_smoke(sv):
+    """The one-call smoke check of the package entry (one small draft sample
+    and verify on cuda:0, compared with the oracle) runs clean."""
+    import importlib.util
+    import os
+    spec = importlib.util.spec_from_file_location(
+        "graft_entry", os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "__graft_entry__.py"))
+    entry = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(entry)
+    entry.smoke()
