@@ -625,14 +625,9 @@ int check_common(int B, int V, int dtype) {
 #define SPEC_RESOLVE_BLOCKS_PER_SM 8
 #endif
 // resolve_kernel blocks per sequence for n sequences on an idle GPU:
-// 1..SPEC_RESOLVE_MAX_SPLIT, as many as fit one wave of
-// SPEC_RESOLVE_BLOCKS_PER_SM per SM.  (More than 8 per sequence measured
-// slower at B = 64: every block repeats the sequence's decision.)
-#ifndef SPEC_RESOLVE_MAX_SPLIT
-#define SPEC_RESOLVE_MAX_SPLIT 8
-#endif
+// 1..kSub, as many as fit one wave of SPEC_RESOLVE_BLOCKS_PER_SM per SM.
 int resolve_split(const DeviceState &st, const Geometry &g, int n) {
-    return std::max(1, std::min({SPEC_RESOLVE_MAX_SPLIT, g.n_sub, (SPEC_RESOLVE_BLOCKS_PER_SM * st.sms) / std::max(n, 1)}));
+    return std::max(1, std::min({kSub, g.n_sub, (SPEC_RESOLVE_BLOCKS_PER_SM * st.sms) / std::max(n, 1)}));
 }
 
 // The verify pass: stats_kernel streams the target rows (and, without
