@@ -632,14 +632,18 @@ int resolve_split(const DeviceState &st, const Geometry &g, int n) {
 
 // The verify pass: stats_kernel streams the target rows (and, without
 // draft_lse2, the draft rows of sampled sequences), then resolve_kernel.
-// pdl_first: the call's first kernel may start early, which is safe only
-// when an earlier kernel of the same call precedes it on the stream.
+// The streaming kernel is launched early behind the stream's previous
+// kernel (programmatic dependent launch).  pdl_first: an earlier kernel of
+// the same call precedes it, so it may read the inputs before its wait;
+// otherwise it opens the call and waits first (the previous kernel may be
+// writing them).  after_event: the stream waits on an event just before
+// (another stream's copy), and the kernel is launched plainly.
 template <int DT>
 int launch_verify(const void *target, const void *draft, const double *draft_lse2, const int32_t *tokens,
                   const float *u_accept, const float *u_resample, const float *temperature, int B,
                   const int32_t *k_offsets, const Geometry &g, int32_t *out_tokens, int32_t *out_num,
                   const spec_verify_aux_t &aux, void *ws_base, const WsLayout &l, const DeviceState &st,
-                  cudaStream_t stream, bool pdl_first = false) {
+                  cudaStream_t stream, bool pdl_first = false, bool after_event = false) {
     int ns, per_sm;
     size_t smem;
     pick_ring(st, B, &ns, &smem, &per_sm);
@@ -648,12 +652,12 @@ int launch_verify(const void *target, const void *draft, const double *draft_lse
     const int grid = st.sms * per_sm;
     const int nsplit = resolve_split(st, g, B);
     const cudaError_t e1 =
-        draft_lse2 ? launch_k(pdl_first, stats_kernel<DT, kModeTarget>, dim3(grid), dim3(kThreads), smem, stream,
+        draft_lse2 ? launch_k(!after_event, stats_kernel<DT, kModeTarget>, dim3(grid), dim3(kThreads), smem, stream,
                               target, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, w.seqcnt,
-                              nullptr, nullptr, 0)
-                   : launch_k(pdl_first, stats_kernel<DT, kModeVerify>, dim3(grid), dim3(kThreads), smem, stream,
+                              nullptr, nullptr, 0, pdl_first ? 0 : 1)
+                   : launch_k(!after_event, stats_kernel<DT, kModeVerify>, dim3(grid), dim3(kThreads), smem, stream,
                               target, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, w.seqcnt,
-                              nullptr, nullptr, 0);
+                              nullptr, nullptr, 0, pdl_first ? 0 : 1);
     if (!cuda_ok(e1, "launch stats_kernel") ||
         !cuda_ok(launch_k(true, resolve_kernel<DT>, dim3(B * nsplit), dim3(SPEC_RESOLVE_THREADS), 0, stream, target, draft, tokens,
                           u_accept, u_resample, temperature, k_offsets, draft_lse2, B, g, nsplit, w, out_tokens,
@@ -678,9 +682,11 @@ int launch_draft(const void *draft, const float *temperature, const float *u_dra
     // one warp per draft row (grid-stride): at most B * kMaxK rows, 8 warps per block
     const int grid = static_cast<int>(
         std::min(static_cast<int64_t>(st.sms) * SPEC_SELECT_BLOCKS_PER_SM, (static_cast<int64_t>(B) * kMaxK + 7) / 8));
-    if (!cuda_ok(launch_k(false, stats_kernel<DT, kModeDraft>, dim3(st.sms * per_sm), dim3(kThreads), smem, stream,
+    // the call's first kernel: launched early behind the stream's previous
+    // kernel, it waits for it before reading the inputs (wait_first)
+    if (!cuda_ok(launch_k(true, stats_kernel<DT, kModeDraft>, dim3(st.sms * per_sm), dim3(kThreads), smem, stream,
                           draft, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, nullptr, nullptr,
-                          nullptr, 0),
+                          nullptr, 0, 1),
                  "launch stats_kernel") ||
         !cuda_ok(launch_k(true, draft_select_kernel<DT>, dim3(std::max(grid, 1)), dim3(256),
                           (B + 1) * sizeof(int), stream, draft, temperature, u_draft, k_offsets, B, g,
@@ -815,7 +821,7 @@ int round_call(const void *target_logits, const void *draft_logits, const float 
         if (!chained && !cuda_ok(cudaStreamWaitEvent(s, before_verify, 0), "cudaStreamWaitEvent")) return SPEC_ERR_CUDA;
         return launch_verify<SPEC_F32>(target_logits, draft_logits, lse2, out_draft_tokens, u_accept, u_resample,
                                        temperature, B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st, s,
-                                       chained);
+                                       chained, !chained);
     }
     rc = launch_draft<SPEC_BF16>(draft_logits, temperature, u_draft, B, k_offsets, g, out_draft_tokens, lse2, ws, l,
                                  *st, s);
@@ -823,7 +829,7 @@ int round_call(const void *target_logits, const void *draft_logits, const float 
     if (!chained && !cuda_ok(cudaStreamWaitEvent(s, before_verify, 0), "cudaStreamWaitEvent")) return SPEC_ERR_CUDA;
     return launch_verify<SPEC_BF16>(target_logits, draft_logits, lse2, out_draft_tokens, u_accept, u_resample,
                                     temperature, B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st, s,
-                                    chained);
+                                    chained, !chained);
 }
 
 }  // namespace specv

@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
     const void *__restrict__ target, const void *__restrict__ draft,
     const float *__restrict__ temperature, const int *__restrict__ k_offsets, int B, Geometry g, int ns,
     float2 *__restrict__ part, int *__restrict__ counters, int *__restrict__ seqcnt,
-    const int *__restrict__ tree_nint, const int *__restrict__ tree_int, int tree_nodes) {
+    const int *__restrict__ tree_nint, const int *__restrict__ tree_int, int tree_nodes, int wait_first) {
     using E = Elem<DT>;
     constexpr bool DRAFT = MODE == kModeDraft;
     constexpr bool TREE = MODE == kModeTree || MODE == kModeTreeDraft;
@@ -183,6 +183,10 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
     int *s_tmp = reinterpret_cast<int *>(s_c + B);  // [kThreads/32 + 1]
 
     const int tid = threadIdx.x;
+    // wait_first: the kernel opens its call and was launched early behind
+    // whatever kernel precedes it on the stream, which may still be writing
+    // the inputs: wait for it before reading them
+    if (wait_first) grid_dependency_wait();
     for (int i = tid; i <= B; i += kThreads) {
         s_kofs[i] = k_offsets[i];
         if (i < B) s_c[i] = temp_scale(temperature[i]);
