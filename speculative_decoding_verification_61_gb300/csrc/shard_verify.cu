@@ -723,10 +723,12 @@ int launch_shard_stats(const void *target, const void *draft, const int32_t *tok
     size_t smem;
     pick_ring(st, B, &ns, &smem, &per_sm);
     if (ns == 0) return SPEC_ERR_INVALID_ARG;
-    if (!cuda_ok(launch_k(false, stats_kernel<DT, kModeShard>, dim3(st.sms * per_sm), dim3(kThreads), smem, stream,
+    // the call's first kernel: launched early behind the stream's previous
+    // kernel, it waits for it before reading the inputs (wait_first)
+    if (!cuda_ok(launch_k(true, stats_kernel<DT, kModeShard>, dim3(st.sms * per_sm), dim3(kThreads), smem, stream,
                           target, draft, temperature, k_offsets, B, g, ns, w.part, w.counters,
                           static_cast<int *>(nullptr), static_cast<const int *>(nullptr),
-                          static_cast<const int *>(nullptr), 0, 0),
+                          static_cast<const int *>(nullptr), 0, 1),
                  "launch stats_kernel (shard)") ||
         !cuda_ok(launch_k(true, shard_row_kernel<DT>, dim3(B), dim3(256), 0, stream, target,
                           draft, tokens, temperature, k_offsets, B, g, sp.v0, static_cast<const float2 *>(w.part),

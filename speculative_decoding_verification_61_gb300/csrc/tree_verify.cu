@@ -57,6 +57,9 @@ __global__ void __launch_bounds__(256) tree_setup_kernel(const int *__restrict__
                                                          const int *__restrict__ parent, int B, int N,
                                                          int *__restrict__ nint, int *__restrict__ tint,
                                                          int *__restrict__ pair) {
+    // the call's first kernel, launched early behind the stream's previous
+    // kernel: wait for it before reading the inputs or writing the workspace
+    grid_dependency_wait();
     const int b = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = lane_id();
     if (b >= B) return;
@@ -837,9 +840,9 @@ int launch_tree(const void *target, const void *draft, const int32_t *node_offse
     size_t smem;
     pick_ring(st, B, &ns, &smem, &per_sm);
     if (ns == 0) return SPEC_ERR_INVALID_ARG;
-    // setup, then stats_kernel launched plainly: its prologue reads the
-    // setup's tables before waiting on anything
-    if (!cuda_ok(launch_k(false, tree_setup_kernel, dim3((B * 32 + 255) / 256), dim3(256), 0, stream, node_offsets,
+    // setup (launched early; it waits first), then stats_kernel launched
+    // plainly: its prologue reads the setup's tables before waiting on anything
+    if (!cuda_ok(launch_k(true, tree_setup_kernel, dim3((B * 32 + 255) / 256), dim3(256), 0, stream, node_offsets,
                           parent, B, N, nint, tint, VERIFY ? pair : static_cast<int *>(nullptr)),
                  "launch tree_setup_kernel"))
         return SPEC_ERR_CUDA;
