@@ -489,8 +489,8 @@ int spec_abi_version(void);
 
 /* Frees the library-owned device buffers of every device (the workspaces of
  * the entry points without a workspace argument, and the staging buffer of
- * spec_round_host), after waiting for each such device.  Later calls
- * allocate them again.  Must not run while another thread calls the
+ * spec_round_host) and spec_round_host's copy stream and events, after
+ * waiting for each such device.  Later calls create them again.  Must not run while another thread calls the
  * library or during stream capture.  Returns SPEC_OK, or SPEC_ERR_CUDA if a
  * device could not be synchronised (its buffers are then kept). */
 int spec_shutdown(void);

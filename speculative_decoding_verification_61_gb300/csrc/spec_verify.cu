@@ -946,12 +946,18 @@ int spec_round_host(const void *target_logits_host, const void *draft_logits_hos
     cudaEvent_t ev_draft, ev_target;
     {
         std::lock_guard<std::mutex> lock(g_mu);
-        if (!st->host_stream) {
-            if (!cuda_ok(cudaStreamCreateWithFlags(&st->host_stream, cudaStreamNonBlocking), "cudaStreamCreate") ||
-                !cuda_ok(cudaEventCreateWithFlags(&st->host_ev[0], cudaEventDisableTiming), "cudaEventCreate") ||
-                !cuda_ok(cudaEventCreateWithFlags(&st->host_ev[1], cudaEventDisableTiming), "cudaEventCreate"))
-                return SPEC_ERR_CUDA;
+        // created on first use; each handle on its own, so that one that
+        // failed is tried again by the next call
+        if (!st->host_stream &&
+            !cuda_ok(cudaStreamCreateWithFlags(&st->host_stream, cudaStreamNonBlocking), "cudaStreamCreate")) {
+            st->host_stream = nullptr;
+            return SPEC_ERR_CUDA;
         }
+        for (cudaEvent_t &e : st->host_ev)
+            if (!e && !cuda_ok(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "cudaEventCreate")) {
+                e = nullptr;
+                return SPEC_ERR_CUDA;
+            }
         s2 = st->host_stream;
         ev_draft = st->host_ev[0];
         ev_target = st->host_ev[1];
@@ -1028,7 +1034,7 @@ int spec_shutdown(void) {
     int rc = SPEC_OK;
     for (int d = 0; d < kMaxDevices; ++d) {
         DeviceState &st = g_dev[d];
-        if (!st.ws && !st.stage) continue;
+        if (!st.ws && !st.stage && !st.host_stream) continue;
         if (!cuda_ok(cudaSetDevice(d), "cudaSetDevice") || !cuda_ok(cudaDeviceSynchronize(), "cudaDeviceSynchronize")) {
             rc = SPEC_ERR_CUDA;
             continue;
@@ -1039,6 +1045,12 @@ int spec_shutdown(void) {
         st.ws_bytes = 0;
         st.stage = nullptr;
         st.stage_bytes = 0;
+        for (cudaEvent_t &e : st.host_ev) {
+            if (e) cudaEventDestroy(e);
+            e = nullptr;
+        }
+        if (st.host_stream) cudaStreamDestroy(st.host_stream);
+        st.host_stream = nullptr;
     }
     if (prev >= 0) cudaSetDevice(prev);
     return rc;
