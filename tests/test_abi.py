@@ -124,6 +124,26 @@ def test_fused_round_host_argument_errors(lib):
     assert lib.spec_round(None, None, None, None, None, None, 0, None, 1000, 0, None, None, None, None) == 0
 
 
+def test_round_host_argument_errors(lib):
+    """spec_round_host reads k_offsets on the host to size its copies: a bad
+    array, a null pointer or a bad dtype is refused before any CUDA call."""
+    import numpy as np
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)  # never dereferenced: validation fails first
+
+    def call(ko, B=3, V=1000, dtype=0, first=fake):
+        k = np.ascontiguousarray(ko, dtype=np.int32)
+        return lib.spec_round_host(first, fake, fake, fake, fake, fake, B, k.ctypes.data_as(vp), V, dtype,
+                                   fake, fake, fake, None)
+    assert call([1, 2, 3, 4]) == -1        # k_offsets[0] != 0
+    assert call([0, 2, 1, 4]) == -1        # a negative k_b
+    assert call([0, 2, 40, 41]) == -1      # k_b = 38 > MAX_K
+    assert call([0, 1, 2, 3], first=None) == -1
+    assert call([0, 1, 2, 3], dtype=7) == -1
+    assert call([0, 1, 2, 3], V=1001, dtype=1) == -2
+    assert lib.spec_round_host(None, None, None, None, None, None, 0, None, 1000, 0, None, None, None, None) == 0
+
+
 def test_tree_host_argument_errors(lib):
     vp = ctypes.c_void_p
     fake = vp(1 << 20)  # never dereferenced: validation fails first
