@@ -60,6 +60,11 @@
  *     [0, SPEC_MAX_K]) fails the whole call on the device: every
  *     out_num_accepted = -1, out_tokens untouched, and the workspace status
  *     word set to SPEC_ERR_INVALID_ARG.
+ *   - Time-outs: every device-side wait is bounded (2 s).  A wait that runs
+ *     out records SPEC_ERR_TIMEOUT in the workspace status word, and while
+ *     that word holds it every verify or draft-sampling call on the
+ *     workspace reports all its sequences (rows) as data errors (-1) rather
+ *     than outputs that look valid; clear it with spec_workspace_status.
  *   - Temperature: every row of sequence b, target and draft, is divided by
  *     T_b before the softmax.
  *   - Randomness is never drawn inside the library: all uniforms are inputs,
@@ -227,32 +232,35 @@ int spec_round_host(const void *target_logits_host, const void *draft_logits_hos
                     int32_t *out_num_accepted_host, void *stream);
 
 /*
- * Allocation-free spec_verify (no counterpart on the pages: a deployment
- * convenience of this library).
+ * Allocation-free spec_verify.  The pages have no counterpart: it is a
+ * deployment convenience of this library.
  *
- * For callers that cannot allocate device memory when they verify: code
- * running under CUDA stream capture, serving loops that forbid allocation on
- * the hot path to keep latency predictable, and runtimes whose memory pool
- * owns all device memory.  Arguments, layout, outputs and data-error
- * behaviour are those of spec_verify; the caller still provides every input
- * and output buffer.  The scratch memory the kernels need comes from a
- * fixed array inside the library (SPEC_NOALLOC_SCRATCH_BYTES, held on every
- * GPU that loads the library until the process exits), so the call performs
- * no cudaMalloc, cudaFree or other allocation.
+ * For callers that cannot allocate device memory at the moment they
+ * verify: a serving loop that keeps cudaMalloc off its hot path so that
+ * latency stays predictable, or a runtime whose own memory pool owns all
+ * device memory and hands out none.  Arguments, layout, outputs and
+ * data-error behaviour are those of spec_verify; the caller still provides
+ * every input and output buffer.  The scratch memory the kernels need is a
+ * fixed array compiled into the library (SPEC_NOALLOC_SCRATCH_BYTES = 48
+ * MiB), so the call performs no cudaMalloc, cudaFree or other allocation.
+ *   - The array is held on a device from this entry point's first call
+ *     there until the process exits (with the CUDA runtime's default lazy
+ *     module loading; with CUDA_MODULE_LOADING=EAGER every device that
+ *     loads the library holds it).
  *   - A call whose scratch need, spec_noalloc_bytes(B, V, dtype), exceeds
  *     SPEC_NOALLOC_SCRATCH_BYTES is rejected with SPEC_ERR_WORKSPACE before
  *     anything is launched (spec_last_error() names the sizes).  The limit
  *     covers, e.g., B = 512 at V = 152064 in bf16.
- *   - The first call on each device looks up the array's device address
- *     (once per device, with that device current); make that first call
- *     before any stream capture.
+ *   - The first call on each device does a one-time set-up: it looks up the
+ *     array's device address (with that device current).  Make that first
+ *     call before any stream capture.
  *   - All calls share the one array: calls that may overlap on the GPU (on
  *     different streams without ordering) race and give wrong results.
  *     Order them on one stream.
- *   - The array keeps the previous call's contents; the call clears the
- *     parts that must start at zero.  Device-side status (time-outs) is not
- *     reported by this entry point; data errors still mark sequences with
- *     out_num_accepted = -1.
+ *   - The array keeps the previous call's contents; each call first clears
+ *     (cudaMemsetAsync) the words that must start at zero, the status word
+ *     among them, so a time-out shows in that call's outputs only (every
+ *     sequence -1; see Time-outs above).
  */
 #define SPEC_NOALLOC_SCRATCH_BYTES ((size_t)48 << 20)
 int spec_verify_noalloc(const void *target_logits, const void *draft_logits,
@@ -465,7 +473,8 @@ size_t spec_noalloc_bytes(int B, int V, int dtype);
  * Device status word of a workspace (NULL: the library-owned one of the
  * current device): SPEC_OK or the first device-side error (SPEC_ERR_TIMEOUT,
  * SPEC_ERR_INVALID_ARG) since it was last cleared.  Synchronous (it waits
- * for the device).  clear != 0 resets it to SPEC_OK.
+ * for the device).  clear != 0 resets it to SPEC_OK (needed after a
+ * time-out: until then, calls on the workspace report every sequence -1).
  */
 int spec_workspace_status(const void *workspace, int *status_out, int clear);
 

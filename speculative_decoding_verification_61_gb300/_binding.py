@@ -546,23 +546,37 @@ def workspace_status(workspace=None, clear: bool = False) -> int:
 def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, u_accept, u_resample,
                         temperature, k_offsets, out_tokens=None, out_num_accepted=None,
                         stream=None):
-    """spec_verify without any device allocation inside the call: for callers
-    that cannot allocate while verifying (stream capture, allocation-free
-    serving loops, externally managed memory pools).  Scratch comes from a
-    fixed array in the library (48 MiB); larger batches raise SpecError
-    (SPEC_ERR_WORKSPACE).  Calls share that array, so keep them ordered on
-    one stream.  Output buffers may be passed in to avoid allocating them
-    here as well."""
+    """spec_verify without any device allocation inside the call, for callers
+    that cannot allocate while they verify (a serving loop that keeps
+    allocation off its hot path, a runtime whose memory pool owns the
+    device).  Scratch comes from a fixed array in the library (48 MiB);
+    larger batches raise SpecError (SPEC_ERR_WORKSPACE).  Calls share that
+    array, so keep them ordered on one stream.  Pass out_tokens and
+    out_num_accepted to keep this wrapper from allocating them; the inputs
+    are checked as spec_verify checks them."""
     import torch
     B = temperature.numel()
     V = target_logits.shape[-1]
     dt = _dtype_code(target_logits)
+    for name, t in (("target_logits", target_logits), ("draft_logits", draft_logits)):
+        _check_dev(name, t, target_logits.dtype)
+    _check_dev("draft_tokens", draft_tokens, torch.int32)
+    _check_dev("u_accept", u_accept, torch.float32)
+    _check_dev("u_resample", u_resample, torch.float32)
+    _check_dev("temperature", temperature, torch.float32)
+    _check_dev("k_offsets", k_offsets, torch.int32)
+    if k_offsets.numel() != B + 1:
+        raise ValueError("k_offsets must have B + 1 entries")
     R_t = u_resample.numel()
     dev = target_logits.device
     if out_tokens is None:
         out_tokens = torch.empty(R_t, dtype=torch.int32, device=dev)
     if out_num_accepted is None:
         out_num_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    _check_dev("out_tokens", out_tokens, torch.int32)
+    _check_dev("out_num_accepted", out_num_accepted, torch.int32)
+    if out_tokens.numel() < R_t or out_num_accepted.numel() < B:
+        raise ValueError("out_tokens needs R_t = u_resample.numel() entries and out_num_accepted B")
     rc = lib().spec_verify_noalloc(_p(target_logits), _p(draft_logits), _p(draft_tokens), _p(u_accept),
                                    _p(u_resample), _p(temperature), B, _p(k_offsets), V, dt,
                                    _p(out_tokens), _p(out_num_accepted), _stream(stream))

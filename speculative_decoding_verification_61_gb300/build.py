@@ -1,8 +1,8 @@
 """Build the sm_103a CUDA library in-tree:
 speculative_decoding_verification_61_gb300/_build/libspecverify.so
 
-Four translation units (chain verify, tree verify, vocab-sharded verify, the adaptive-k
-controller), one
+Five translation units (chain verify, tree verify, vocab-sharded verify, the adaptive-k
+controller, the allocation-free verify), one
 -gencode (sm_103a), static CUDA runtime, so the shared object loads with
 plain ctypes and needs no GPU at load time.
 """
@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libspecverify.so")
-SOURCES = [os.path.join(CSRC, n) for n in ("spec_verify.cu", "tree_verify.cu", "shard_verify.cu", "adapt_k.cu")]
+SOURCES = [os.path.join(CSRC, n)
+           for n in ("spec_verify.cu", "tree_verify.cu", "shard_verify.cu", "adapt_k.cu", "noalloc.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, n) for n in ("device_utils.cuh", "verify_common.cuh", "host_common.h")] + [
     os.path.join(INCLUDE, "spec_verify.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -56,6 +56,15 @@ void *get_internal_ws(DeviceState &st, size_t need);
 bool reset_tickets(void *ws, cudaStream_t stream);
 bool aligned16(const void *p);
 int check_common(int B, int V, int dtype);
+// One verify call (spec_verify, spec_verify_ex, spec_verify_lse): the
+// caller's workspace if given (checked; its ticket words zeroed on the
+// stream unless reset_counters is false, when the caller has cleared them),
+// else the library-owned one.
+int verify_call(const void *target_logits, const void *draft_logits, const double *draft_lse2,
+                const int32_t *draft_tokens, const float *u_accept, const float *u_resample, const float *temperature,
+                int B, const int32_t *k_offsets, int V, int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
+                const spec_verify_aux_t *aux, void *workspace, size_t workspace_bytes, void *stream,
+                bool reset_counters);
 
 // Launch with programmatic stream serialization: the kernel may begin
 // while its predecessor on the stream drains; it orders itself with

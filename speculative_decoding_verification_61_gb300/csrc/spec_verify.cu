@@ -145,6 +145,10 @@ __global__ void __launch_bounds__(SPEC_RESOLVE_THREADS, SPEC_RESOLVE_MIN_BLOCKS)
 
     // --- 1. row statistics and the decision -------------------------------
     grid_dependency_wait();
+    // a streaming CTA that timed out leaves partials of unknown age behind:
+    // every sequence then reports a data error rather than outputs that
+    // look valid (the status word is read here, used in the decision)
+    const int status = (warp == 0) ? __ldcg(ws.counters + kStatus) : 0;
     if (c == c) {
         const int nrows = (greedy || given) ? k + 1 : 2 * k + 1;
         for (int rr = warp; rr < nrows; rr += blockDim.x >> 5) {
@@ -176,7 +180,7 @@ __global__ void __launch_bounds__(SPEC_RESOLVE_THREADS, SPEC_RESOLVE_MIN_BLOCKS)
     }
     __syncthreads();
     if (warp == 0) {
-        bool err = (c != c) || __any_sync(0xffffffffu, xbad);
+        bool err = (c != c) || status == SPEC_ERR_TIMEOUT || __any_sync(0xffffffffu, xbad);
         int n = -1, tok = -1, kind = kJobNone;
         float alpha_out = NAN;
         double Lt = NAN, Ld = NAN;
@@ -408,6 +412,9 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
         if (blockIdx.x == 0 && threadIdx.x == 0) set_status(counters + kStatus, SPEC_ERR_INVALID_ARG);
         return;
     }
+    // the streaming pass timed out: its partials are of unknown age, so every
+    // row gets -1 (and no normaliser) instead of a token that looks valid
+    const bool timed_out = __ldcg(counters + kStatus) == SPEC_ERR_TIMEOUT;
     const int R = s_kofs[B];
     const int lane = lane_id();
     const int nw = (gridDim.x * blockDim.x) >> 5;
@@ -417,7 +424,7 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
             const int mid = (lo + hi + 1) >> 1;
             if (s_kofs[mid] <= r) lo = mid; else hi = mid - 1;
         }
-        const float c = temp_scale(temperature[lo]);
+        const float c = timed_out ? __int_as_float(0x7fc00000) : temp_scale(temperature[lo]);
         const float2 *pr = part + static_cast<int64_t>(r) * g.n_sub;
         int token = -1;
         double L = NAN;
@@ -709,8 +716,6 @@ size_t spec_workspace_bytes(int B, int V, int dtype) {
     return ws_layout(std::max(B, 1), g).total;
 }
 
-size_t spec_noalloc_bytes(int B, int V, int dtype) { return spec_workspace_bytes(B, V, dtype); }
-
 }  // extern "C"
 
 namespace specv {
@@ -735,7 +740,8 @@ void *call_workspace(void *workspace, size_t workspace_bytes, const WsLayout &l,
 int verify_call(const void *target_logits, const void *draft_logits, const double *draft_lse2,
                 const int32_t *draft_tokens, const float *u_accept, const float *u_resample, const float *temperature,
                 int B, const int32_t *k_offsets, int V, int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
-                const spec_verify_aux_t *aux, void *workspace, size_t workspace_bytes, void *stream) {
+                const spec_verify_aux_t *aux, void *workspace, size_t workspace_bytes, void *stream,
+                bool reset_counters) {
     int rc = check_common(B, V, dtype);
     if (rc != SPEC_OK) return rc;
     if (B == 0) return SPEC_OK;
@@ -750,7 +756,7 @@ int verify_call(const void *target_logits, const void *draft_logits, const doubl
     DeviceState *st = device_state(&dev);
     if (!st) return SPEC_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    void *ws = call_workspace(workspace, workspace_bytes, l, *st, s, &rc);
+    void *ws = reset_counters ? call_workspace(workspace, workspace_bytes, l, *st, s, &rc) : workspace;
     if (!ws) return rc;
     spec_verify_aux_t a{};
     if (aux) a = *aux;
@@ -841,7 +847,8 @@ int spec_verify_ex(const void *target_logits, const void *draft_logits, const in
                    const int32_t *k_offsets, int V, int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
                    const spec_verify_aux_t *aux, void *workspace, size_t workspace_bytes, void *stream) {
     return verify_call(target_logits, draft_logits, nullptr, draft_tokens, u_accept, u_resample, temperature, B,
-                       k_offsets, V, dtype, out_tokens, out_num_accepted, aux, workspace, workspace_bytes, stream);
+                       k_offsets, V, dtype, out_tokens, out_num_accepted, aux, workspace, workspace_bytes, stream,
+                       true);
 }
 
 int spec_verify(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
@@ -849,7 +856,7 @@ int spec_verify(const void *target_logits, const void *draft_logits, const int32
                 const int32_t *k_offsets, int V, int dtype, int32_t *out_tokens, int32_t *out_num_accepted,
                 void *stream) {
     return verify_call(target_logits, draft_logits, nullptr, draft_tokens, u_accept, u_resample, temperature, B,
-                       k_offsets, V, dtype, out_tokens, out_num_accepted, nullptr, nullptr, 0, stream);
+                       k_offsets, V, dtype, out_tokens, out_num_accepted, nullptr, nullptr, 0, stream, true);
 }
 
 int spec_verify_lse(const void *target_logits, const void *draft_logits, const double *draft_lse2,
@@ -859,7 +866,8 @@ int spec_verify_lse(const void *target_logits, const void *draft_logits, const d
                     size_t workspace_bytes, void *stream) {
     if (B > 0 && !draft_lse2) return SPEC_ERR_INVALID_ARG;
     return verify_call(target_logits, draft_logits, draft_lse2, draft_tokens, u_accept, u_resample, temperature, B,
-                       k_offsets, V, dtype, out_tokens, out_num_accepted, aux, workspace, workspace_bytes, stream);
+                       k_offsets, V, dtype, out_tokens, out_num_accepted, aux, workspace, workspace_bytes, stream,
+                       true);
 }
 
 int spec_draft_sample_ex(const void *draft_logits, const float *temperature, const float *u_draft, int B,
@@ -1057,82 +1065,5 @@ int spec_shutdown(void) {
 }
 
 const char *spec_last_error(void) { return g_last_error; }
-
-}  // extern "C"
-
-// ------------------------------------------------------------------
-// Allocation-free verify.
-//
-// Some callers cannot allocate device memory at the moment they need a
-// verify step: code running inside a CUDA stream capture (a cudaMalloc
-// there breaks the capture), serving loops that forbid allocation on the
-// hot path so that latency stays predictable, and memory pools or embedded
-// runtimes that own all device memory themselves.  spec_verify_noalloc
-// serves them: it runs the same kernels as spec_verify, but its scratch
-// memory is a fixed array compiled into this library, so the call itself
-// never allocates.
-//
-// The array below is a file-scope device variable.  Every GPU on which the
-// library is loaded holds kNoAllocScratchBytes of it until the process
-// exits.  Its name in host code only stands in for the device object, so
-// the host looks its device address up with cudaGetSymbolAddress, once per
-// device, with that device current.
-constexpr size_t kNoAllocScratchBytes = SPEC_NOALLOC_SCRATCH_BYTES;  // 48 MiB
-static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-void *g_noalloc_addr[kMaxDevices] = {};
-
-extern "C" {
-
-int spec_verify_noalloc(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
-                        const float *u_accept, const float *u_resample, const float *temperature, int B,
-                        const int32_t *k_offsets, int V, int dtype, int32_t *out_tokens,
-                        int32_t *out_num_accepted, void *stream) {
-    int rc = check_common(B, V, dtype);
-    if (rc != SPEC_OK) return rc;
-    if (B == 0) return SPEC_OK;
-    if (!target_logits || !draft_logits || !draft_tokens || !u_accept || !u_resample || !temperature ||
-        !k_offsets || !out_tokens || !out_num_accepted)
-        return SPEC_ERR_INVALID_ARG;
-    if (!aligned16(target_logits) || !aligned16(draft_logits)) return SPEC_ERR_ALIGNMENT;
-    Geometry g;
-    make_geometry(V, dtype, &g);
-    const WsLayout l = ws_layout(B, g);
-    if (l.total > kNoAllocScratchBytes) {
-        snprintf(g_last_error, sizeof g_last_error,
-                 "spec_verify_noalloc: B=%d, V=%d needs %zu bytes of scratch, the fixed array holds %zu", B, V,
-                 l.total, kNoAllocScratchBytes);
-        return SPEC_ERR_WORKSPACE;
-    }
-    int dev;
-    DeviceState *st = device_state(&dev);
-    if (!st) return SPEC_ERR_CUDA;
-    void *ws;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_noalloc_addr[dev]) {
-            // first call on this device: resolve the array's device address
-            void *p = nullptr;
-            if (!cuda_ok(cudaGetSymbolAddress(&p, g_noalloc_scratch), "cudaGetSymbolAddress(g_noalloc_scratch)"))
-                return SPEC_ERR_CUDA;
-            g_noalloc_addr[dev] = p;
-        }
-        ws = g_noalloc_addr[dev];
-    }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the array keeps the previous call's contents: the status word must
-    // start at zero; the unit-ticket words, which stats_kernel leaves at
-    // zero, are cleared by the same memset at no extra cost; the
-    // per-sequence counters are reset by stats_kernel
-    if (!cuda_ok(cudaMemsetAsync(static_cast<unsigned char *>(ws) + kStatusOffset, 0,
-                                 (kCounterWords - kStatus) * sizeof(int), s),
-                 "cudaMemsetAsync(noalloc status and tickets)"))
-        return SPEC_ERR_CUDA;
-    const spec_verify_aux_t a{};
-    if (dtype == SPEC_F32)
-        return launch_verify<SPEC_F32>(target_logits, draft_logits, nullptr, draft_tokens, u_accept, u_resample,
-                                       temperature, B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st, s);
-    return launch_verify<SPEC_BF16>(target_logits, draft_logits, nullptr, draft_tokens, u_accept, u_resample,
-                                    temperature, B, k_offsets, g, out_tokens, out_num_accepted, a, ws, l, *st, s);
-}
 
 }  // extern "C"

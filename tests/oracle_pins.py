@@ -155,21 +155,33 @@ def enumerate_law(lib, t_rows, d_rows, T):
     B = len(seqs)
     slots = np.stack([res.tokens[slot_of(kw["k_offsets"], b): slot_of(kw["k_offsets"], b) + k + 1]
                       for b in range(B)])
-    return dict(p=p, q=q, weights=weights, slots=slots, num=res.num_accepted)
+    return dict(p=p, q=q, weights=weights, slots=slots, num=res.num_accepted, kw=kw, margin=res.margin)
 
 
-def check_enumeration(lib, k, seed, V=8, T=1.0):
+def enumeration_rows(k, seed, V=8):
+    """The tiny-vocabulary target and draft rows the enumeration pins use."""
     rng = np.random.default_rng(seed)
     t_rows = (rng.standard_normal((k + 1, V)) * 1.5).astype(np.float32)
     d_rows = (t_rows[:k] + rng.standard_normal((k, V)) * 0.8).astype(np.float32)
+    return t_rows, d_rows
+
+
+def emitted_law(weights, slots, num, i, V):
+    """Law of output slot i over the enumeration cells (weighted), given that
+    the slot holds a token (at least i drafted tokens accepted)."""
+    emitted = num >= i
+    mass = weights[emitted].sum()
+    return np.array([weights[emitted & (slots[:, i] == y)].sum() for y in range(V)]) / mass
+
+
+def check_enumeration(lib, k, seed, V=8, T=1.0):
+    t_rows, d_rows = enumeration_rows(k, seed, V)
     e = enumerate_law(lib, t_rows, d_rows, T)
     w, slots, num, p, q = e["weights"], e["slots"], e["num"], e["p"], e["q"]
     assert abs(w.sum() - 1.0) < 1e-12
     assert (num >= 0).all()
     for i in range(k + 1):
-        emitted = num >= i  # slot i holds a token iff at least i accepted
-        mass = w[emitted].sum()
-        law = np.array([w[emitted & (slots[:, i] == y)].sum() for y in range(V)]) / mass
+        law = emitted_law(w, slots, num, i, V)  # slot i holds a token iff at least i accepted
         np.testing.assert_allclose(law, p[i], atol=1e-12, rtol=0,
                                    err_msg=f"law of slot {i} != p_{i}")
         # slots after the emitted one are -1

@@ -209,3 +209,15 @@ def test_selfcheck_host_argument_errors(lib):
     assert lib.spec_selfcheck_wait_timeout(None, 256, None) == -1
     assert lib.spec_selfcheck_wait_timeout(vp(1 << 20), 64, None) == -5
     assert lib.spec_selfcheck_wait_timeout(vp((1 << 20) + 4), 256, None) == -2
+
+
+def test_noalloc_wrapper_refuses_host_tensors(lib):
+    """The allocation-free wrapper checks its tensors before it hands any
+    pointer to the library: host (CPU) tensors are refused on the host."""
+    torch = pytest.importorskip("torch")
+    import speculative_decoding_verification_61_gb300 as sv
+    B, V, R_d = 2, 64, 4
+    z = torch.zeros((R_d + B, V), dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        sv.spec_verify_noalloc(z, z[:R_d], torch.zeros(R_d, dtype=torch.int32), torch.zeros(R_d),
+                               torch.zeros(R_d + B), torch.ones(B), torch.tensor([0, 2, 4], dtype=torch.int32))

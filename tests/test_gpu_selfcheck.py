@@ -40,3 +40,29 @@ def test_bounded_waits_give_up_and_report_timeout(sv):
     ora = oracle.verify(w.target_logits, w.draft_logits, toks.cpu().numpy(), w.u_accept, w.u_resample,
                         w.temperature, w.k_offsets)
     compare_verify(w, gt.cpu().numpy(), gn.cpu().numpy(), None, ora)
+
+
+def test_timed_out_workspace_reports_every_sequence_as_an_error(sv):
+    """While a workspace's status word holds SPEC_ERR_TIMEOUT (a bounded wait
+    gave up, so its partials may be of any age), verify and draft-sampling
+    calls on it mark every sequence and row -1 instead of giving outputs that
+    look valid; once the status is cleared the same calls match the
+    library-owned workspace's results again."""
+    w = workloads.make_case(B=6, k=4, V=2000, dtype="f32", seed=7, temperature="odd_greedy")
+    d = to_device(w)
+    toks = gpu_draft_sample(d)
+    ref_t, ref_n, _ = gpu_verify(d, toks)
+    ws = torch.zeros(sv.workspace_bytes(w.B, w.V, sv.F32), dtype=torch.uint8, device="cuda")
+    sv.selfcheck_wait_timeout(ws)  # records SPEC_ERR_TIMEOUT in ws (about 4 s)
+    args = (d["u_accept"], d["u_resample"], d["temperature"], d["k_offsets"])
+    gt, gn = sv.spec_verify(d["target_logits"], d["draft_logits"], toks, *args, workspace=ws)
+    gd = sv.spec_draft_sample(d["draft_logits"], d["temperature"], d["u_draft"], d["k_offsets"], workspace=ws)
+    torch.cuda.synchronize()
+    assert sv.workspace_status(ws) == -4
+    assert (gn == -1).all() and (gt == -1).all() and (gd == -1).all()
+    assert sv.workspace_status(ws, clear=True) == -4
+    gt, gn = sv.spec_verify(d["target_logits"], d["draft_logits"], toks, *args, workspace=ws)
+    gd = sv.spec_draft_sample(d["draft_logits"], d["temperature"], d["u_draft"], d["k_offsets"], workspace=ws)
+    torch.cuda.synchronize()
+    assert sv.workspace_status(ws) == 0
+    assert torch.equal(gt, ref_t) and torch.equal(gn, ref_n) and torch.equal(gd, toks)

@@ -186,3 +186,21 @@ def test_generator_is_deterministic_and_shaped():
     assert c.target_logits.dtype == np.uint16 and c.rows_target == c.rows_draft + 10
     assert (c.temperature[1::2] == 0).all() and (c.temperature[::2] == 1).all()
     assert c.k.min() >= 1 and c.k.max() <= 10
+
+
+def test_generator_row_arrangements():
+    """Without noise a target row is the Zipf ranks -a ln(1 + pi_r(v)) laid out
+    by its permutation pi_r.  The default draws one arrangement per workload
+    and rotates it per row (every row is a cyclic shift of the first);
+    perm="per_row" draws an independent permutation for every row (no row is
+    a cyclic shift of another)."""
+    kw = dict(B=3, k=2, V=48, sigma_t=0.0, sigma_d=0.0, seed=5)
+    base = np.sort((-1.1 * np.log1p(np.arange(48, dtype=np.float64))).astype(np.float32))
+    for perm, cyclic in (("rotated", True), ("per_row", False)):
+        w = workloads.make_case(perm=perm, **kw)
+        rows = w.target_logits
+        for r in rows:  # every row holds each Zipf rank exactly once
+            assert np.array_equal(np.sort(r), base)
+        shifts = [any(np.array_equal(rows[i], np.roll(rows[0], c)) for c in range(48))
+                  for i in range(1, len(rows))]
+        assert all(shifts) if cyclic else not any(shifts), perm

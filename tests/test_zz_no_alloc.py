@@ -1,9 +1,9 @@
 """The allocation-free verify entry point (spec_verify_noalloc).
 
 It exists for callers that cannot allocate device memory while they verify:
-code under CUDA stream capture, serving loops that forbid allocation on the
-hot path, and runtimes whose memory pool owns the whole GPU.  Its scratch
-memory is a fixed array inside the library, so these tests check that it
+serving loops that keep allocation off the hot path, and runtimes whose
+memory pool owns the whole GPU.  Its scratch memory is a fixed array inside
+the library, so these tests check that it
 gives exactly the outputs of spec_verify (all outputs are integers: token
 ids and accept counts, compared exactly, as every GPU parity test does
 outside flagged margins), on two calls in a row (the array keeps the first
@@ -94,3 +94,37 @@ def test_noalloc_refuses_batches_beyond_the_array(sv):
     assert rc == -5  # SPEC_ERR_WORKSPACE
     assert b"scratch" in sv.lib().spec_last_error()
     assert sv.noalloc_bytes(512, 152064, sv.BF16) <= limit
+
+
+def test_noalloc_wrapper_checks_its_inputs(sv):
+    """The Python wrapper refuses what spec_verify refuses, before the C ABI
+    sees a pointer: host tensors, mixed logit dtypes, non-contiguous views,
+    a short k_offsets, and output buffers of the wrong type or size."""
+    w = workloads.make_case(B=4, k=3, V=1000, dtype="f32", seed=33)
+    d = _device(w)
+    toks = sv.spec_draft_sample(d["draft_logits"], d["temperature"], d["u_draft"], d["k_offsets"])
+    rest = (d["u_accept"], d["u_resample"], d["temperature"], d["k_offsets"])
+    tl, dl = d["target_logits"], d["draft_logits"]
+    with pytest.raises(ValueError):
+        sv.spec_verify_noalloc(tl.cpu(), dl, toks, *rest)
+    with pytest.raises(TypeError):
+        sv.spec_verify_noalloc(tl, dl.to(torch.bfloat16), toks, *rest)
+    strided = torch.empty((tl.shape[1], tl.shape[0]), dtype=tl.dtype, device="cuda").t()
+    strided.copy_(tl)
+    with pytest.raises(ValueError):
+        sv.spec_verify_noalloc(strided, dl, toks, *rest)
+    with pytest.raises(ValueError):
+        sv.spec_verify_noalloc(tl, dl, toks, *rest[:3], d["k_offsets"][:-1])
+    with pytest.raises(ValueError):
+        sv.spec_verify_noalloc(tl, dl, toks, *rest, out_tokens=torch.empty(2, dtype=torch.int32, device="cuda"))
+    with pytest.raises(TypeError):
+        sv.spec_verify_noalloc(tl, dl, toks, *rest,
+                               out_num_accepted=torch.empty(w.B, dtype=torch.int64, device="cuda"))
+    # given buffers of the right kind are used as they are
+    out_t = torch.empty(w.rows_target, dtype=torch.int32, device="cuda")
+    out_n = torch.empty(w.B, dtype=torch.int32, device="cuda")
+    t, n = sv.spec_verify_noalloc(tl, dl, toks, *rest, out_tokens=out_t, out_num_accepted=out_n)
+    ref_t, ref_n = sv.spec_verify(tl, dl, toks, *rest)
+    torch.cuda.synchronize()
+    assert t is out_t and n is out_n
+    assert torch.equal(t, ref_t) and torch.equal(n, ref_n)

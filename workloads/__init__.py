@@ -15,7 +15,9 @@ sees from a real target/draft pair):
   the vocabulary per workload, rotated by a random offset per row,
   pi_r(v) = P[(v + c_r) mod V].  Each row keeps its multiset of logits
   exactly Zipf + noise and puts its large logits at different token ids;
-  rotations make 128K-wide rows cheap to draw;
+  rotations make 128K-wide rows cheap to draw.  make_case(perm="per_row")
+  draws instead a fresh, independent permutation pi_r for every row (the
+  workload text's wording taken literally), for parity cases;
 * draft row i of a sequence: z_d = z_t(target row i of that sequence) +
   N(0, sigma_d^2);
 * bf16 workloads are generated in fp32 and rounded to bf16 here
@@ -120,14 +122,17 @@ def uniforms(rng: np.random.Generator, n: int) -> np.ndarray:
 
 def make_case(B: int, k, V: int, dtype: str = F32, temperature=1.0, a: float = 1.1,
               sigma_t: float = 1.0, sigma_d=0.5, seed: int = 1234,
-              uniform_seed: int = 0, name: str | None = None) -> Workload:
+              uniform_seed: int = 0, name: str | None = None, perm: str = "rotated") -> Workload:
     """Build a workload.
 
     k: int (uniform), a sequence of per-sequence k_b, or "ragged_1_10".
     temperature: float (all sequences), a sequence, or "odd_greedy" (odd
       sequences T=0, even sequences T=1).
     sigma_d: float, or "uniform_0.2_1.5" (one sigma per draft row).
+    perm: "rotated" (one arrangement per workload, rotated per row) or
+      "per_row" (an independent random permutation for every target row).
     """
+    assert perm in ("rotated", "per_row")
     ss = np.random.SeedSequence(seed)
     ss_k, ss_layout, ss_seq = ss.spawn(3)
     if isinstance(k, str):
@@ -175,9 +180,12 @@ def make_case(B: int, k, V: int, dtype: str = F32, temperature=1.0, a: float = 1
             sig = np.full(k_b, float(sigma_d))
         row = np.empty(V, dtype=np.float32)
         for i in range(k_b + 1):
-            c = int(shifts[i])
-            row[:V - c] = arranged[c:]
-            row[V - c:] = arranged[:c]
+            if perm == "per_row":
+                row[:] = base[rng.permutation(V)]
+            else:
+                c = int(shifts[i])
+                row[:V - c] = arranged[c:]
+                row[V - c:] = arranged[:c]
             row += rng.standard_normal(V, dtype=np.float32) * np.float32(sigma_t)
             store(zt_out[t0 + i], row)
             if i < k_b:
@@ -202,7 +210,7 @@ def make_case(B: int, k, V: int, dtype: str = F32, temperature=1.0, a: float = 1
                     draft_logits=zd, u_accept=u_accept, u_resample=u_resample,
                     u_draft=u_draft,
                     meta=dict(a=a, sigma_t=sigma_t, sigma_d=sigma_d, seed=seed,
-                              uniform_seed=uniform_seed))
+                              uniform_seed=uniform_seed, perm=perm))
 
 
 def make_config(cfg: int) -> Workload:
