@@ -57,7 +57,18 @@ def parse():
     ap.add_argument("--tree", type=int, default=1, help="also time the tree verify workload (0: skip)")
     ap.add_argument("--vocab-shard", default="2,4,8",
                     help="rank counts of the vocab-sharded verify to time ('' to skip)")
+    ap.add_argument("--k-sweep", default="1,2,3,4,5,6,7,8,9,10",
+                    help="draft lengths k of the spec_round sweep (B=512, V=128256, bf16, T=1; '' to skip)")
     return ap.parse_args()
+
+
+def line_config(w, world: int) -> dict:
+    """The workload as both arms describe it on their JSON lines."""
+    return {"workload": w.name, "B": w.B, "V": w.V, "k": "uniform 1..10 per sequence",
+            "temperature": 1.0, "logits": w.dtype, "rows_target": w.rows_target, "rows_draft": w.rows_draft,
+            "step": "one sampling round: the draft-side softmax + multinomial of every draft row, then the "
+                    "verify-and-resample of every sequence (spec_round)",
+            "l2": "inputs > L2 (no flush)", "parallelism": f"replicas x{world}"}
 
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "spec_round_traffic_B512_ragged_k1to10_V128256_bf16.txt")
@@ -179,12 +190,13 @@ def to_device(w, torch, dev):
                 ud=t(w.u_draft), T=t(w.temperature), ko=t(w.k_offsets))
 
 
-def measure(w, steps, warmup, torch, sv, dev, sampler=None, barrier=None, mode="fused"):
+def measure(w, steps, warmup, torch, sv, dev, sampler=None, barrier=None, mode="fused", keep_outputs=False):
     """Device-resident timing of one sampling round with CUDA events on the
     launching stream.  mode "round": spec_round (both passes in one call);
     "fused": spec_draft_sample_lse + spec_verify_lse (each row read once);
     "separate": spec_draft_sample + spec_verify.  Returns per-step and
-    per-call times (ms; in round mode the draft slot is empty)."""
+    per-call times (ms; in round mode the draft slot is empty) and, with
+    keep_outputs, the last step's draft tokens, tokens and counts (host)."""
     fused = mode == "fused"
     d = to_device(w, torch, dev)
     toks = torch.empty(w.rows_draft, dtype=torch.int32, device=dev)
@@ -247,9 +259,10 @@ def measure(w, steps, warmup, torch, sv, dev, sampler=None, barrier=None, mode="
         draft = [e[0].elapsed_time(e[1]) for e in ev]
         ver = [e[1].elapsed_time(e[2]) for e in ev]
     n_acc = out_n.float().mean().item()
+    outs = (toks.cpu().numpy(), out_t.cpu().numpy(), out_n.cpu().numpy()) if keep_outputs else None
     del d
     return dict(step_ms=total / steps, draft_ms=statistics.mean(draft), verify_ms=statistics.mean(ver),
-                verify_ms_median=statistics.median(ver), mean_accepted=n_acc)
+                verify_ms_median=statistics.median(ver), mean_accepted=n_acc, outputs=outs)
 
 
 class _Null:
@@ -398,6 +411,66 @@ def measure_vocab_shard(torch, sv, dev, reps, warmup, Gs):
                      "spec_shard_decide (shard_decide_kernel), spec_shard_draw (shard_draw_kernel); exchanges not timed"}
 
 
+def k_sweep(torch, sv, dev, ks, reps, warmup, peak):
+    """spec_round on B = 512 sequences that all draft k tokens, V = 128256,
+    bf16, T = 1, for each k in ks ("【大模型】- 推测解码", optimize_parameters:
+    the draft length tried over 1..10).  One seeded batch with k = max(ks)
+    is generated; the batch for a smaller k keeps each sequence's first k
+    drafted positions and its target row at position k (the bonus row after
+    k acceptances), with their uniforms, cut out on the device.  Per k: the
+    round's time, rows/s, algorithmic GB/s and its fraction of the measured
+    copy peak, the mean accepted count and the emitted tokens per second
+    (B * (n + 1) per round); best_k maximises the latter for this step."""
+    import numpy as np
+    import workloads
+    kmax, B, V = max(ks), 512, 128256
+    w = workloads.make_case(B=B, k=kmax, V=V, dtype=workloads.BF16, temperature=1.0, a=1.1, sigma_t=1.0,
+                            sigma_d=0.5, seed=1105, name=f"B{B}_k{kmax}_V{V}_bf16_T1")
+    d = to_device(w, torch, dev)
+    stream = torch.cuda.current_stream()
+    out = {}
+    for k in ks:
+        bb = torch.arange(B, device=dev)
+        t_idx = (bb[:, None] * (kmax + 1) + torch.arange(k + 1, device=dev)[None, :]).reshape(-1)
+        d_idx = (bb[:, None] * kmax + torch.arange(k, device=dev)[None, :]).reshape(-1)
+        tl, dl = d["tl"].index_select(0, t_idx), d["dl"].index_select(0, d_idx)
+        ua, ud, ur = d["ua"][d_idx], d["ud"][d_idx], d["ur"][t_idx]
+        ko = (torch.arange(B + 1, device=dev, dtype=torch.int32) * k).contiguous()
+        toks = torch.empty(B * k, dtype=torch.int32, device=dev)
+        out_t = torch.empty(B * (k + 1), dtype=torch.int32, device=dev)
+        out_n = torch.empty(B, dtype=torch.int32, device=dev)
+
+        def call():
+            sv.spec_round(tl, dl, ud, ua, ur, d["T"], ko, out_draft_tokens=toks, out_tokens=out_t,
+                          out_num_accepted=out_n)
+        for _ in range(max(3, warmup)):
+            call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        sub = workloads.Workload(name=f"k{k}", B=B, V=V, dtype=w.dtype, k_offsets=np.arange(B + 1, dtype=np.int32) * k,
+                                 temperature=w.temperature, target_logits=None, draft_logits=None,
+                                 u_accept=None, u_resample=None, u_draft=None)
+        ab = workloads.algorithmic_bytes(sub)
+        nbytes = ab["verify_lse"] + ab["draft_sample"]
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        n_acc = out_n.float().mean().item()
+        out[str(k)] = {"k": k, "round_ms": round(ms, 5), "rows_per_s": (B * (2 * k + 1)) / (ms * 1e-3),
+                       "gbs": gbs, "frac_of_peak": gbs / peak, "bytes": nbytes, "mean_accepted": n_acc,
+                       "acceptance_per_draft": n_acc / k, "emitted_tokens_per_s": B * (n_acc + 1) / (ms * 1e-3)}
+        del tl, dl, ua, ud, ur, toks, out_t, out_n
+    del d
+    best = max(out.values(), key=lambda r: r["emitted_tokens_per_s"])["k"]
+    return {"workload": f"B{B}, every sequence k drafted tokens, V={V}, bf16, T=1 (sigma_t 1, sigma_d 0.5, "
+                        f"seed 1105; batches cut from one k={kmax} batch)",
+            "step": "spec_round", "reps_per_k": reps, "by_k": out, "best_k_by_emitted_tokens_per_s": best}
+
+
 def adaptive_k_timing(torch, sv, dev, B=4096, reps=1000):
     """Device time of one adaptive-k update (spec_adapt_update) for B
     sequences, the round-to-round step of a serving loop."""
@@ -487,18 +560,63 @@ class OracleSample:
         return cls(w, nthreads, max(probe.n, probe.n * seconds / max(t, 1e-3)))
 
     def describe(self, reps, t):
+        how = "OpenMP over sequences" if self.nthreads > 1 else "one thread"
         return (f"first {self.n} of {self.w.B} sequences of {self.w.name} x{reps} ({self.rows * reps} rows), "
-                f"draft sample + verify, fp64 C oracle, OpenMP over sequences, {t:.1f} s")
+                f"draft sample + verify, fp64 C oracle, {how}, {t:.1f} s")
 
 
-def cpu_baseline(w, seconds, nthreads):
-    """The oracle on a bounded sample of the workload, about `seconds` of CPU time."""
+def _timed_sample(w, nthreads, seconds):
     smp = OracleSample.sized(w, nthreads, seconds)
     reps, t = 1, smp.step()
     while t * (reps + 1) / reps < seconds and reps < 64:
         t += smp.step()
         reps += 1
-    return dict(value=smp.rows * reps / t, unit=UNIT, cores=nthreads, kind="oracle", sample=smp.describe(reps, t))
+    return dict(value=smp.rows * reps / t, unit=UNIT, cores=nthreads, kind="oracle",
+                sequences_per_s=smp.n * reps / t, sample=smp.describe(reps, t))
+
+
+def cpu_baseline(w, seconds, nthreads):
+    """The oracle on bounded samples of the workload: about `seconds` of CPU
+    time with OpenMP over sequences on every host core, and a third of that
+    on one thread."""
+    line = _timed_sample(w, nthreads, seconds)
+    line["single_thread"] = _timed_sample(w, 1, seconds / 3)
+    return line
+
+
+FLAG_MARGIN = 1e-5
+
+
+def oracle_parity(w, gpu_outputs, nthreads):
+    """The timed round's outputs for every sequence of the workload against
+    the oracle (part of the CPU-baseline leg, outside every timed region):
+    the draft tokens against the oracle's draft sampling, then the verify
+    outputs against the oracle's verify on the same draft tokens.  Decisions
+    whose oracle margin is <= 1e-5 are flagged: counted, and not required to
+    match.  Returns the counts."""
+    import numpy as np
+    import oracle
+    g_draft, g_tok, g_num = gpu_outputs
+    ds = oracle.draft_sample(w.draft_logits, w.temperature, w.u_draft, w.k_offsets, nthreads=nthreads)
+    dflag = ds.margin <= FLAG_MARGIN
+    dsame = g_draft == ds.tokens
+    ov = oracle.verify(w.target_logits, w.draft_logits, g_draft, w.u_accept, w.u_resample, w.temperature,
+                       w.k_offsets, nthreads=nthreads)
+    flagged = flagged_match = mismatches = 0
+    for b in range(w.B):
+        o, k = int(w.k_offsets[b]) + b, int(w.k_offsets[b + 1] - w.k_offsets[b])
+        same = bool(g_num[b] == ov.num_accepted[b] and np.array_equal(g_tok[o:o + k + 1], ov.tokens[o:o + k + 1]))
+        if ov.num_accepted[b] >= 0 and ov.margin[b] <= FLAG_MARGIN:
+            flagged += 1
+            flagged_match += int(same)
+        elif not same:
+            mismatches += 1
+    return {"oracle": "fp64 C oracle (oracle/)", "flag_margin": FLAG_MARGIN, "sequences": int(w.B),
+            "flagged_sequences": flagged, "flagged_match": flagged_match,
+            "mismatched_sequences_outside_flags": mismatches,
+            "draft_rows": int(w.rows_draft), "draft_flagged_rows": int(dflag.sum()),
+            "draft_flagged_match": int((dflag & dsame).sum()),
+            "draft_mismatched_rows_outside_flags": int((~dflag & ~dsame).sum())}
 
 
 # ------------------------------------------------------------------ main
@@ -525,7 +643,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * rows_step / v,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded Zipf-like logits)",
-            "config": {"workload": w.name, "B": w.B, "V": w.V, "k": "uniform 1..10", "logits": w.dtype},
+            "config": line_config(w, world),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": nthreads, "kind": "oracle",
                              "sample": smp.describe(args.steps, sum(times)) + " (median step)"},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -558,7 +676,8 @@ def main():
     w = workloads.make_config(args.config)
     ab = workloads.algorithmic_bytes(w)
     sampler = ClockSampler(local, enabled=(rank == 0 and not args.no_clocks))
-    m = measure(w, args.steps, args.warmup, torch, sv, dev, sampler=sampler, barrier=barrier, mode="round")
+    m = measure(w, args.steps, args.warmup, torch, sv, dev, sampler=sampler, barrier=barrier, mode="round",
+                keep_outputs=(rank == 0))
     step_ms = m["step_ms"]
     if world > 1:
         import torch.distributed as dist
@@ -599,6 +718,9 @@ def main():
         del wc
 
     adapt = adaptive_k_timing(torch, sv, dev) if rank == 0 else None
+    sweep_ks = [int(x) for x in args.k_sweep.split(",") if x.strip()]
+    sweep = (k_sweep(torch, sv, dev, sweep_ks, max(50, args.steps // 10), args.warmup, peak)
+             if rank == 0 and sweep_ks else None)
     tree = measure_tree(torch, sv, dev, max(50, args.steps // 4), args.warmup) if rank == 0 and args.tree else None
     shard_gs = [int(x) for x in args.vocab_shard.split(",") if x.strip()]
     vshard = (measure_vocab_shard(torch, sv, dev, max(20, args.steps // 20), args.warmup, shard_gs)
@@ -618,16 +740,14 @@ def main():
         return 0
     import oracle
     cpu = cpu_baseline(w, args.cpu_seconds, oracle.cores()) if args.cpu_seconds > 0 else None
+    # the CPU-baseline leg also checks the timed round's outputs against the oracle
+    parity = oracle_parity(w, m["outputs"], oracle.cores()) if args.cpu_seconds > 0 else None
     clocks = sampler.summary()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Zipf-like logits + Gaussian noise)",
-        "config": {"workload": w.name, "B": w.B, "V": w.V, "k": "uniform 1..10 per sequence",
-                   "temperature": 1.0, "rows_target": w.rows_target, "rows_draft": w.rows_draft,
-                   "step": "spec_round (the draft pass of spec_draft_sample_lse and the verify pass of "
-                           "spec_verify_lse in one call)", "l2": "inputs > L2 (no flush)",
-                   "parallelism": f"replicas x{world}"},
+        "config": line_config(w, world),
         "hbm_gbs": step_bytes / (step_ms * 1e-3) / 1e9,
         "frac_of_8tbs": step_bytes / (step_ms * 1e-3) / 8e12,
         "bytes_per_step": step_bytes,
@@ -658,12 +778,14 @@ def main():
         # per step (spec_round): stats_kernel + draft_select_kernel, stats_kernel + resolve_kernel
         "gpu_launches": 4 * args.steps,
         "cpu_baseline": cpu,
+        "parity": parity,
         "e2e": e2e_line,
         "clocks": clocks,
         "other_workloads": extra,
         "adaptive_k": adapt,
         "tree_verify": tree,
         "vocab_sharded_verify": vshard,
+        "k_sweep": sweep,
     }
     print(json.dumps(line))
     if world > 1:

@@ -33,3 +33,32 @@ def test_reference_arm_under_two_ranks():
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload"] == "B512_ragged_k1to10_V128256_bf16"
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    assert d["config"] == bench.line_config(workloads.make_config(5), 2)  # the GPU arm's dict, key for key
+
+
+def test_oracle_parity_counts_flags_and_mismatches():
+    """The bench's parity block: outputs equal to the oracle's give no
+    mismatch, a flipped token outside the flags is counted."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    import oracle
+    import workloads
+    w = workloads.make_config(2)
+    ds = oracle.draft_sample(w.draft_logits, w.temperature, w.u_draft, w.k_offsets)
+    ov = oracle.verify(w.target_logits, w.draft_logits, ds.tokens, w.u_accept, w.u_resample, w.temperature,
+                       w.k_offsets)
+    p = bench.oracle_parity(w, (ds.tokens.copy(), ov.tokens.copy(), ov.num_accepted.copy()), 2)
+    assert p["mismatched_sequences_outside_flags"] == 0 and p["draft_mismatched_rows_outside_flags"] == 0
+    assert p["flagged_match"] == p["flagged_sequences"] and p["draft_flagged_match"] == p["draft_flagged_rows"]
+    assert p["draft_flagged_rows"] == int((ds.margin <= 1e-5).sum())
+    b = int(np.flatnonzero(ov.margin > 1e-5)[0])
+    tok = ov.tokens.copy()
+    o = int(w.k_offsets[b]) + b
+    tok[o] = (tok[o] + 1) % w.V
+    p = bench.oracle_parity(w, (ds.tokens.copy(), tok, ov.num_accepted.copy()), 2)
+    assert p["mismatched_sequences_outside_flags"] == 1
