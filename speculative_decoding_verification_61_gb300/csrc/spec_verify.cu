@@ -72,6 +72,9 @@ struct ResolveSmem {
     int n;     // accepted count, -1 on a data error
     int kind;  // kJobNone, kJobResid or kJobBonus
     float lth, ltl, ldh, ldl, u;
+    int last;  // this block finished the sequence's residual slices last
+    F2 Z;      // residual mass (the drawing block)
+    DrawSmem ds;
 };
 
 #ifndef SPEC_RESOLVE_THREADS
@@ -86,7 +89,8 @@ __global__ void __launch_bounds__(SPEC_RESOLVE_THREADS, SPEC_RESOLVE_MIN_BLOCKS)
     const int32_t *__restrict__ tokens, const float *__restrict__ u_accept,
     const float *__restrict__ u_resample, const float *__restrict__ temperature,
     const int *__restrict__ k_offsets, const double *__restrict__ draft_lse2, int B, Geometry g, int nsplit,
-    WsPtrs ws, int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_num, spec_verify_aux_t aux) {
+    WsPtrs ws, int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_num, spec_verify_aux_t aux,
+    int defer) {
     using E = Elem<DT>;
     __shared__ ResolveSmem sm;
     const int b = blockIdx.x / nsplit;
@@ -145,6 +149,9 @@ __global__ void __launch_bounds__(SPEC_RESOLVE_THREADS, SPEC_RESOLVE_MIN_BLOCKS)
 
     // --- 1. row statistics and the decision -------------------------------
     grid_dependency_wait();
+    // (deferred mode: resid_stream_kernel may be scheduled; it waits for this
+    // grid before it reads the pair list)
+    grid_launch_dependents();
     // a streaming CTA that timed out leaves partials of unknown age behind:
     // every sequence then reports a data error rather than outputs that
     // look valid (the status word is read here, used in the decision)
@@ -281,17 +288,33 @@ __global__ void __launch_bounds__(SPEC_RESOLVE_THREADS, SPEC_RESOLVE_MIN_BLOCKS)
 
     if (kind == kJobBonus) {
         // --- bonus draw from p at position k, by block 0 of b --------------
-        if (s != 0 || warp != 0) return;
-        const float2 *pr = ws.part + trow * g.n_sub;
-        float2 pc[kPartCache];
-        load_parts(pr, g.n_sub, pc);
-        const int token = warp_draw_row<DT>(target, trow, pr, pc, g, c, sm.M[k], sm.u);
-        if (lane == 0) out_tokens[trow] = token;
+        if (s != 0) return;
+        const int token = block_draw_row<DT>(target, trow, ws.part + trow * g.n_sub, g, c, sm.M[k], sm.u, sm.ds);
+        if (threadIdx.x == 0) out_tokens[trow] = token;
+        return;
+    }
+
+    const int64_t drow = od + n;
+    if (defer) {
+        // deferred: list the pair; resid_stream_kernel streams its two rows
+        // and resid_draw_kernel draws (nsplit is 1 in this mode)
+        if (threadIdx.x == 0) {
+            PairRec r{};
+            r.b = b;
+            r.trow = static_cast<int>(trow);
+            r.drow = static_cast<int>(drow);
+            r.c = c;
+            r.lth = sm.lth;
+            r.ltl = sm.ltl;
+            r.ldh = sm.ldh;
+            r.ldl = sm.ldl;
+            r.u = sm.u;
+            ws.pairs[atomicAdd(ws.counters + kPairs, 1)] = r;
+        }
         return;
     }
 
     // --- 2. residual mass of this block's slice of sub-chunks -------------
-    const int64_t drow = od + n;
     const float lth = sm.lth, ltl = sm.ltl, ldh = sm.ldh, ldl = sm.ldl;
     const float2 c2 = make_float2(c, c), nlth2 = make_float2(-lth, -lth), nltl2 = make_float2(-ltl, -ltl);
     const float2 nldh2 = make_float2(-ldh, -ldh), nldl2 = make_float2(-ldl, -ldl);
@@ -344,42 +367,274 @@ __global__ void __launch_bounds__(SPEC_RESOLVE_THREADS, SPEC_RESOLVE_MIN_BLOCKS)
         const float sum = warp_sum_f((acc0.x + acc0.y) + (acc1.x + acc1.y));
         if (lane == 0) rp[sc] = sum;
     }
-    // arrival, one per warp (no block barrier): the warp that arrives last,
-    // of all nsplit * 8 warps of b, draws
-    // (acquire-release add: this warp's masses are released with it, and
-    // the last warp acquires everyone's)
-    bool last = false;
-    if (lane == 0)
-        last = atomic_add_acq_rel_gpu(ws.seqcnt + b, 1) == nsplit * static_cast<int>(blockDim.x >> 5) - 1;
-    if (!__shfl_sync(0xffffffffu, last, 0)) return;
-    __syncwarp();  // lane 0's acquire, before the other lanes' reads
+    // arrival, one per block once all its warps are done: the block that
+    // arrives last, of the nsplit blocks of b, draws (acquire-release add:
+    // this block's masses are released with it, and the last block
+    // acquires everyone's; the barrier after it extends that to its warps)
+    __syncthreads();
+    if (threadIdx.x == 0) sm.last = atomic_add_acq_rel_gpu(ws.seqcnt + b, 1) == nsplit - 1;
+    __syncthreads();
+    if (!sm.last) return;
 
-    // --- 3. the residual draw, by the last warp of b -----------------------
-    float w[kPartCache];
+    // --- 3. the residual draw, by the last block of b ----------------------
+    if (warp == 0) {
+        float w[kPartCache];
 #pragma unroll
-    for (int j = 0; j < kPartCache; ++j) w[j] = (lane + 32 * j < g.n_sub) ? __ldcg(rp + lane + 32 * j) : 0.0f;
-    auto wfar = [&](int i) -> float { return __ldcg(rp + i); };
-    F2 before, Z, tgt;
-    const int sc = warp_locate(g.n_sub, w, wfar, sm.u, &before, &Z, &tgt);
+        for (int j = 0; j < kPartCache; ++j) w[j] = (lane + 32 * j < g.n_sub) ? __ldcg(rp + lane + 32 * j) : 0.0f;
+        auto wfar = [&](int i) -> float { return __ldcg(rp + i); };
+        F2 before, Z, tgt;
+        const int sc = warp_locate(g.n_sub, w, wfar, sm.u, &before, &Z, &tgt);
+        if (lane == 0) {
+            sm.ds.sc = sc;
+            sm.ds.before = before;
+            sm.ds.target = tgt;
+            sm.Z = Z;
+        }
+    }
+    __syncthreads();
     int token = -1;
+    const int sc = sm.ds.sc;
     if (sc >= 0) {
         int a, e1;
         sub_range(g, sc, &a, &e1);
         const void *rt = static_cast<const unsigned char *>(target) + trow * V * static_cast<int64_t>(E::kBytes);
         const void *rd = static_cast<const unsigned char *>(draft) + drow * V * static_cast<int64_t>(E::kBytes);
         auto W = [&](float a1, float a2) -> float { return resid_weight(a1, a2, c, lth, ltl, ldh, ldl); };
-        token = warp_scan_elems<DT>(rt, rd, a, e1, W, before, tgt);
+        token = block_scan_elems<DT>(rt, rd, a, e1, W, sm.ds.before, sm.ds.target, sm.ds);
     } else {
         // every residual weight rounded to 0: p at position n is drawn with
         // the same uniform instead
-        const float2 *pr = ws.part + trow * g.n_sub;
-        float2 pc[kPartCache];
-        load_parts(pr, g.n_sub, pc);
-        token = warp_draw_row<DT>(target, trow, pr, pc, g, c, sm.M[n], sm.u);
+        token = block_draw_row<DT>(target, trow, ws.part + trow * g.n_sub, g, c, sm.M[n], sm.u, sm.ds);
     }
-    if (lane == 0) {
+    if (threadIdx.x == 0) {
         out_tokens[trow] = token;
-        if (aux.residual_mass) aux.residual_mass[b] = __fadd_rn(Z.hi, Z.lo);
+        if (aux.residual_mass) aux.residual_mass[b] = __fadd_rn(sm.Z.hi, sm.Z.lo);
+    }
+}
+
+// ================================================================== kernel 3
+// The residual pass of the deferred epilogue, as a stream: every listed pair
+// (the target and the draft row at a rejected position) is cut into units
+// of one chunk of each row; lane 0 of warp 8 copies a unit's two chunks
+// into a 32 KB ring slot (two 1-D bulk copies on one mbarrier), and the
+// eight consumer warps each sum max(0, p - q) over their 2 KB sub-chunk of
+// the pair and store that mass.  Units are taken by tickets (unit_batch),
+// so every SM keeps its slots full until the last pair; the bytes read are
+// the pairs' rows, at the rate of the main pass instead of the rate of
+// per-block loads that wait on their decisions.
+constexpr int kRSlotBytes = 2 * kSlotBytes;  // a target chunk, then the draft chunk
+
+struct RUnit {
+    uint32_t nbytes;  // bytes of each row's chunk (0: end marker)
+    float c, lth, ltl, ldh, ldl;
+    int64_t out;      // index of the unit's first sub-chunk mass in resid_part
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 2) resid_stream_kernel(
+    const void *__restrict__ target, const void *__restrict__ draft, Geometry g, int ns,
+    const PairRec *__restrict__ pairs, float *__restrict__ resid_part, int *__restrict__ counters) {
+    using E = Elem<DT>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *ring = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + static_cast<size_t>(ns) * kRSlotBytes);
+    uint64_t *empty = full + ns;
+    RUnit *desc = reinterpret_cast<RUnit *>(empty + ns);
+    const int tid = threadIdx.x, lane = lane_id();
+    // the pair list is complete once resolve_kernel has finished
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int npairs = __ldcg(counters + kPairs);
+    if (tid == 0) {
+        for (int i = 0; i < ns; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (warp_id() == kConsumerWarps) {
+        // ------------------------------------------------------ producer
+        if (lane == 0) {
+            const int64_t total_units = static_cast<int64_t>(npairs) * g.n_chunks;
+            const int64_t n_big = big_batches(total_units, gridDim.x);
+            int issued = 0, islot = 0, cur = -1;
+            uint32_t iphase = 0;
+            bool ok = true;
+            PairRec r{};
+            int t = atomicAdd(counters + kTicket, 1);
+            while (ok) {
+                int64_t u0;
+                int cnt;
+                unit_batch(t, n_big, &u0, &cnt);
+                if (u0 >= total_units) break;
+                const int tn = atomicAdd(counters + kTicket, 1);  // next batch, in flight meanwhile
+                cnt = static_cast<int>(min(static_cast<int64_t>(cnt), total_units - u0));
+                for (int q = 0; q < cnt; ++q) {
+                    const int64_t u = u0 + q;
+                    const int p = static_cast<int>(u / g.n_chunks);
+                    const int ch = static_cast<int>(u - static_cast<int64_t>(p) * g.n_chunks);
+                    if (p != cur) {
+                        r = pairs[p];
+                        cur = p;
+                    }
+                    if (issued >= ns && !mbar_wait_bounded(&empty[islot], iphase ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    const int e0 = ch * g.chunk_elems;
+                    const int e1 = min(g.V, e0 + g.chunk_elems);
+                    RUnit d;
+                    d.nbytes = static_cast<uint32_t>(e1 - e0) * E::kBytes;
+                    d.c = r.c;
+                    d.lth = r.lth;
+                    d.ltl = r.ltl;
+                    d.ldh = r.ldh;
+                    d.ldl = r.ldl;
+                    d.out = static_cast<int64_t>(r.b) * g.n_sub + static_cast<int64_t>(ch) * kSub;
+                    desc[islot] = d;
+                    const int64_t off = static_cast<int64_t>(e0) * E::kBytes;
+                    const unsigned char *ts = static_cast<const unsigned char *>(target) +
+                                              static_cast<int64_t>(r.trow) * g.V * E::kBytes + off;
+                    const unsigned char *dsrc = static_cast<const unsigned char *>(draft) +
+                                                static_cast<int64_t>(r.drow) * g.V * E::kBytes + off;
+                    unsigned char *slot = ring + static_cast<size_t>(islot) * kRSlotBytes;
+                    mbar_arrive_expect_tx(&full[islot], 2 * d.nbytes);
+                    bulk_g2s(slot, ts, d.nbytes, &full[islot]);
+                    bulk_g2s(slot + kSlotBytes, dsrc, d.nbytes, &full[islot]);
+                    ++issued;
+                    if (++islot == ns) {
+                        islot = 0;
+                        iphase ^= 1u;
+                    }
+                }
+                t = tn;
+            }
+            if (ok && issued >= ns) ok = mbar_wait_bounded(&empty[islot], iphase ^ 1u);
+            desc[islot].nbytes = 0;  // end marker (also on time-out, so that consumers leave)
+            mbar_arrive(&full[islot]);
+            if (!ok) {
+                set_status(counters + kStatus, SPEC_ERR_TIMEOUT);
+                for (int i = max(0, issued - ns); i < issued; ++i) mbar_wait_bounded(&full[i % ns], (i / ns) & 1);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------- consumers
+        const int w = warp_id();
+        int slot = 0;
+        uint32_t phase = 0;
+        for (;;) {
+            if (!mbar_wait_bounded(&full[slot], phase)) {
+                set_status(counters + kStatus, SPEC_ERR_TIMEOUT);
+                break;
+            }
+            const RUnit d = desc[slot];
+            if (d.nbytes == 0) break;
+            const unsigned char *sl = ring + static_cast<size_t>(slot) * kRSlotBytes;
+            const uint4 *pt = reinterpret_cast<const uint4 *>(sl) + w * kSubVecs;
+            const uint4 *pd = reinterpret_cast<const uint4 *>(sl + kSlotBytes) + w * kSubVecs;
+            const int nvec = min(kSubVecs, static_cast<int>(d.nbytes >> 4) - w * kSubVecs);  // may be <= 0
+            uint4 xt4[4], xd4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = lane + 32 * j;
+                if (i < nvec) {
+                    xt4[j] = pt[i];
+                    xd4[j] = pd[i];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);  // the slot's data is in registers
+            if (++slot == ns) {
+                slot = 0;
+                phase ^= 1u;
+            }
+            // (a sub-chunk past the row's end has no elements and gets mass 0)
+            // the same operations, in the same order, as the residual pass of
+            // resolve_kernel, so both epilogues give the same masses
+            const float2 c2 = make_float2(d.c, d.c), nlth2 = make_float2(-d.lth, -d.lth);
+            const float2 nltl2 = make_float2(-d.ltl, -d.ltl);
+            const float2 nldh2 = make_float2(-d.ldh, -d.ldh), nldl2 = make_float2(-d.ldl, -d.ldl);
+            float2 acc0 = make_float2(0.0f, 0.0f), acc1 = acc0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (lane + 32 * j >= nvec) continue;
+#pragma unroll
+                for (int p = 0; p < E::kPairs; ++p) {
+                    const float2 w2 =
+                        resid_weight2(E::pair(xt4[j], p), E::pair(xd4[j], p), c2, nlth2, nltl2, nldh2, nldl2);
+                    if (p & 1) acc1 = fadd2(acc1, w2); else acc0 = fadd2(acc0, w2);
+                }
+            }
+            const float sum = warp_sum_f((acc0.x + acc0.y) + (acc1.x + acc1.y));
+            if (lane == 0) resid_part[d.out + w] = sum;
+        }
+    }
+    // the last CTA out resets the ticket counters for the next launch
+    __syncthreads();
+    if (tid == 0 && atomic_add_acq_rel_gpu(counters + kDone, 1) == static_cast<int>(gridDim.x) - 1) {
+        counters[kTicket] = 0;
+        counters[kDone] = 0;
+    }
+}
+
+// The residual draw of the deferred epilogue: one block per listed pair.
+// Warp 0 locates the sub-chunk where the cumulative residual mass crosses
+// u * Z; the block scans its elements (the draw of resolve_kernel's step 3).
+template <int DT>
+__global__ void __launch_bounds__(kDrawThreads) resid_draw_kernel(
+    const void *__restrict__ target, const void *__restrict__ draft, Geometry g,
+    const PairRec *__restrict__ pairs, const float *__restrict__ resid_part, const float2 *__restrict__ part,
+    const int *__restrict__ counters, int32_t *__restrict__ out_tokens, float *__restrict__ aux_resid) {
+    using E = Elem<DT>;
+    __shared__ DrawSmem ds;
+    __shared__ F2 sZ;
+    __shared__ float sM;
+    __shared__ int sok;
+    grid_dependency_wait();
+    const int npairs = __ldcg(counters + kPairs);
+    const int p = blockIdx.x;
+    if (p >= npairs) return;
+    const int lane = lane_id();
+    const PairRec r = pairs[p];
+    if (warp_id() == 0) {
+        const float *rp = resid_part + static_cast<int64_t>(r.b) * g.n_sub;
+        float w[kPartCache];
+#pragma unroll
+        for (int j = 0; j < kPartCache; ++j) w[j] = (lane + 32 * j < g.n_sub) ? __ldcg(rp + lane + 32 * j) : 0.0f;
+        auto wfar = [&](int i) -> float { return __ldcg(rp + i); };
+        F2 before, Z, tgt;
+        const int sc = warp_locate(g.n_sub, w, wfar, r.u, &before, &Z, &tgt);
+        float M = 0.0f, S = 0.0f;
+        bool ok = true;
+        if (sc < 0) ok = warp_combine_soft(part + static_cast<int64_t>(r.trow) * g.n_sub, g.n_sub, &M, &S);
+        if (lane == 0) {
+            ds.sc = sc;
+            ds.before = before;
+            ds.target = tgt;
+            sZ = Z;
+            sM = M;
+            sok = ok;
+        }
+    }
+    __syncthreads();
+    int token = -1;
+    if (ds.sc >= 0) {
+        int a, e1;
+        sub_range(g, ds.sc, &a, &e1);
+        const void *rt = static_cast<const unsigned char *>(target) + static_cast<int64_t>(r.trow) * g.V * E::kBytes;
+        const void *rd = static_cast<const unsigned char *>(draft) + static_cast<int64_t>(r.drow) * g.V * E::kBytes;
+        auto W = [&](float a1, float a2) -> float { return resid_weight(a1, a2, r.c, r.lth, r.ltl, r.ldh, r.ldl); };
+        token = block_scan_elems<DT>(rt, rd, a, e1, W, ds.before, ds.target, ds);
+    } else if (sok) {
+        // every residual weight rounded to 0: p at the position is drawn with
+        // the same uniform instead
+        token = block_draw_row<DT>(target, r.trow, part + static_cast<int64_t>(r.trow) * g.n_sub, g, r.c, sM, r.u, ds);
+    }
+    if (threadIdx.x == 0) {
+        out_tokens[r.trow] = token;
+        if (aux_resid) aux_resid[r.b] = __fadd_rn(sZ.hi, sZ.lo);
     }
 }
 
@@ -467,7 +722,7 @@ bool make_geometry(int V, int dtype, Geometry *g) {
 }
 
 struct WsLayout {
-    size_t part, counters, seqcnt, resid, lse2, total;
+    size_t part, counters, seqcnt, resid, lse2, pairs, total;
 };
 
 // Workspace layout.  The counters block comes first (kStatusOffset).
@@ -486,6 +741,8 @@ WsLayout ws_layout(int B, const Geometry &g) {
     off = align_up(off + static_cast<size_t>(B) * g.n_sub * sizeof(float), 256);
     l.lse2 = off;  // spec_round: the draft rows' lse2 between its two passes
     off = align_up(off + static_cast<size_t>(B) * kMaxK * sizeof(double), 256);
+    l.pairs = off;  // the deferred epilogue's residual pairs
+    off = align_up(off + static_cast<size_t>(B) * sizeof(PairRec), 256);
     l.total = off;
     return l;
 }
@@ -497,6 +754,7 @@ WsPtrs ws_ptrs(void *base, const WsLayout &l) {
     w.counters = reinterpret_cast<int *>(p + l.counters);
     w.seqcnt = reinterpret_cast<int *>(p + l.seqcnt);
     w.resid_part = reinterpret_cast<float *>(p + l.resid);
+    w.pairs = reinterpret_cast<PairRec *>(p + l.pairs);
     return w;
 }
 
@@ -520,10 +778,17 @@ bool set_stats_attrs(int smem_optin) {
                    "cudaFuncSetAttribute(stats_kernel)");
 }
 
+// resid_stream_kernel: up to kResidSlots 32 KB slots.
+constexpr int kResidSlots = 3;
+size_t resid_smem(int ns) { return align_up(ns * (kRSlotBytes + 2 * sizeof(uint64_t) + sizeof(RUnit)), 128); }
+
 template <int DT>
 bool set_stats_attrs_all(int smem_optin) {
     return set_stats_attrs<DT, kModeVerify>(smem_optin) && set_stats_attrs<DT, kModeDraft>(smem_optin) &&
-           set_stats_attrs<DT, kModeTarget>(smem_optin);
+           set_stats_attrs<DT, kModeTarget>(smem_optin) &&
+           cuda_ok(cudaFuncSetAttribute(resid_stream_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(resid_smem(kResidSlots))),
+                   "cudaFuncSetAttribute(resid_stream_kernel)");
 }
 
 DeviceState *device_state(int *dev_out) {
@@ -631,6 +896,16 @@ int check_common(int B, int V, int dtype) {
 #ifndef SPEC_RESOLVE_BLOCKS_PER_SM
 #define SPEC_RESOLVE_BLOCKS_PER_SM 8
 #endif
+// The epilogue's residual pass: inside resolve_kernel (blocks per sequence
+// stream their slices of the two rows, then the last warp draws), or, for
+// batches of at least SPEC_DEFER_MIN_B sequences, deferred: resolve_kernel
+// only decides and lists the rejected positions, resid_stream_kernel streams
+// their rows, resid_draw_kernel draws.
+#ifndef SPEC_DEFER_MIN_B
+#define SPEC_DEFER_MIN_B 128
+#endif
+bool defer_residual(const DeviceState &, int B) { return B >= SPEC_DEFER_MIN_B; }
+
 // resolve_kernel blocks per sequence for n sequences on an idle GPU:
 // 1..kSub, as many as fit one wave of SPEC_RESOLVE_BLOCKS_PER_SM per SM.
 int resolve_split(const DeviceState &st, const Geometry &g, int n) {
@@ -657,7 +932,8 @@ int launch_verify(const void *target, const void *draft, const double *draft_lse
     if (ns == 0) return SPEC_ERR_INVALID_ARG;
     const WsPtrs w = ws_ptrs(ws_base, l);
     const int grid = st.sms * per_sm;
-    const int nsplit = resolve_split(st, g, B);
+    const bool defer = defer_residual(st, B);
+    const int nsplit = defer ? 1 : resolve_split(st, g, B);
     const cudaError_t e1 =
         draft_lse2 ? launch_k(!after_event, stats_kernel<DT, kModeTarget>, dim3(grid), dim3(kThreads), smem, stream,
                               target, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, w.seqcnt,
@@ -668,8 +944,21 @@ int launch_verify(const void *target, const void *draft, const double *draft_lse
     if (!cuda_ok(e1, "launch stats_kernel") ||
         !cuda_ok(launch_k(true, resolve_kernel<DT>, dim3(B * nsplit), dim3(SPEC_RESOLVE_THREADS), 0, stream, target, draft, tokens,
                           u_accept, u_resample, temperature, k_offsets, draft_lse2, B, g, nsplit, w, out_tokens,
-                          out_num, aux),
+                          out_num, aux, defer ? 1 : 0),
                  "launch resolve_kernel"))
+        return SPEC_ERR_CUDA;
+    if (!defer) return SPEC_OK;
+    // deferred epilogue: the listed pairs' rows streamed, then the draws
+    const int rgrid = st.sms * std::max(1, std::min(2, st.smem_per_sm / static_cast<int>(resid_smem(kResidSlots) + 1024)));
+    if (!cuda_ok(launch_k(true, resid_stream_kernel<DT>, dim3(rgrid), dim3(kThreads), resid_smem(kResidSlots), stream,
+                          target, draft, g, kResidSlots, static_cast<const PairRec *>(w.pairs), w.resid_part,
+                          w.counters),
+                 "launch resid_stream_kernel") ||
+        !cuda_ok(launch_k(true, resid_draw_kernel<DT>, dim3(B), dim3(kDrawThreads), 0, stream, target, draft, g,
+                          static_cast<const PairRec *>(w.pairs), static_cast<const float *>(w.resid_part),
+                          static_cast<const float2 *>(w.part), static_cast<const int *>(w.counters), out_tokens,
+                          aux.residual_mass),
+                 "launch resid_draw_kernel"))
         return SPEC_ERR_CUDA;
     return SPEC_OK;
 }

@@ -39,14 +39,29 @@ struct UnitDesc {
 };
 
 // Words of the workspace's counter block.
-// Status word, then stats_kernel's unit tickets and count of CTAs done.
-enum CounterWord : int { kStatus = 1, kTicket = 2, kDone = 3, kCounterWords = 4 };
+// Status word, then the streaming kernels' unit tickets and count of CTAs
+// done, then the number of listed residual pairs (see PairRec).
+enum CounterWord : int { kStatus = 1, kTicket = 2, kDone = 3, kPairs = 4, kCounterWords = 5 };
+
+// A rejected position whose residual is streamed by resid_stream_kernel:
+// written by resolve_kernel (deferred mode), one per rejected sequence, in
+// the order the decisions land.
+struct __align__(16) PairRec {
+    int b;           // sequence
+    int trow, drow;  // target and draft row at the rejected position
+    float c;         // temperature scale log2(e) / T_b
+    float lth, ltl;  // the target row's log2-sum-exp, fp32 hi + lo
+    float ldh, ldl;  // the draft row's
+    float u;         // u_resample at the rejected position
+    int pad[3];
+};
 
 struct WsPtrs {
     float2 *part;        // [rows_cap * n_sub] sub-chunk partials
-    int *counters;       // CounterWord: status, unit tickets and CTAs done
+    int *counters;       // CounterWord: status, unit tickets and CTAs done, pairs
     int *seqcnt;         // [B] resolve_kernel arrivals per sequence
     float *resid_part;   // [B * n_sub] residual mass per sub-chunk
+    PairRec *pairs;      // [B] listed residual pairs (deferred mode)
 };
 
 // ------------------------------------------------------------------ helpers
@@ -230,8 +245,11 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
     // written, so the previous kernel on the stream must have finished
     grid_dependency_wait();
     const bool any_bad = __syncthreads_or(bad);
-    if (MODE == kModeVerify || MODE == kModeTarget)
+    if (MODE == kModeVerify || MODE == kModeTarget) {
         for (int i = blockIdx.x * kThreads + tid; i < B; i += gridDim.x * kThreads) seqcnt[i] = 0;
+        // the epilogue of this call lists its residual pairs from zero
+        if (blockIdx.x == 0 && tid == 0) counters[kPairs] = 0;
+    }
     // the next kernel may be scheduled as soon as SMs free up; it waits for
     // this grid's completion before it reads anything written here
     grid_launch_dependents();
@@ -781,6 +799,127 @@ __device__ int warp_scan_elems(const void *row1, const void *row2, int a, int b,
     if (!pos) return -1;
     const int src = 31 - __clz(pos);
     return a + 4 * PV * src + __shfl_sync(0xffffffffu, lastpos, src);
+}
+
+// Block-level inverse CDF inside elements [a, b) (at most one 2 KB
+// sub-chunk) of one or two rows, by a block of kDrawThreads threads: thread t
+// owns the 8 bytes at element a + t * PE (4 bf16 or 2 fp32 elements; a
+// sub-chunk is 1024 bf16 or 512 fp32 elements, so one group per thread), so
+// each thread holds a contiguous run and the cumulative mass is one block
+// scan.  Weights are W(x_row1, x_row2).  Every thread returns the first
+// element whose cumulative mass, starting at `before`, exceeds `target`;
+// else the last element with positive weight (rounding fallback); else -1.
+// The same rule as warp_scan_elems, with the work spread over 8 warps so
+// that the draw is a few dependent steps long instead of 64.
+constexpr int kDrawThreads = 256;
+struct DrawSmem {
+    float wsum[kDrawThreads / 32];
+    int found, lastpos;
+    int sc;             // located sub-chunk (block_draw_row)
+    F2 before, target;  // its cumulative mass before it, and u * Z
+};
+
+template <int DT, class WF>
+__device__ int block_scan_elems(const void *row1, const void *row2, int a, int b, WF W, F2 before, F2 target,
+                                DrawSmem &ds) {
+    using E = Elem<DT>;
+    constexpr int PE = 8 / E::kBytes;
+    const int t = threadIdx.x, lane = lane_id(), warp = warp_id();
+    const int e0 = a + t * PE;
+    float wv[PE];
+    float tsum = 0.0f;
+    if (t == 0) {
+        ds.found = INT_MAX;
+        ds.lastpos = -1;
+    }
+    if (e0 < b) {
+        const uint2 v1 = __ldg(reinterpret_cast<const uint2 *>(static_cast<const unsigned char *>(row1) +
+                                                             static_cast<int64_t>(e0) * E::kBytes));
+        const uint2 v2 = (row2 != row1) ? __ldg(reinterpret_cast<const uint2 *>(static_cast<const unsigned char *>(row2) +
+                                                                               static_cast<int64_t>(e0) * E::kBytes))
+                                        : v1;
+        float x1[PE], x2[PE];
+        if constexpr (E::kBytes == 2) {
+            x1[0] = __uint_as_float(v1.x << 16);
+            x1[1] = __uint_as_float(v1.x & 0xffff0000u);
+            x1[PE - 2] = __uint_as_float(v1.y << 16);
+            x1[PE - 1] = __uint_as_float(v1.y & 0xffff0000u);
+            x2[0] = __uint_as_float(v2.x << 16);
+            x2[1] = __uint_as_float(v2.x & 0xffff0000u);
+            x2[PE - 2] = __uint_as_float(v2.y << 16);
+            x2[PE - 1] = __uint_as_float(v2.y & 0xffff0000u);
+        } else {
+            x1[0] = __uint_as_float(v1.x);
+            x1[PE - 1] = __uint_as_float(v1.y);
+            x2[0] = __uint_as_float(v2.x);
+            x2[PE - 1] = __uint_as_float(v2.y);
+        }
+#pragma unroll
+        for (int q = 0; q < PE; ++q) {
+            wv[q] = W(x1[q], x2[q]);
+            tsum += wv[q];
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < PE; ++q) wv[q] = 0.0f;
+    }
+    // block exclusive scan of the per-thread sums
+    const float incl = warp_incl_scan_f(tsum);
+    if (lane == 31) ds.wsum[warp] = incl;
+    __syncthreads();
+    float wpre = 0.0f;
+    for (int i = 0; i < warp; ++i) wpre += ds.wsum[i];
+    const F2 start = f2_add(before, wpre + (incl - tsum));
+    const float rem = f2_round_down(f2_sub(target, start));  // acc > rem  <=>  start + acc > target
+    float acc = 0.0f;
+    int found = -1, lastpos = -1;
+#pragma unroll
+    for (int q = 0; q < PE; ++q) {
+        acc += wv[q];
+        if (wv[q] > 0.0f) lastpos = q;
+        if (found < 0 && wv[q] > 0.0f && acc > rem) found = q;
+    }
+    // the cumulative mass only grows, so the earliest crossing is the answer
+    if (found >= 0) atomicMin(&ds.found, e0 + found);
+    if (lastpos >= 0) atomicMax(&ds.lastpos, e0 + lastpos);
+    __syncthreads();
+    const int r = ds.found != INT_MAX ? ds.found : ds.lastpos;
+    __syncthreads();  // ds may be reused right after
+    return r;
+}
+
+// One draw from a soft row by a whole block: warp 0 locates the sub-chunk
+// from the row's partials (as warp_draw_row), then the block scans it.
+// Every thread returns the token.
+template <int DT>
+__device__ int block_draw_row(const void *logits, int64_t row, const float2 *part, const Geometry &g, float c,
+                              float M, float u, DrawSmem &ds) {
+    if (warp_id() == 0) {
+        float2 pc[kPartCache];
+        load_parts(part, g.n_sub, pc);
+        float w[kPartCache];
+#pragma unroll
+        for (int j = 0; j < kPartCache; ++j) w[j] = pc[j].x > -INFINITY ? pc[j].y * ex2(pc[j].x - M) : 0.0f;
+        auto wfar = [&](int i) -> float {
+            const float2 v = __ldcg(part + i);
+            return v.x > -INFINITY ? v.y * ex2(v.x - M) : 0.0f;
+        };
+        F2 before, total, target;
+        const int sc = warp_locate(g.n_sub, w, wfar, u, &before, &total, &target);
+        if (lane_id() == 0) {
+            ds.sc = sc;
+            ds.before = before;
+            ds.target = target;
+        }
+    }
+    __syncthreads();
+    const int sc = ds.sc;
+    if (sc < 0) return -1;
+    int a, b;
+    sub_range(g, sc, &a, &b);
+    const void *rp = static_cast<const unsigned char *>(logits) + row * g.V * static_cast<int64_t>(Elem<DT>::kBytes);
+    auto W = [&](float x, float) -> float { return prob_weight(x, c, M); };
+    return block_scan_elems<DT>(rp, rp, a, b, W, ds.before, ds.target, ds);
 }
 
 // One draw from a soft row (bonus token or draft token) by one warp:
