@@ -260,12 +260,16 @@ __device__ __forceinline__ ArgPart warp_arg(ArgPart p) {
     return p;
 }
 
-// c = log2(e) / T rounded to fp32 (T > 0), 0 for greedy (T == 0), NaN for an
-// invalid temperature.  Every kernel derives the scale the same way.
+// c = log2(e) / T as the fp32 quotient of fp32(log2 e) and T, rounded to
+// nearest (an IEEE division: within an ulp or so of log2(e) / T); 0 for
+// greedy (T == 0); NaN for an invalid temperature.  Every kernel derives the
+// scale the same way.  It is computed in fp32: a stats_kernel CTA derives it
+// for every sequence of the batch in its prologue, and an fp64 division per
+// sequence there took several microseconds per call on GB300's fp64 pipe.
 __device__ __forceinline__ float temp_scale(float T) {
     if (T == 0.0f) return 0.0f;
     if (!(T > 0.0f) || !isfinite(T)) return __int_as_float(0x7fc00000);
-    const float c = static_cast<float>(kLog2eD / static_cast<double>(T));
+    const float c = __fdiv_rn(kLog2e, T);
     return isfinite(c) ? c : __int_as_float(0x7fc00000);
 }
 

@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(SPEC_RESOLVE_THREADS, SPEC_RESOLVE_MIN_BLOCKS)
     const float *__restrict__ u_resample, const float *__restrict__ temperature,
     const int *__restrict__ k_offsets, const double *__restrict__ draft_lse2, int B, Geometry g, int nsplit,
     WsPtrs ws, int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_num, spec_verify_aux_t aux,
-    int defer) {
+    int defer, int inputs_early) {
     using E = Elem<DT>;
     __shared__ ResolveSmem sm;
     const int b = blockIdx.x / nsplit;
@@ -133,22 +133,29 @@ __global__ void __launch_bounds__(SPEC_RESOLVE_THREADS, SPEC_RESOLVE_MIN_BLOCKS)
     int x = 0;
     bool xbad = false;
     float zt = 0.0f, zd = 0.0f, ua = 0.0f, ur = 0.0f;
-    if (warp == 0 && lane <= k) {
-        ur = u_resample[ot + lane];  // lane <= k <= 32 is at most lane 31 here
-        if (lane < k) {
-            x = tokens[od + lane];
-            ua = u_accept[od + lane];
-            xbad = (x < 0 || x >= V);
-            if (!xbad && !greedy && c == c) {
-                zt = E::load1(target, (ot + lane) * V + x);
-                zd = E::load1(draft, (od + lane) * V + x);
-                if (given) sm.Ld[lane] = draft_lse2[od + lane];  // read by warp 0 only
+    // the drafted tokens, their logits, the uniforms and the given draft
+    // normalisers: before the wait when the caller passed them
+    // (inputs_early), after it when the draft pass of the same call wrote them
+    auto load_inputs = [&]() {
+        if (warp == 0 && lane <= k) {
+            ur = u_resample[ot + lane];  // lane <= k <= 32 is at most lane 31 here
+            if (lane < k) {
+                x = tokens[od + lane];
+                ua = u_accept[od + lane];
+                xbad = (x < 0 || x >= V);
+                if (!xbad && !greedy && c == c) {
+                    zt = E::load1(target, (ot + lane) * V + x);
+                    zd = E::load1(draft, (od + lane) * V + x);
+                    if (given) sm.Ld[lane] = draft_lse2[od + lane];  // read by warp 0 only
+                }
             }
         }
-    }
+    };
+    if (inputs_early) load_inputs();
 
     // --- 1. row statistics and the decision -------------------------------
     grid_dependency_wait();
+    if (!inputs_early) load_inputs();
     // (deferred mode: resid_stream_kernel may be scheduled; it waits for this
     // grid before it reads the pair list)
     grid_launch_dependents();
@@ -646,8 +653,12 @@ template <int DT>
 __global__ void __launch_bounds__(256) draft_select_kernel(
     const void *__restrict__ draft, const float *__restrict__ temperature, const float *__restrict__ u_draft,
     const int *__restrict__ k_offsets, int B, Geometry g, const float2 *__restrict__ part,
-    int32_t *__restrict__ out, double *__restrict__ out_lse2, int *__restrict__ counters) {
+    int32_t *__restrict__ out, double *__restrict__ out_lse2, int *__restrict__ counters, int early_trigger) {
     extern __shared__ int s_kofs[];  // [B+1]
+    // spec_round: the target pass may launch at once (it streams rows of its
+    // own while these draws wait for the draft pass, and waits for this grid
+    // before it exits)
+    if (early_trigger) grid_launch_dependents();
     __shared__ int s_bad;
     if (threadIdx.x == 0) s_bad = 0;
     __syncthreads();
@@ -680,7 +691,8 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
             if (s_kofs[mid] <= r) lo = mid; else hi = mid - 1;
         }
         const float c = timed_out ? __int_as_float(0x7fc00000) : temp_scale(temperature[lo]);
-        const float2 *pr = part + static_cast<int64_t>(r) * g.n_sub;
+        // (draft row r's partials are at slot R_t + r, R_t = R + B)
+        const float2 *pr = part + (static_cast<int64_t>(R) + B + r) * g.n_sub;
         int token = -1;
         double L = NAN;
         if (c == 0.0f) {
@@ -915,11 +927,14 @@ int resolve_split(const DeviceState &st, const Geometry &g, int n) {
 // The verify pass: stats_kernel streams the target rows (and, without
 // draft_lse2, the draft rows of sampled sequences), then resolve_kernel.
 // The streaming kernel is launched early behind the stream's previous
-// kernel (programmatic dependent launch).  pdl_first: an earlier kernel of
-// the same call precedes it, so it may read the inputs before its wait;
-// otherwise it opens the call and waits first (the previous kernel may be
-// writing them).  after_event: the stream waits on an event just before
-// (another stream's copy), and the kernel is launched plainly.
+// kernel (programmatic dependent launch).  pdl_first: the draft pass of the
+// same call precedes it (spec_round): the target rows stream at once, while
+// draft_select_kernel still draws (the two use disjoint partial slots), the
+// streaming kernel waits for it only before it exits, and resolve_kernel
+// reads the drafted tokens and normalisers only after its own wait.
+// Otherwise it opens the call and waits first (the previous kernel may be
+// writing the inputs).  after_event: the stream waits on an event just
+// before (another stream's copy), and the kernel is launched plainly.
 template <int DT>
 int launch_verify(const void *target, const void *draft, const double *draft_lse2, const int32_t *tokens,
                   const float *u_accept, const float *u_resample, const float *temperature, int B,
@@ -937,14 +952,14 @@ int launch_verify(const void *target, const void *draft, const double *draft_lse
     const cudaError_t e1 =
         draft_lse2 ? launch_k(!after_event, stats_kernel<DT, kModeTarget>, dim3(grid), dim3(kThreads), smem, stream,
                               target, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, w.seqcnt,
-                              nullptr, nullptr, 0, pdl_first ? 0 : 1)
+                              nullptr, nullptr, 0, pdl_first ? 2 : 1)
                    : launch_k(!after_event, stats_kernel<DT, kModeVerify>, dim3(grid), dim3(kThreads), smem, stream,
                               target, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, w.seqcnt,
-                              nullptr, nullptr, 0, pdl_first ? 0 : 1);
+                              nullptr, nullptr, 0, pdl_first ? 2 : 1);
     if (!cuda_ok(e1, "launch stats_kernel") ||
         !cuda_ok(launch_k(true, resolve_kernel<DT>, dim3(B * nsplit), dim3(SPEC_RESOLVE_THREADS), 0, stream, target, draft, tokens,
                           u_accept, u_resample, temperature, k_offsets, draft_lse2, B, g, nsplit, w, out_tokens,
-                          out_num, aux, defer ? 1 : 0),
+                          out_num, aux, defer ? 1 : 0, pdl_first ? 0 : 1),
                  "launch resolve_kernel"))
         return SPEC_ERR_CUDA;
     if (!defer) return SPEC_OK;
@@ -969,24 +984,29 @@ int launch_verify(const void *target, const void *draft, const double *draft_lse
 template <int DT>
 int launch_draft(const void *draft, const float *temperature, const float *u_draft, int B,
                  const int32_t *k_offsets, const Geometry &g, int32_t *out, double *out_lse2, void *ws_base,
-                 const WsLayout &l, const DeviceState &st, cudaStream_t stream) {
+                 const WsLayout &l, const DeviceState &st, cudaStream_t stream, bool beside_stream = false) {
     int ns, per_sm;
     size_t smem;
     pick_ring(st, B, &ns, &smem, &per_sm);
     if (ns == 0) return SPEC_ERR_INVALID_ARG;
     const WsPtrs w = ws_ptrs(ws_base, l);
-    // one warp per draft row (grid-stride): at most B * kMaxK rows, 8 warps per block
-    const int grid = static_cast<int>(
-        std::min(static_cast<int64_t>(st.sms) * SPEC_SELECT_BLOCKS_PER_SM, (static_cast<int64_t>(B) * kMaxK + 7) / 8));
+    // one warp per draft row (grid-stride): at most B * kMaxK rows, 8 warps
+    // per block.  beside_stream (spec_round): the target pass streams while
+    // the draws run and needs them only at its end, so the draws take one
+    // 4-warp block per SM and leave each SM room for four streaming CTAs
+    const int threads = beside_stream ? 128 : 256;
+    const int grid = beside_stream ? st.sms
+                                   : static_cast<int>(std::min(static_cast<int64_t>(st.sms) * SPEC_SELECT_BLOCKS_PER_SM,
+                                                               (static_cast<int64_t>(B) * kMaxK + 7) / 8));
     // the call's first kernel: launched early behind the stream's previous
     // kernel, it waits for it before reading the inputs (wait_first)
     if (!cuda_ok(launch_k(true, stats_kernel<DT, kModeDraft>, dim3(st.sms * per_sm), dim3(kThreads), smem, stream,
                           draft, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, nullptr, nullptr,
                           nullptr, 0, 1),
                  "launch stats_kernel") ||
-        !cuda_ok(launch_k(true, draft_select_kernel<DT>, dim3(std::max(grid, 1)), dim3(256),
+        !cuda_ok(launch_k(true, draft_select_kernel<DT>, dim3(std::max(grid, 1)), dim3(threads),
                           (B + 1) * sizeof(int), stream, draft, temperature, u_draft, k_offsets, B, g,
-                          static_cast<const float2 *>(w.part), out, out_lse2, w.counters),
+                          static_cast<const float2 *>(w.part), out, out_lse2, w.counters, beside_stream ? 1 : 0),
                  "launch draft_select_kernel"))
         return SPEC_ERR_CUDA;
     return SPEC_OK;
@@ -1111,7 +1131,7 @@ int round_call(const void *target_logits, const void *draft_logits, const float 
     const bool chained = before_verify == nullptr;
     if (dtype == SPEC_F32) {
         rc = launch_draft<SPEC_F32>(draft_logits, temperature, u_draft, B, k_offsets, g, out_draft_tokens, lse2, ws,
-                                    l, *st, s);
+                                    l, *st, s, chained);
         if (rc != SPEC_OK) return rc;
         if (!chained && !cuda_ok(cudaStreamWaitEvent(s, before_verify, 0), "cudaStreamWaitEvent")) return SPEC_ERR_CUDA;
         return launch_verify<SPEC_F32>(target_logits, draft_logits, lse2, out_draft_tokens, u_accept, u_resample,
@@ -1119,7 +1139,7 @@ int round_call(const void *target_logits, const void *draft_logits, const float 
                                        chained, !chained);
     }
     rc = launch_draft<SPEC_BF16>(draft_logits, temperature, u_draft, B, k_offsets, g, out_draft_tokens, lse2, ws, l,
-                                 *st, s);
+                                 *st, s, chained);
     if (rc != SPEC_OK) return rc;
     if (!chained && !cuda_ok(cudaStreamWaitEvent(s, before_verify, 0), "cudaStreamWaitEvent")) return SPEC_ERR_CUDA;
     return launch_verify<SPEC_BF16>(target_logits, draft_logits, lse2, out_draft_tokens, u_accept, u_resample,

@@ -40,8 +40,10 @@ struct UnitDesc {
 
 // Words of the workspace's counter block.
 // Status word, then the streaming kernels' unit tickets and count of CTAs
-// done, then the number of listed residual pairs (see PairRec).
-enum CounterWord : int { kStatus = 1, kTicket = 2, kDone = 3, kPairs = 4, kCounterWords = 5 };
+// done, the number of listed residual pairs (see PairRec), and a second
+// ticket pair for the target pass of spec_round, which streams while the
+// draft pass's kernels may still hold the first.
+enum CounterWord : int { kStatus = 1, kTicket = 2, kDone = 3, kPairs = 4, kTicketB = 5, kDoneB = 6, kCounterWords = 7 };
 
 // A rejected position whose residual is streamed by resid_stream_kernel:
 // written by resolve_kernel (deferred mode), one per rejected sequence, in
@@ -167,9 +169,15 @@ constexpr int kMaxTreeNodes = SPEC_MAX_TREE_NODES;
 //                nodes, then the draft rows of its internal nodes if b is
 //                sampled; nothing for a bad temperature or parent array;
 //   tree-draft:  the draft rows of b's internal nodes.
-// Partials go to slot row r (target row r, and draft rows in draft mode) or
-// R + r (draft row r otherwise), R = R_t in verify mode and the node count
-// N in tree mode; tree-draft mode uses slot r for draft row r.
+// Partials go to slot row r for target row r and R + r for draft row r, with
+// R = R_t in the chain modes (draft rows included, so that a target pass may
+// stream while the draft pass's epilogue still reads its partials) and the
+// node count N in tree mode; tree-draft mode uses slot r for draft row r.
+// wait_first: 1 = the kernel opens its call and waits for the stream's
+// previous kernel before it reads anything; 0 = it reads the call's inputs,
+// then waits before it writes the workspace; 2 = it does not wait until its
+// end (its predecessor in the same call writes nothing it reads or writes,
+// and its completion still implies the predecessor's).
 // Units are taken by tickets (unit_batch).  One lane of warp 8 is the
 // producer: it waits for a free ring slot and issues the bulk copy of the
 // next unit into it.  Warps 0..7 consume: warp w owns the w-th 2 KB
@@ -187,6 +195,8 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
     using E = Elem<DT>;
     constexpr bool DRAFT = MODE == kModeDraft;
     constexpr bool TREE = MODE == kModeTree || MODE == kModeTreeDraft;
+    // unit tickets and CTAs done (the target pass has its own pair)
+    int *tickets = counters + (MODE == kModeTarget ? kTicketB : kTicket);
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)ns * kSlotBytes);
@@ -201,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
     // wait_first: the kernel opens its call and was launched early behind
     // whatever kernel precedes it on the stream, which may still be writing
     // the inputs: wait for it before reading them
-    if (wait_first) grid_dependency_wait();
+    if (wait_first == 1) grid_dependency_wait();
     for (int i = tid; i <= B; i += kThreads) {
         s_kofs[i] = k_offsets[i];
         if (i < B) s_c[i] = temp_scale(temperature[i]);
@@ -243,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
     if (tid == 0) s_rowpre[B] = total_rows;
     // everything above only read the inputs; from here on the workspace is
     // written, so the previous kernel on the stream must have finished
-    grid_dependency_wait();
+    if (wait_first != 2) grid_dependency_wait();
     const bool any_bad = __syncthreads_or(bad);
     if (MODE == kModeVerify || MODE == kModeTarget) {
         for (int i = blockIdx.x * kThreads + tid; i < B; i += gridDim.x * kThreads) seqcnt[i] = 0;
@@ -253,7 +263,10 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
     // the next kernel may be scheduled as soon as SMs free up; it waits for
     // this grid's completion before it reads anything written here
     grid_launch_dependents();
-    if (any_bad) return;
+    if (any_bad) {
+        if (wait_first == 2) grid_dependency_wait();
+        return;
+    }
 
     if (tid == 0) {
         for (int s = 0; s < ns; ++s) {
@@ -279,13 +292,13 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
             int b = 0;
             int islot = 0;
             uint32_t iphase = 0;  // slot and use parity of the next issue
-            int t = atomicAdd(counters + kTicket, 1);
+            int t = atomicAdd(tickets, 1);
             while (ok) {
                 int64_t u0;
                 int cnt;
                 unit_batch(t, n_big, &u0, &cnt);
                 if (u0 >= total_units) break;
-                const int tn = atomicAdd(counters + kTicket, 1);  // next batch, in flight meanwhile
+                const int tn = atomicAdd(tickets, 1);  // next batch, in flight meanwhile
                 cnt = static_cast<int>(min(static_cast<int64_t>(cnt), total_units - u0));
                 int r = static_cast<int>(u0 / g.n_chunks);
                 int ch = static_cast<int>(u0 - static_cast<int64_t>(r) * g.n_chunks);
@@ -317,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
                     } else if (DRAFT) {
                         row = s_kofs[b] + l;
                         base_ptr = draft;
-                        slot_row = row;
+                        slot_row = R_t + row;
                     } else if (l <= k) {
                         row = static_cast<int64_t>(s_kofs[b]) + b + l;
                         base_ptr = target;
@@ -453,10 +466,11 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
     }
     // the last CTA out resets the ticket counters for the next launch on the
     // stream (the library zeroes them once when it allocates a workspace)
+    if (wait_first == 2) grid_dependency_wait();
     __syncthreads();
-    if (tid == 0 && atomic_add_acq_rel_gpu(counters + kDone, 1) == static_cast<int>(gridDim.x) - 1) {
-        counters[kTicket] = 0;
-        counters[kDone] = 0;
+    if (tid == 0 && atomic_add_acq_rel_gpu(tickets + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+        tickets[0] = 0;
+        tickets[1] = 0;
     }
 }
 
