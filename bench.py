@@ -812,18 +812,18 @@ def main():
                         "spec_verify_frac_of_8tbs": gbs(ab["verify"], sep["verify_ms"]) / 8000.0,
                         "spec_draft_sample_ms": sep["draft_ms"]}},
         "roofline": {"bound": "hbm",
-                     "kernel": "spec_round, all six launches (stats_kernel over the draft rows, draft_select_kernel, "
-                               "stats_kernel over the target rows, resolve_kernel, resid_stream_kernel, "
-                               "resid_draw_kernel), timed as the step",
+                     "kernel": "spec_round, all five launches (stats_kernel over the draft rows, draft_select_kernel, "
+                               "stats_kernel over the target rows, decide_stream_kernel, resid_draw_kernel), "
+                               "timed as the step",
                      "achieved": step_gbs, "peak": peak, "unit": "GB/s",
                      "frac": step_gbs / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": measured_traffic(w.name), "algorithmic_bytes_per_launch": step_bytes,
-                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the round's six "
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the round's five "
                                        "kernels, one capture per kernel (profiles/, null unless taken with the "
                                        "current kernel sources)"},
         # per step (spec_round on B=512): stats_kernel + draft_select_kernel, stats_kernel +
-        # resolve_kernel + resid_stream_kernel + resid_draw_kernel
-        "gpu_launches": 6 * args.steps,
+        # decide_stream_kernel + resid_draw_kernel
+        "gpu_launches": 5 * args.steps,
         "cpu_baseline": cpu,
         "parity": parity,
         "e2e": e2e_line,

@@ -98,6 +98,19 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v) {
     return old;
 }
 
+// Release-add and release-store at GPU scope, acquire-load at GPU scope.
+__device__ __forceinline__ void red_add_release_gpu(int *p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_release_gpu(int *p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Hardware base-2 exponential (MUFU.EX2): ~2 ulp, subnormal results flushed
 // to zero, ex2(-inf) = 0, ex2(NaN) = NaN.
 __device__ __forceinline__ float ex2(float x) {

@@ -18,6 +18,7 @@ struct DeviceState {
     int sms = 0;
     int smem_per_sm = 0;
     int smem_optin = 0;
+    int fuse_per_sm[2] = {0, 0};  // resident decide_stream_kernel CTAs per SM, by dtype
     void *ws = nullptr;
     size_t ws_bytes = 0;
     void *stage = nullptr;

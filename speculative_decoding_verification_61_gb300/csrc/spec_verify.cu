@@ -83,18 +83,17 @@ struct ResolveSmem {
 #ifndef SPEC_RESOLVE_MIN_BLOCKS
 #define SPEC_RESOLVE_MIN_BLOCKS 4
 #endif
+// One block's part of the epilogue for sequence b (slice s of nsplit); the
+// body of resolve_kernel, and the decision phase of decide_stream_kernel.
 template <int DT>
-__global__ void __launch_bounds__(SPEC_RESOLVE_THREADS, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
+__device__ __forceinline__ void resolve_block(
     const void *__restrict__ target, const void *__restrict__ draft,
     const int32_t *__restrict__ tokens, const float *__restrict__ u_accept,
     const float *__restrict__ u_resample, const float *__restrict__ temperature,
-    const int *__restrict__ k_offsets, const double *__restrict__ draft_lse2, int B, Geometry g, int nsplit,
-    WsPtrs ws, int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_num, spec_verify_aux_t aux,
-    int defer, int inputs_early) {
+    const int *__restrict__ k_offsets, const double *__restrict__ draft_lse2, int B, const Geometry &g, int nsplit,
+    const WsPtrs &ws, int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_num,
+    const spec_verify_aux_t &aux, int defer, int inputs_early, int b, int s, ResolveSmem &sm) {
     using E = Elem<DT>;
-    __shared__ ResolveSmem sm;
-    const int b = blockIdx.x / nsplit;
-    const int s = blockIdx.x - b * nsplit;
     const int lane = lane_id(), warp = warp_id();
 
     // --- inputs only (written before this call) --------------------------
@@ -303,8 +302,9 @@ __global__ void __launch_bounds__(SPEC_RESOLVE_THREADS, SPEC_RESOLVE_MIN_BLOCKS)
 
     const int64_t drow = od + n;
     if (defer) {
-        // deferred: list the pair; resid_stream_kernel streams its two rows
-        // and resid_draw_kernel draws (nsplit is 1 in this mode)
+        // deferred: list the pair; resid_stream_kernel (or the stream phase
+        // of decide_stream_kernel) streams its two rows and resid_draw_kernel
+        // draws (nsplit is 1 in this mode)
         if (threadIdx.x == 0) {
             PairRec r{};
             r.b = b;
@@ -316,7 +316,12 @@ __global__ void __launch_bounds__(SPEC_RESOLVE_THREADS, SPEC_RESOLVE_MIN_BLOCKS)
             r.ldh = sm.ldh;
             r.ldl = sm.ldl;
             r.u = sm.u;
-            ws.pairs[atomicAdd(ws.counters + kPairs, 1)] = r;
+            r.ready = 0;
+            r.t0 = static_cast<int>(ot);
+            r.k = k;
+            PairRec *dst = ws.pairs + atomicAdd(ws.counters + kPairs, 1);
+            *dst = r;
+            st_release_gpu(&dst->ready, 1);  // the residual stream may take it now
         }
         return;
     }
@@ -419,6 +424,20 @@ __global__ void __launch_bounds__(SPEC_RESOLVE_THREADS, SPEC_RESOLVE_MIN_BLOCKS)
     }
 }
 
+template <int DT>
+__global__ void __launch_bounds__(SPEC_RESOLVE_THREADS, SPEC_RESOLVE_MIN_BLOCKS) resolve_kernel(
+    const void *__restrict__ target, const void *__restrict__ draft,
+    const int32_t *__restrict__ tokens, const float *__restrict__ u_accept,
+    const float *__restrict__ u_resample, const float *__restrict__ temperature,
+    const int *__restrict__ k_offsets, const double *__restrict__ draft_lse2, int B, Geometry g, int nsplit,
+    WsPtrs ws, int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_num, spec_verify_aux_t aux,
+    int defer, int inputs_early) {
+    __shared__ ResolveSmem sm;
+    const int b = blockIdx.x / nsplit;
+    resolve_block<DT>(target, draft, tokens, u_accept, u_resample, temperature, k_offsets, draft_lse2, B, g, nsplit,
+                      ws, out_tokens, out_num, aux, defer, inputs_early, b, blockIdx.x - b * nsplit, sm);
+}
+
 // ================================================================== kernel 3
 // The residual pass of the deferred epilogue, as a stream: every listed pair
 // (the target and the draft row at a rejected position) is cut into units
@@ -437,37 +456,171 @@ struct RUnit {
     int64_t out;      // index of the unit's first sub-chunk mass in resid_part
 };
 
+// A streaming CTA's residual ring: ns slots of a target chunk and the
+// draft chunk at the same place, their full/empty barriers and descriptors.
+struct RRing {
+    unsigned char *ring;
+    uint64_t *full, *empty;
+    RUnit *desc;
+    int ns;
+};
+__device__ __forceinline__ RRing rring_carve(unsigned char *smem, int ns) {
+    RRing q;
+    q.ring = smem;
+    q.full = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(ns) * kRSlotBytes);
+    q.empty = q.full + ns;
+    q.desc = reinterpret_cast<RUnit *>(q.empty + ns);
+    q.ns = ns;
+    return q;
+}
+// (thread 0; a barrier must follow before other threads use the ring)
+__device__ __forceinline__ void rring_init(const RRing &q) {
+    for (int i = 0; i < q.ns; ++i) {
+        mbar_init(&q.full[i], 1);
+        mbar_init(&q.empty[i], kConsumerWarps);
+    }
+    fence_barrier_init();
+}
+
+// Producer state of a ring (lane 0 of the producer warp).
+struct RProd {
+    int slot = 0, issued = 0;
+    uint32_t phase = 0;
+};
+
+// Issue unit (pair r, chunk ch): wait for a free slot, write its
+// descriptor, copy the two chunks.  False when the wait for a slot timed out.
+template <int DT>
+__device__ __forceinline__ bool rring_push(const RRing &q, RProd &st, const PairRec &r, int ch, const void *target,
+                                           const void *draft, const Geometry &g) {
+    using E = Elem<DT>;
+    if (st.issued >= q.ns && !mbar_wait_bounded(&q.empty[st.slot], st.phase ^ 1u)) return false;
+    const int e0 = ch * g.chunk_elems;
+    const int e1 = min(g.V, e0 + g.chunk_elems);
+    RUnit d;
+    d.nbytes = static_cast<uint32_t>(e1 - e0) * E::kBytes;
+    d.c = r.c;
+    d.lth = r.lth;
+    d.ltl = r.ltl;
+    d.ldh = r.ldh;
+    d.ldl = r.ldl;
+    d.out = static_cast<int64_t>(r.b) * g.n_sub + static_cast<int64_t>(ch) * kSub;
+    q.desc[st.slot] = d;
+    const int64_t off = static_cast<int64_t>(e0) * E::kBytes;
+    const unsigned char *ts =
+        static_cast<const unsigned char *>(target) + static_cast<int64_t>(r.trow) * g.V * E::kBytes + off;
+    const unsigned char *dsrc =
+        static_cast<const unsigned char *>(draft) + static_cast<int64_t>(r.drow) * g.V * E::kBytes + off;
+    unsigned char *slot = q.ring + static_cast<size_t>(st.slot) * kRSlotBytes;
+    mbar_arrive_expect_tx(&q.full[st.slot], 2 * d.nbytes);
+    bulk_g2s(slot, ts, d.nbytes, &q.full[st.slot]);
+    bulk_g2s(slot + kSlotBytes, dsrc, d.nbytes, &q.full[st.slot]);
+    ++st.issued;
+    if (++st.slot == q.ns) {
+        st.slot = 0;
+        st.phase ^= 1u;
+    }
+    return true;
+}
+
+// Close the ring: the end marker (also after a time-out, so that the
+// consumers leave), and on a time-out the status word, after the copies in
+// flight have landed.
+__device__ __forceinline__ void rring_close(const RRing &q, const RProd &st, bool ok, int *counters) {
+    if (ok && st.issued >= q.ns) ok = mbar_wait_bounded(&q.empty[st.slot], st.phase ^ 1u);
+    q.desc[st.slot].nbytes = 0;
+    mbar_arrive(&q.full[st.slot]);
+    if (!ok) {
+        set_status(counters + kStatus, SPEC_ERR_TIMEOUT);
+        for (int i = max(0, st.issued - q.ns); i < st.issued; ++i) mbar_wait_bounded(&q.full[i % q.ns], (i / q.ns) & 1);
+    }
+}
+
+// Consumer warps: each sums max(0, p - q) over its 2 KB sub-chunk of every
+// unit until the end marker, and stores that mass.
+template <int DT>
+__device__ __forceinline__ void rring_consume(const RRing &q, float *__restrict__ resid_part, int *counters) {
+    using E = Elem<DT>;
+    const int w = warp_id(), lane = lane_id();
+    int slot = 0;
+    uint32_t phase = 0;
+    for (;;) {
+        if (!mbar_wait_bounded(&q.full[slot], phase)) {
+            set_status(counters + kStatus, SPEC_ERR_TIMEOUT);
+            break;
+        }
+        const RUnit d = q.desc[slot];
+        if (d.nbytes == 0) break;
+        const unsigned char *sl = q.ring + static_cast<size_t>(slot) * kRSlotBytes;
+        const uint4 *pt = reinterpret_cast<const uint4 *>(sl) + w * kSubVecs;
+        const uint4 *pd = reinterpret_cast<const uint4 *>(sl + kSlotBytes) + w * kSubVecs;
+        const int nvec = min(kSubVecs, static_cast<int>(d.nbytes >> 4) - w * kSubVecs);  // may be <= 0
+        uint4 xt4[4], xd4[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = lane + 32 * j;
+            if (i < nvec) {
+                xt4[j] = pt[i];
+                xd4[j] = pd[i];
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q.empty[slot]);  // the slot's data is in registers
+        if (++slot == q.ns) {
+            slot = 0;
+            phase ^= 1u;
+        }
+        // (a sub-chunk past the row's end has no elements and gets mass 0)
+        // the same operations, in the same order, as the residual pass of
+        // resolve_kernel, so both epilogues give the same masses
+        const float2 c2 = make_float2(d.c, d.c), nlth2 = make_float2(-d.lth, -d.lth);
+        const float2 nltl2 = make_float2(-d.ltl, -d.ltl);
+        const float2 nldh2 = make_float2(-d.ldh, -d.ldh), nldl2 = make_float2(-d.ldl, -d.ldl);
+        float2 acc0 = make_float2(0.0f, 0.0f), acc1 = acc0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (lane + 32 * j >= nvec) continue;
+#pragma unroll
+            for (int p = 0; p < E::kPairs; ++p) {
+                const float2 w2 =
+                    resid_weight2(E::pair(xt4[j], p), E::pair(xd4[j], p), c2, nlth2, nltl2, nldh2, nldl2);
+                if (p & 1) acc1 = fadd2(acc1, w2); else acc0 = fadd2(acc0, w2);
+            }
+        }
+        const float sum = warp_sum_f((acc0.x + acc0.y) + (acc1.x + acc1.y));
+        if (lane == 0) resid_part[d.out + w] = sum;
+    }
+}
+
+// The last CTA out resets the ticket counters for the next launch.
+__device__ __forceinline__ void rring_retire(int *counters) {
+    __syncthreads();
+    if (threadIdx.x == 0 && atomic_add_acq_rel_gpu(counters + kDone, 1) == static_cast<int>(gridDim.x) - 1) {
+        counters[kTicket] = 0;
+        counters[kDone] = 0;
+    }
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 2) resid_stream_kernel(
     const void *__restrict__ target, const void *__restrict__ draft, Geometry g, int ns,
     const PairRec *__restrict__ pairs, float *__restrict__ resid_part, int *__restrict__ counters) {
-    using E = Elem<DT>;
     extern __shared__ __align__(128) unsigned char smem[];
-    unsigned char *ring = smem;
-    uint64_t *full = reinterpret_cast<uint64_t *>(ring + static_cast<size_t>(ns) * kRSlotBytes);
-    uint64_t *empty = full + ns;
-    RUnit *desc = reinterpret_cast<RUnit *>(empty + ns);
-    const int tid = threadIdx.x, lane = lane_id();
+    const RRing q = rring_carve(smem, ns);
     // the pair list is complete once resolve_kernel has finished
     grid_dependency_wait();
     grid_launch_dependents();
     const int npairs = __ldcg(counters + kPairs);
-    if (tid == 0) {
-        for (int i = 0; i < ns; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kConsumerWarps);
-        }
-        fence_barrier_init();
-    }
+    if (threadIdx.x == 0) rring_init(q);
     __syncthreads();
     if (warp_id() == kConsumerWarps) {
         // ------------------------------------------------------ producer
-        if (lane == 0) {
+        if (lane_id() == 0) {
             const int64_t total_units = static_cast<int64_t>(npairs) * g.n_chunks;
             const int64_t n_big = big_batches(total_units, gridDim.x);
-            int issued = 0, islot = 0, cur = -1;
-            uint32_t iphase = 0;
+            RProd st;
             bool ok = true;
+            int cur = -1;
             PairRec r{};
             int t = atomicAdd(counters + kTicket, 1);
             while (ok) {
@@ -477,113 +630,120 @@ __global__ void __launch_bounds__(kThreads, 2) resid_stream_kernel(
                 if (u0 >= total_units) break;
                 const int tn = atomicAdd(counters + kTicket, 1);  // next batch, in flight meanwhile
                 cnt = static_cast<int>(min(static_cast<int64_t>(cnt), total_units - u0));
-                for (int q = 0; q < cnt; ++q) {
-                    const int64_t u = u0 + q;
+                for (int qi = 0; qi < cnt && ok; ++qi) {
+                    const int64_t u = u0 + qi;
                     const int p = static_cast<int>(u / g.n_chunks);
-                    const int ch = static_cast<int>(u - static_cast<int64_t>(p) * g.n_chunks);
                     if (p != cur) {
                         r = pairs[p];
                         cur = p;
                     }
-                    if (issued >= ns && !mbar_wait_bounded(&empty[islot], iphase ^ 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    const int e0 = ch * g.chunk_elems;
-                    const int e1 = min(g.V, e0 + g.chunk_elems);
-                    RUnit d;
-                    d.nbytes = static_cast<uint32_t>(e1 - e0) * E::kBytes;
-                    d.c = r.c;
-                    d.lth = r.lth;
-                    d.ltl = r.ltl;
-                    d.ldh = r.ldh;
-                    d.ldl = r.ldl;
-                    d.out = static_cast<int64_t>(r.b) * g.n_sub + static_cast<int64_t>(ch) * kSub;
-                    desc[islot] = d;
-                    const int64_t off = static_cast<int64_t>(e0) * E::kBytes;
-                    const unsigned char *ts = static_cast<const unsigned char *>(target) +
-                                              static_cast<int64_t>(r.trow) * g.V * E::kBytes + off;
-                    const unsigned char *dsrc = static_cast<const unsigned char *>(draft) +
-                                                static_cast<int64_t>(r.drow) * g.V * E::kBytes + off;
-                    unsigned char *slot = ring + static_cast<size_t>(islot) * kRSlotBytes;
-                    mbar_arrive_expect_tx(&full[islot], 2 * d.nbytes);
-                    bulk_g2s(slot, ts, d.nbytes, &full[islot]);
-                    bulk_g2s(slot + kSlotBytes, dsrc, d.nbytes, &full[islot]);
-                    ++issued;
-                    if (++islot == ns) {
-                        islot = 0;
-                        iphase ^= 1u;
-                    }
+                    ok = rring_push<DT>(q, st, r, static_cast<int>(u - static_cast<int64_t>(p) * g.n_chunks), target,
+                                        draft, g);
                 }
                 t = tn;
             }
-            if (ok && issued >= ns) ok = mbar_wait_bounded(&empty[islot], iphase ^ 1u);
-            desc[islot].nbytes = 0;  // end marker (also on time-out, so that consumers leave)
-            mbar_arrive(&full[islot]);
-            if (!ok) {
-                set_status(counters + kStatus, SPEC_ERR_TIMEOUT);
-                for (int i = max(0, issued - ns); i < issued; ++i) mbar_wait_bounded(&full[i % ns], (i / ns) & 1);
-            }
+            rring_close(q, st, ok, counters);
         }
         __syncwarp();
     } else {
-        // ---------------------------------------------------------- consumers
-        const int w = warp_id();
-        int slot = 0;
-        uint32_t phase = 0;
-        for (;;) {
-            if (!mbar_wait_bounded(&full[slot], phase)) {
-                set_status(counters + kStatus, SPEC_ERR_TIMEOUT);
-                break;
-            }
-            const RUnit d = desc[slot];
-            if (d.nbytes == 0) break;
-            const unsigned char *sl = ring + static_cast<size_t>(slot) * kRSlotBytes;
-            const uint4 *pt = reinterpret_cast<const uint4 *>(sl) + w * kSubVecs;
-            const uint4 *pd = reinterpret_cast<const uint4 *>(sl + kSlotBytes) + w * kSubVecs;
-            const int nvec = min(kSubVecs, static_cast<int>(d.nbytes >> 4) - w * kSubVecs);  // may be <= 0
-            uint4 xt4[4], xd4[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int i = lane + 32 * j;
-                if (i < nvec) {
-                    xt4[j] = pt[i];
-                    xd4[j] = pd[i];
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);  // the slot's data is in registers
-            if (++slot == ns) {
-                slot = 0;
-                phase ^= 1u;
-            }
-            // (a sub-chunk past the row's end has no elements and gets mass 0)
-            // the same operations, in the same order, as the residual pass of
-            // resolve_kernel, so both epilogues give the same masses
-            const float2 c2 = make_float2(d.c, d.c), nlth2 = make_float2(-d.lth, -d.lth);
-            const float2 nltl2 = make_float2(-d.ltl, -d.ltl);
-            const float2 nldh2 = make_float2(-d.ldh, -d.ldh), nldl2 = make_float2(-d.ldl, -d.ldl);
-            float2 acc0 = make_float2(0.0f, 0.0f), acc1 = acc0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (lane + 32 * j >= nvec) continue;
-#pragma unroll
-                for (int p = 0; p < E::kPairs; ++p) {
-                    const float2 w2 =
-                        resid_weight2(E::pair(xt4[j], p), E::pair(xd4[j], p), c2, nlth2, nltl2, nldh2, nldl2);
-                    if (p & 1) acc1 = fadd2(acc1, w2); else acc0 = fadd2(acc0, w2);
-                }
-            }
-            const float sum = warp_sum_f((acc0.x + acc0.y) + (acc1.x + acc1.y));
-            if (lane == 0) resid_part[d.out + w] = sum;
-        }
+        rring_consume<DT>(q, resid_part, counters);
     }
-    // the last CTA out resets the ticket counters for the next launch
+    rring_retire(counters);
+}
+
+// Units (consecutive chunks of one pair) per ticket of decide_stream_kernel:
+// one ticket, and one check of the pair's flag, per SPEC_FUSE_UNITS copies.
+// Measured on B=256: 1 unit 176.3 µs, 2-4 units 173.2-174.1 µs per verify.
+#ifndef SPEC_FUSE_UNITS
+#define SPEC_FUSE_UNITS 3
+#endif
+// The deferred epilogue's decisions and residual stream in one launch (for
+// B at most twice the grid).  Each CTA first decides its sequences
+// (b = blockIdx.x, blockIdx.x + gridDim.x, ...) as resolve_kernel does in
+// deferred mode: a rejected position's pair is listed with a ready flag
+// (release), and every decided sequence is counted (release, after its
+// pair).  Then the CTA streams units of listed pairs, SPEC_FUSE_UNITS
+// chunks of one pair per ticket, in the order of the list: the producer
+// waits (acquire) until the ticket's pair is ready, and leaves once every
+// sequence is decided and the ticket lies past the list.  The first pairs
+// stream while later ones are still being decided, and no launch boundary
+// lies between decision and stream.  A CTA may wait on pairs that another
+// lists, so the grid never exceeds the CTAs that are resident at once (the
+// occupancy the host queries); should another kernel hold SMs for longer
+// than the bounded wait (2 s), the call reports a time-out, not a hang.
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 2) decide_stream_kernel(
+    const void *__restrict__ target, const void *__restrict__ draft,
+    const int32_t *__restrict__ tokens, const float *__restrict__ u_accept,
+    const float *__restrict__ u_resample, const float *__restrict__ temperature,
+    const int *__restrict__ k_offsets, const double *__restrict__ draft_lse2, int B, Geometry g, WsPtrs ws,
+    int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_num, spec_verify_aux_t aux, int inputs_early,
+    int ns) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ ResolveSmem sm;
+    const RRing q = rring_carve(smem, ns);
+    int *counters = ws.counters;
+    if (threadIdx.x == 0) rring_init(q);
+    // ------------------------------------------------------------ decisions
+    for (int b = blockIdx.x; b < B; b += gridDim.x) {
+        resolve_block<DT>(target, draft, tokens, u_accept, u_resample, temperature, k_offsets, draft_lse2, B, g, 1, ws,
+                          out_tokens, out_num, aux, 1, inputs_early && b == static_cast<int>(blockIdx.x), b, 0, sm);
+        __syncthreads();  // (thread 0 listed the pair, if any, before this)
+        if (threadIdx.x == 0) red_add_release_gpu(counters + kDecided, 1);
+    }
+    grid_dependency_wait();  // (a CTA without a sequence)
+    grid_launch_dependents();
     __syncthreads();
-    if (tid == 0 && atomic_add_acq_rel_gpu(counters + kDone, 1) == static_cast<int>(gridDim.x) - 1) {
-        counters[kTicket] = 0;
-        counters[kDone] = 0;
+    // ------------------------------------------------------------ residual stream
+    if (warp_id() == kConsumerWarps) {
+        if (lane_id() == 0) {
+            RProd st;
+            bool ok = true;
+            int cur = -1;
+            PairRec r{};
+            const int per = (g.n_chunks + SPEC_FUSE_UNITS - 1) / SPEC_FUSE_UNITS;  // tickets per pair
+            int t = atomicAdd(counters + kTicket, 1);
+            while (ok) {
+                const int p = t / per;
+                const int tn = atomicAdd(counters + kTicket, 1);  // the next ticket, in flight meanwhile
+                if (p != cur) {
+                    // wait for pair p: listed and ready, or never listed
+                    bool listed = false;
+                    const uint64_t t0 = global_timer_ns();
+                    for (;;) {
+                        int np = ld_acquire_gpu(counters + kPairs);
+                        if (p < np && ld_acquire_gpu(&ws.pairs[p].ready)) {
+                            listed = true;
+                            break;
+                        }
+                        if (p >= np && ld_acquire_gpu(counters + kDecided) >= B) {
+                            // every listing precedes its sequence's count
+                            np = ld_acquire_gpu(counters + kPairs);
+                            if (p >= np) break;
+                            continue;
+                        }
+                        if (global_timer_ns() - t0 > kWaitLimitNs) {
+                            ok = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    if (!listed) break;
+                    r = ws.pairs[p];
+                    cur = p;
+                }
+                const int c0 = (t - p * per) * SPEC_FUSE_UNITS;
+                const int c1 = min(g.n_chunks, c0 + SPEC_FUSE_UNITS);
+                for (int ch = c0; ch < c1 && ok; ++ch) ok = rring_push<DT>(q, st, r, ch, target, draft, g);
+                t = tn;
+            }
+            rring_close(q, st, ok, counters);
+        }
+        __syncwarp();
+    } else {
+        rring_consume<DT>(q, ws.resid_part, counters);
     }
+    rring_retire(counters);
 }
 
 // The residual draw of the deferred epilogue: one block per listed pair.
@@ -593,7 +753,8 @@ template <int DT>
 __global__ void __launch_bounds__(kDrawThreads) resid_draw_kernel(
     const void *__restrict__ target, const void *__restrict__ draft, Geometry g,
     const PairRec *__restrict__ pairs, const float *__restrict__ resid_part, const float2 *__restrict__ part,
-    const int *__restrict__ counters, int32_t *__restrict__ out_tokens, float *__restrict__ aux_resid) {
+    const int *__restrict__ counters, int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_num,
+    float *__restrict__ aux_resid) {
     using E = Elem<DT>;
     __shared__ DrawSmem ds;
     __shared__ F2 sZ;
@@ -605,6 +766,16 @@ __global__ void __launch_bounds__(kDrawThreads) resid_draw_kernel(
     if (p >= npairs) return;
     const int lane = lane_id();
     const PairRec r = pairs[p];
+    if (__ldcg(counters + kStatus) == SPEC_ERR_TIMEOUT) {
+        // the residual stream gave up: masses of unknown age, so the
+        // sequence is a data error, not a draw that looks valid
+        for (int i = threadIdx.x; i <= r.k; i += blockDim.x) out_tokens[r.t0 + i] = -1;
+        if (threadIdx.x == 0) {
+            out_num[r.b] = -1;
+            if (aux_resid) aux_resid[r.b] = NAN;
+        }
+        return;
+    }
     if (warp_id() == 0) {
         const float *rp = resid_part + static_cast<int64_t>(r.b) * g.n_sub;
         float w[kPartCache];
@@ -795,12 +966,17 @@ constexpr int kResidSlots = 3;
 size_t resid_smem(int ns) { return align_up(ns * (kRSlotBytes + 2 * sizeof(uint64_t) + sizeof(RUnit)), 128); }
 
 template <int DT>
-bool set_stats_attrs_all(int smem_optin) {
-    return set_stats_attrs<DT, kModeVerify>(smem_optin) && set_stats_attrs<DT, kModeDraft>(smem_optin) &&
-           set_stats_attrs<DT, kModeTarget>(smem_optin) &&
-           cuda_ok(cudaFuncSetAttribute(resid_stream_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(resid_smem(kResidSlots))),
-                   "cudaFuncSetAttribute(resid_stream_kernel)");
+bool set_stats_attrs_all(DeviceState &st) {
+    const int rs = static_cast<int>(resid_smem(kResidSlots));
+    return set_stats_attrs<DT, kModeVerify>(st.smem_optin) && set_stats_attrs<DT, kModeDraft>(st.smem_optin) &&
+           set_stats_attrs<DT, kModeTarget>(st.smem_optin) &&
+           cuda_ok(cudaFuncSetAttribute(resid_stream_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, rs),
+                   "cudaFuncSetAttribute(resid_stream_kernel)") &&
+           cuda_ok(cudaFuncSetAttribute(decide_stream_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, rs),
+                   "cudaFuncSetAttribute(decide_stream_kernel)") &&
+           cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&st.fuse_per_sm[DT == SPEC_F32 ? 0 : 1],
+                                                                 decide_stream_kernel<DT>, kThreads, rs),
+                   "cudaOccupancyMaxActiveBlocksPerMultiprocessor(decide_stream_kernel)");
 }
 
 DeviceState *device_state(int *dev_out) {
@@ -815,7 +991,7 @@ DeviceState *device_state(int *dev_out) {
             !cuda_ok(cudaDeviceGetAttribute(&st.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
                      "cudaDeviceGetAttribute"))
             return nullptr;
-        if (!set_stats_attrs_all<SPEC_F32>(st.smem_optin) || !set_stats_attrs_all<SPEC_BF16>(st.smem_optin))
+        if (!set_stats_attrs_all<SPEC_F32>(st) || !set_stats_attrs_all<SPEC_BF16>(st))
             return nullptr;
         st.smem_optin -= 1024;  // headroom for the kernels' static shared memory
         st.init = true;
@@ -918,6 +1094,18 @@ int check_common(int B, int V, int dtype) {
 #endif
 bool defer_residual(const DeviceState &, int B) { return B >= SPEC_DEFER_MIN_B; }
 
+// Deferred epilogues of at most SPEC_FUSE_PER_CTA sequences per resident
+// CTA take decide_stream_kernel (decisions and residual stream in one
+// launch); larger ones resolve_kernel, then resid_stream_kernel.
+#ifndef SPEC_FUSE_PER_CTA
+#define SPEC_FUSE_PER_CTA 2
+#endif
+template <int DT>
+int fuse_grid(const DeviceState &st, int B) {
+    const int g = st.sms * std::min(2, st.fuse_per_sm[DT == SPEC_F32 ? 0 : 1]);
+    return (g > 0 && B <= SPEC_FUSE_PER_CTA * g) ? g : 0;
+}
+
 // resolve_kernel blocks per sequence for n sequences on an idle GPU:
 // 1..kSub, as many as fit one wave of SPEC_RESOLVE_BLOCKS_PER_SM per SM.
 int resolve_split(const DeviceState &st, const Geometry &g, int n) {
@@ -952,12 +1140,19 @@ int launch_verify(const void *target, const void *draft, const double *draft_lse
     const cudaError_t e1 =
         draft_lse2 ? launch_k(!after_event, stats_kernel<DT, kModeTarget>, dim3(grid), dim3(kThreads), smem, stream,
                               target, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, w.seqcnt,
-                              nullptr, nullptr, 0, pdl_first ? 2 : 1)
+                              nullptr, nullptr, 0, pdl_first ? 2 : 1, w.pairs)
                    : launch_k(!after_event, stats_kernel<DT, kModeVerify>, dim3(grid), dim3(kThreads), smem, stream,
                               target, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, w.seqcnt,
-                              nullptr, nullptr, 0, pdl_first ? 2 : 1);
-    if (!cuda_ok(e1, "launch stats_kernel") ||
-        !cuda_ok(launch_k(true, resolve_kernel<DT>, dim3(B * nsplit), dim3(SPEC_RESOLVE_THREADS), 0, stream, target, draft, tokens,
+                              nullptr, nullptr, 0, pdl_first ? 2 : 1, w.pairs);
+    if (!cuda_ok(e1, "launch stats_kernel")) return SPEC_ERR_CUDA;
+    const int fgrid = defer ? fuse_grid<DT>(st, B) : 0;
+    if (fgrid > 0) {
+        if (!cuda_ok(launch_k(true, decide_stream_kernel<DT>, dim3(fgrid), dim3(kThreads), resid_smem(kResidSlots), stream,
+                              target, draft, tokens, u_accept, u_resample, temperature, k_offsets, draft_lse2, B, g, w,
+                              out_tokens, out_num, aux, pdl_first ? 0 : 1, kResidSlots),
+                     "launch decide_stream_kernel"))
+            return SPEC_ERR_CUDA;
+    } else if (!cuda_ok(launch_k(true, resolve_kernel<DT>, dim3(B * nsplit), dim3(SPEC_RESOLVE_THREADS), 0, stream, target, draft, tokens,
                           u_accept, u_resample, temperature, k_offsets, draft_lse2, B, g, nsplit, w, out_tokens,
                           out_num, aux, defer ? 1 : 0, pdl_first ? 0 : 1),
                  "launch resolve_kernel"))
@@ -965,14 +1160,14 @@ int launch_verify(const void *target, const void *draft, const double *draft_lse
     if (!defer) return SPEC_OK;
     // deferred epilogue: the listed pairs' rows streamed, then the draws
     const int rgrid = st.sms * std::max(1, std::min(2, st.smem_per_sm / static_cast<int>(resid_smem(kResidSlots) + 1024)));
-    if (!cuda_ok(launch_k(true, resid_stream_kernel<DT>, dim3(rgrid), dim3(kThreads), resid_smem(kResidSlots), stream,
+    if ((fgrid == 0 && !cuda_ok(launch_k(true, resid_stream_kernel<DT>, dim3(rgrid), dim3(kThreads), resid_smem(kResidSlots), stream,
                           target, draft, g, kResidSlots, static_cast<const PairRec *>(w.pairs), w.resid_part,
                           w.counters),
-                 "launch resid_stream_kernel") ||
+                 "launch resid_stream_kernel")) ||
         !cuda_ok(launch_k(true, resid_draw_kernel<DT>, dim3(B), dim3(kDrawThreads), 0, stream, target, draft, g,
                           static_cast<const PairRec *>(w.pairs), static_cast<const float *>(w.resid_part),
                           static_cast<const float2 *>(w.part), static_cast<const int *>(w.counters), out_tokens,
-                          aux.residual_mass),
+                          out_num, aux.residual_mass),
                  "launch resid_draw_kernel"))
         return SPEC_ERR_CUDA;
     return SPEC_OK;
@@ -1002,7 +1197,7 @@ int launch_draft(const void *draft, const float *temperature, const float *u_dra
     // kernel, it waits for it before reading the inputs (wait_first)
     if (!cuda_ok(launch_k(true, stats_kernel<DT, kModeDraft>, dim3(st.sms * per_sm), dim3(kThreads), smem, stream,
                           draft, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, nullptr, nullptr,
-                          nullptr, 0, 1),
+                          nullptr, 0, 1, static_cast<PairRec *>(nullptr)),
                  "launch stats_kernel") ||
         !cuda_ok(launch_k(true, draft_select_kernel<DT>, dim3(std::max(grid, 1)), dim3(threads),
                           (B + 1) * sizeof(int), stream, draft, temperature, u_draft, k_offsets, B, g,

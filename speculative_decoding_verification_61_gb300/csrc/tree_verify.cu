@@ -270,12 +270,6 @@ __device__ __forceinline__ unsigned cluster_ctarank() {
     return r;
 }
 
-__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
 // Meeting point of a tree's CTAs after a pass, run by thread 0 of each CTA
 // once the CTA's masses and warp partials are written: the CTA's partial
 // T_cr = its warps' partials added in order; with two CTAs it publishes T_cr
@@ -849,10 +843,12 @@ int launch_tree(const void *target, const void *draft, const int32_t *node_offse
     const cudaError_t e =
         VERIFY ? launch_k(false, stats_kernel<DT, kModeTree>, dim3(st.sms * per_sm), dim3(kThreads), smem, stream,
                           target, draft, temperature, node_offsets, B, g, ns, part, counters,
-                          static_cast<int *>(nullptr), static_cast<const int *>(nint), static_cast<const int *>(tint), N, 0)
+                          static_cast<int *>(nullptr), static_cast<const int *>(nint), static_cast<const int *>(tint), N, 0,
+                          static_cast<PairRec *>(nullptr))
                : launch_k(false, stats_kernel<DT, kModeTreeDraft>, dim3(st.sms * per_sm), dim3(kThreads), smem,
                           stream, draft, draft, temperature, node_offsets, B, g, ns, part, counters,
-                          static_cast<int *>(nullptr), static_cast<const int *>(nint), static_cast<const int *>(tint), N, 0);
+                          static_cast<int *>(nullptr), static_cast<const int *>(nint), static_cast<const int *>(tint), N, 0,
+                          static_cast<PairRec *>(nullptr));
     if (!cuda_ok(e, "launch stats_kernel (tree)")) return SPEC_ERR_CUDA;
     if (VERIFY) {
         // kTreeCtas CTAs per tree as one cluster (co-scheduled), launched

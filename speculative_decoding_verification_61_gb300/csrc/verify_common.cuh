@@ -40,14 +40,18 @@ struct UnitDesc {
 
 // Words of the workspace's counter block.
 // Status word, then the streaming kernels' unit tickets and count of CTAs
-// done, the number of listed residual pairs (see PairRec), and a second
-// ticket pair for the target pass of spec_round, which streams while the
-// draft pass's kernels may still hold the first.
-enum CounterWord : int { kStatus = 1, kTicket = 2, kDone = 3, kPairs = 4, kTicketB = 5, kDoneB = 6, kCounterWords = 7 };
+// done, the number of listed residual pairs (see PairRec), a second ticket
+// pair for the target pass of spec_round, which streams while the draft
+// pass's kernels may still hold the first, and the number of sequences the
+// deferred epilogue has decided.
+enum CounterWord : int {
+    kStatus = 1, kTicket = 2, kDone = 3, kPairs = 4, kTicketB = 5, kDoneB = 6, kDecided = 7, kCounterWords = 8
+};
 
 // A rejected position whose residual is streamed by resid_stream_kernel:
-// written by resolve_kernel (deferred mode), one per rejected sequence, in
-// the order the decisions land.
+// written by the deferred epilogue's decisions, one per rejected sequence,
+// in the order the decisions land; `ready` is stored last (release), and
+// stats_kernel zeroes it for the next call.
 struct __align__(16) PairRec {
     int b;           // sequence
     int trow, drow;  // target and draft row at the rejected position
@@ -55,7 +59,8 @@ struct __align__(16) PairRec {
     float lth, ltl;  // the target row's log2-sum-exp, fp32 hi + lo
     float ldh, ldl;  // the draft row's
     float u;         // u_resample at the rejected position
-    int pad[3];
+    int ready;       // 1 once the fields above are written
+    int t0, k;       // the sequence's first target row and its draft length
 };
 
 struct WsPtrs {
@@ -191,7 +196,8 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
     const void *__restrict__ target, const void *__restrict__ draft,
     const float *__restrict__ temperature, const int *__restrict__ k_offsets, int B, Geometry g, int ns,
     float2 *__restrict__ part, int *__restrict__ counters, int *__restrict__ seqcnt,
-    const int *__restrict__ tree_nint, const int *__restrict__ tree_int, int tree_nodes, int wait_first) {
+    const int *__restrict__ tree_nint, const int *__restrict__ tree_int, int tree_nodes, int wait_first,
+    PairRec *__restrict__ pairs) {
     using E = Elem<DT>;
     constexpr bool DRAFT = MODE == kModeDraft;
     constexpr bool TREE = MODE == kModeTree || MODE == kModeTreeDraft;
@@ -256,9 +262,15 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
     if (wait_first != 2) grid_dependency_wait();
     const bool any_bad = __syncthreads_or(bad);
     if (MODE == kModeVerify || MODE == kModeTarget) {
-        for (int i = blockIdx.x * kThreads + tid; i < B; i += gridDim.x * kThreads) seqcnt[i] = 0;
-        // the epilogue of this call lists its residual pairs from zero
-        if (blockIdx.x == 0 && tid == 0) counters[kPairs] = 0;
+        for (int i = blockIdx.x * kThreads + tid; i < B; i += gridDim.x * kThreads) {
+            seqcnt[i] = 0;
+            if (pairs) pairs[i].ready = 0;
+        }
+        // the epilogue of this call lists and decides its sequences from zero
+        if (blockIdx.x == 0 && tid == 0) {
+            counters[kPairs] = 0;
+            counters[kDecided] = 0;
+        }
     }
     // the next kernel may be scheduled as soon as SMs free up; it waits for
     // this grid's completion before it reads anything written here
@@ -816,18 +828,18 @@ __device__ int warp_scan_elems(const void *row1, const void *row2, int a, int b,
 }
 
 // Block-level inverse CDF inside elements [a, b) (at most one 2 KB
-// sub-chunk) of one or two rows, by a block of kDrawThreads threads: thread t
-// owns the 8 bytes at element a + t * PE (4 bf16 or 2 fp32 elements; a
-// sub-chunk is 1024 bf16 or 512 fp32 elements, so one group per thread), so
-// each thread holds a contiguous run and the cumulative mass is one block
-// scan.  Weights are W(x_row1, x_row2).  Every thread returns the first
+// sub-chunk) of one or two rows, by a block of kDrawThreads or more threads
+// (up to 1024): thread t owns the 8 bytes at element a + t * PE (4 bf16 or
+// 2 fp32 elements; a sub-chunk is 1024 bf16 or 512 fp32 elements, so one
+// group for each of the first 256 threads), so each thread holds a
+// contiguous run and the cumulative mass is one block scan.  Weights are W(x_row1, x_row2).  Every thread returns the first
 // element whose cumulative mass, starting at `before`, exceeds `target`;
 // else the last element with positive weight (rounding fallback); else -1.
 // The same rule as warp_scan_elems, with the work spread over 8 warps so
 // that the draw is a few dependent steps long instead of 64.
 constexpr int kDrawThreads = 256;
 struct DrawSmem {
-    float wsum[kDrawThreads / 32];
+    float wsum[32];  // per-warp sums of the block scan
     int found, lastpos;
     int sc;             // located sub-chunk (block_draw_row)
     F2 before, target;  // its cumulative mass before it, and u * Z
