@@ -282,7 +282,10 @@ struct DecideSmem {
 // One block per sequence.  Phase 1: the gathered records of each needed row
 // are combined in rank order (one lane per rank), then warp 0 takes the
 // chain verify's decision.  Phase 2 (sampled sequences): this rank's masses
-// of the distribution to draw from and of p at position n.
+// of the distribution to draw from and of p at position n.  Launched with
+// programmatic dependent launch: it waits for the stream's previous kernel
+// (the exchange of the records) before it reads anything, and lets the draw
+// kernel be scheduled right after that wait.
 template <int DT>
 __global__ void __launch_bounds__(256) shard_decide_kernel(
     const void *__restrict__ target, const void *__restrict__ draft, const spec_shard_stat_t *__restrict__ all_stats,
@@ -293,6 +296,8 @@ __global__ void __launch_bounds__(256) shard_decide_kernel(
     __shared__ DecideSmem sm;
     const int b = blockIdx.x;
     const int lane = lane_id(), warp = warp_id();
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (block_bad_offsets(k_offsets, B)) {
         // the whole call fails; outputs of unknown size stay untouched
         if (threadIdx.x == 0) {
@@ -514,112 +519,142 @@ __global__ void __launch_bounds__(256) shard_decide_kernel(
 }
 
 // ================================================================ draw
-// One warp per sequence.  Lane 0 sums the gathered masses in rank order (the
+// One block per sequence.  Warp 0 sums the gathered masses in rank order (the
 // same operations on every rank) and finds the rank whose cumulative mass
 // first exceeds u * Z; that rank alone draws, inside its columns, at the
-// remaining target.  A residual mass of 0 on every rank falls back to p.
+// remaining target: warp 0 locates the sub-chunk, the block scans its
+// elements (block_scan_elems).  A residual mass of 0 on every rank falls
+// back to p.  Launched with programmatic dependent launch: it waits for the
+// stream's previous kernel (the exchange of the masses) before it reads
+// anything.
+struct ShardDrawSmem {
+    DrawSmem ds;
+    int draw;   // this rank draws: 1 from the residual, 2 from p
+    int64_t trow;
+};
+
 template <int DT>
-__global__ void __launch_bounds__(256) shard_draw_kernel(
+__global__ void __launch_bounds__(kDrawThreads) shard_draw_kernel(
     const void *__restrict__ target, const void *__restrict__ draft, const double *__restrict__ all_mass,
     const float *__restrict__ u_resample, const int *__restrict__ k_offsets, int B, Geometry g, ShardSpec sp,
     const float2 *__restrict__ part, const float *__restrict__ resid, const ShardSeq *__restrict__ seq,
     int32_t *__restrict__ out_tokens) {
     using E = Elem<DT>;
+    __shared__ ShardDrawSmem sm;
     const int lane = lane_id();
-    const int b = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
-    if (b >= B) return;
-    // everything that depends on b alone is loaded at once: the decision,
-    // the sequence's offsets, its masses on every rank (lane l: ranks l and
-    // l + 32, G <= 64) and its residual masses on this rank
+    const int b = blockIdx.x;
+    grid_dependency_wait();
     const ShardSeq q = seq[b];
-    const int k0 = k_offsets[b], k1 = k_offsets[b + 1];
-    double mr[2] = {0.0, 0.0}, mp[2] = {0.0, 0.0};
+    if (warp_id() == 0) {
+        if (lane == 0) sm.draw = 0;
+        // everything that depends on b alone is loaded at once: the decision,
+        // the sequence's offsets, its masses on every rank (lane l: ranks l
+        // and l + 32, G <= 64) and its residual masses on this rank
+        const int k0 = k_offsets[b], k1 = k_offsets[b + 1];
+        double mr[2] = {0.0, 0.0}, mp[2] = {0.0, 0.0};
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int h = lane + 32 * j;
-        if (h < sp.G) {
-            const double2 m2 = __ldg(reinterpret_cast<const double2 *>(all_mass + (static_cast<int64_t>(h) * B + b) * 2));
-            mr[j] = m2.x;
-            mp[j] = m2.y;
+        for (int j = 0; j < 2; ++j) {
+            const int h = lane + 32 * j;
+            if (h < sp.G) {
+                const double2 m2 =
+                    __ldg(reinterpret_cast<const double2 *>(all_mass + (static_cast<int64_t>(h) * B + b) * 2));
+                mr[j] = m2.x;
+                mp[j] = m2.y;
+            }
+        }
+        const float *rp = resid + static_cast<int64_t>(b) * g.n_sub;
+        float w[kPartCache];
+        r_weights_cached(rp, g.n_sub, w);
+        // the decision must be the one spec_shard_decide wrote for this
+        // call's k_offsets (it wrote kJobNone everywhere for an invalid array)
+        const int k = k1 - k0;
+        const bool valid = (q.kind == kJobResid || q.kind == kJobBonus) && k >= 0 && k <= kMaxK &&
+                           q.ot == k0 + b && q.od == k0 && q.n >= 0 && q.n <= k && (q.kind == kJobResid) == (q.n < k);
+        if (valid) {
+            const int64_t trow = static_cast<int64_t>(q.ot) + q.n;
+            const float u = u_resample[trow];
+            float2 pc[kPartCache];  // p partials of row n, in case p is drawn from
+            load_parts(part + trow * g.n_sub, g.n_sub, pc);
+            // every lane adds the ranks' masses in rank order, so the sums
+            // are the same on every lane and every rank
+            auto mass_of = [&](int h, bool p) -> double {
+                const double a = __shfl_sync(0xffffffffu, p ? mp[0] : mr[0], h & 31);
+                const double c = __shfl_sync(0xffffffffu, p ? mp[1] : mr[1], h & 31);
+                return h < 32 ? a : c;
+            };
+            double Z = 0.0;
+            for (int h = 0; h < sp.G; ++h) Z += mass_of(h, false);
+            const bool use_p = !(Z > 0.0);
+            if (use_p) {
+                Z = 0.0;
+                for (int h = 0; h < sp.G; ++h) Z += mass_of(h, true);
+            }
+            // u < 1, so t < Z: the running sum, which repeats Z's additions,
+            // exceeds t at the latest at the last rank with positive mass
+            const double t = static_cast<double>(u) * Z;
+            double C = 0.0, before = 0.0;
+            int owner = -1;
+            if (Z > 0.0) {
+                for (int h = 0; h < sp.G; ++h) {
+                    const double m = mass_of(h, use_p);
+                    if (m > 0.0 && C + m > t) {
+                        owner = h;
+                        before = C;
+                        break;
+                    }
+                    C += m;
+                }
+            }
+            if (owner == sp.rank) {
+                const double tl = t - before;
+                F2 tgt;
+                tgt.hi = static_cast<float>(tl);
+                tgt.lo = static_cast<float>(tl - static_cast<double>(tgt.hi));
+                F2 bef;
+                int sc;
+                const bool from_resid = q.kind == kJobResid && !use_p;
+                if (from_resid) {
+                    sc = warp_locate_at(g.n_sub, w, RWeights{rp}, tgt, &bef);
+                } else {
+                    const PWeights pw{part + trow * g.n_sub, q.M};
+#pragma unroll
+                    for (int j = 0; j < kPartCache; ++j)
+                        w[j] = pc[j].x > -INFINITY ? pc[j].y * ex2(pc[j].x - pw.M) : 0.0f;
+                    sc = warp_locate_at(g.n_sub, w, pw, tgt, &bef);
+                }
+                if (lane == 0) {
+                    sm.draw = sc < 0 ? 3 : (from_resid ? 1 : 2);
+                    sm.trow = trow;
+                    sm.ds.sc = sc;
+                    sm.ds.before = bef;
+                    sm.ds.target = tgt;
+                }
+            }
         }
     }
-    const float *rp = resid + static_cast<int64_t>(b) * g.n_sub;
-    float w[kPartCache];
-    r_weights_cached(rp, g.n_sub, w);
-    if (q.kind != kJobResid && q.kind != kJobBonus) return;
-    // the decision must be the one spec_shard_decide wrote for this call's
-    // k_offsets (it wrote kJobNone everywhere for an invalid array)
-    const int k = k1 - k0;
-    if (k < 0 || k > kMaxK || q.ot != k0 + b || q.od != k0 || q.n < 0 || q.n > k ||
-        (q.kind == kJobResid) != (q.n < k))
-        return;
-    const int64_t trow = static_cast<int64_t>(q.ot) + q.n;
-    const float u = u_resample[trow];
-    float2 pc[kPartCache];  // p partials of row n, in case p is drawn from
-    load_parts(part + trow * g.n_sub, g.n_sub, pc);
-    // every lane adds the ranks' masses in rank order, so the sums are the
-    // same on every lane and every rank
-    auto mass_of = [&](int h, bool p) -> double {
-        const double a = __shfl_sync(0xffffffffu, p ? mp[0] : mr[0], h & 31);
-        const double c = __shfl_sync(0xffffffffu, p ? mp[1] : mr[1], h & 31);
-        return h < 32 ? a : c;
-    };
-    double Z = 0.0;
-    for (int h = 0; h < sp.G; ++h) Z += mass_of(h, false);
-    const bool use_p = !(Z > 0.0);
-    if (use_p) {
-        Z = 0.0;
-        for (int h = 0; h < sp.G; ++h) Z += mass_of(h, true);
-    }
-    if (!(Z > 0.0)) return;
-    // u < 1, so t < Z: the running sum, which repeats Z's additions, exceeds
-    // t at the latest at the last rank with positive mass
-    const double t = static_cast<double>(u) * Z;
-    double C = 0.0, before = 0.0;
-    int owner = -1;
-    for (int h = 0; h < sp.G; ++h) {
-        const double m = mass_of(h, use_p);
-        if (m > 0.0 && C + m > t) {
-            owner = h;
-            before = C;
-            break;
-        }
-        C += m;
-    }
-    if (owner != sp.rank) return;
-    const double tl = t - before;
-    F2 tgt;
-    tgt.hi = static_cast<float>(tl);
-    tgt.lo = static_cast<float>(tl - static_cast<double>(tgt.hi));
-    const float c = q.c;
-    F2 bef;
+    __syncthreads();
+    const int draw = sm.draw;
+    if (draw == 0) return;  // not this rank's draw (or nothing to draw)
+    const int64_t trow = sm.trow;
     int token = -1;
-    const unsigned char *rt = static_cast<const unsigned char *>(target) + trow * g.V * static_cast<int64_t>(E::kBytes);
-    if (q.kind == kJobResid && !use_p) {
-        const int sc = warp_locate_at(g.n_sub, w, RWeights{rp}, tgt, &bef);
-        if (sc >= 0) {
-            int a, e1;
-            sub_range(g, sc, &a, &e1);
+    if (draw != 3) {
+        int a, e1;
+        sub_range(g, sm.ds.sc, &a, &e1);
+        const unsigned char *rt = static_cast<const unsigned char *>(target) + trow * g.V * static_cast<int64_t>(E::kBytes);
+        const float c = q.c;
+        if (draw == 1) {
             const unsigned char *rd = static_cast<const unsigned char *>(draft) +
                                       (static_cast<int64_t>(q.od) + q.n) * g.V * static_cast<int64_t>(E::kBytes);
             const float lth = q.lth, ltl = q.ltl, ldh = q.ldh, ldl = q.ldl;
             auto W = [&](float a1, float a2) -> float { return resid_weight(a1, a2, c, lth, ltl, ldh, ldl); };
-            token = warp_scan_elems<DT>(rt, rd, a, e1, W, bef, tgt);
-        }
-    } else {
-        const PWeights pw{part + trow * g.n_sub, q.M};
-#pragma unroll
-        for (int j = 0; j < kPartCache; ++j) w[j] = pc[j].x > -INFINITY ? pc[j].y * ex2(pc[j].x - pw.M) : 0.0f;
-        const int sc = warp_locate_at(g.n_sub, w, pw, tgt, &bef);
-        if (sc >= 0) {
-            int a, e1;
-            sub_range(g, sc, &a, &e1);
+            token = block_scan_elems<DT>(rt, rd, a, e1, W, sm.ds.before, sm.ds.target, sm.ds);
+        } else {
             const float M = q.M;
             auto W = [&](float x, float) -> float { return prob_weight(x, c, M); };
-            token = warp_scan_elems<DT>(rt, rt, a, e1, W, bef, tgt);
+            token = block_scan_elems<DT>(rt, rt, a, e1, W, sm.ds.before, sm.ds.target, sm.ds);
         }
     }
-    if (lane == 0) out_tokens[trow] = token >= 0 ? token + sp.v0 : -1;
+    if (threadIdx.x == 0) out_tokens[trow] = token >= 0 ? token + sp.v0 : -1;
 }
 
 }  // namespace specv
@@ -770,7 +805,8 @@ int spec_shard_stats(const void *target_shard, const void *draft_shard, const in
     DeviceState *st = shard_device_state(&dev);
     if (!st) return SPEC_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (!reset_tickets(workspace, s)) return SPEC_ERR_CUDA;
+    // (the ticket words: zero in a zero-filled workspace, and every
+    // stats_kernel launch leaves them at zero)
     const ShardWs w = shard_ws_ptrs(workspace, l);
     if (dtype == SPEC_F32)
         return launch_shard_stats<SPEC_F32>(target_shard, draft_shard, draft_tokens, temperature, B, k_offsets, sp, g,
@@ -803,11 +839,11 @@ int spec_shard_decide(const void *target_shard, const void *draft_shard, const s
     const ShardWs w = shard_ws_ptrs(workspace, l);
     const cudaError_t e =
         dtype == SPEC_F32
-            ? launch_k(false, shard_decide_kernel<SPEC_F32>, dim3(B), dim3(256), 0, s, target_shard, draft_shard,
+            ? launch_k(true, shard_decide_kernel<SPEC_F32>, dim3(B), dim3(256), 0, s, target_shard, draft_shard,
                        all_stats, draft_tokens, u_accept, temperature, k_offsets, B, g, sp,
                        static_cast<const float2 *>(w.part), w.resid, w.seq, out_tokens, out_num_accepted, out_mass,
                        w.counters)
-            : launch_k(false, shard_decide_kernel<SPEC_BF16>, dim3(B), dim3(256), 0, s, target_shard, draft_shard,
+            : launch_k(true, shard_decide_kernel<SPEC_BF16>, dim3(B), dim3(256), 0, s, target_shard, draft_shard,
                        all_stats, draft_tokens, u_accept, temperature, k_offsets, B, g, sp,
                        static_cast<const float2 *>(w.part), w.resid, w.seq, out_tokens, out_num_accepted, out_mass,
                        w.counters);
@@ -834,13 +870,12 @@ int spec_shard_draw(const void *target_shard, const void *draft_shard, const dou
     if (!shard_device_state(&dev)) return SPEC_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const ShardWs w = shard_ws_ptrs(workspace, l);
-    const int grid = (B + 7) / 8;
     const cudaError_t e =
         dtype == SPEC_F32
-            ? launch_k(false, shard_draw_kernel<SPEC_F32>, dim3(grid), dim3(256), 0, s, target_shard, draft_shard,
+            ? launch_k(true, shard_draw_kernel<SPEC_F32>, dim3(B), dim3(kDrawThreads), 0, s, target_shard, draft_shard,
                        all_mass, u_resample, k_offsets, B, g, sp, static_cast<const float2 *>(w.part),
                        static_cast<const float *>(w.resid), static_cast<const ShardSeq *>(w.seq), out_tokens)
-            : launch_k(false, shard_draw_kernel<SPEC_BF16>, dim3(grid), dim3(256), 0, s, target_shard, draft_shard,
+            : launch_k(true, shard_draw_kernel<SPEC_BF16>, dim3(B), dim3(kDrawThreads), 0, s, target_shard, draft_shard,
                        all_mass, u_resample, k_offsets, B, g, sp, static_cast<const float2 *>(w.part),
                        static_cast<const float *>(w.resid), static_cast<const ShardSeq *>(w.seq), out_tokens);
     return cuda_ok(e, "launch shard_draw_kernel") ? SPEC_OK : SPEC_ERR_CUDA;

@@ -1173,6 +1173,12 @@ int launch_verify(const void *target, const void *draft, const double *draft_lse
     return SPEC_OK;
 }
 
+#ifndef SPEC_SELECT_BESIDE_THREADS
+#define SPEC_SELECT_BESIDE_THREADS 128
+#endif
+#ifndef SPEC_SELECT_BESIDE_BLOCKS
+#define SPEC_SELECT_BESIDE_BLOCKS 1
+#endif
 #ifndef SPEC_SELECT_BLOCKS_PER_SM
 #define SPEC_SELECT_BLOCKS_PER_SM 8
 #endif
@@ -1189,8 +1195,8 @@ int launch_draft(const void *draft, const float *temperature, const float *u_dra
     // per block.  beside_stream (spec_round): the target pass streams while
     // the draws run and needs them only at its end, so the draws take one
     // 4-warp block per SM and leave each SM room for four streaming CTAs
-    const int threads = beside_stream ? 128 : 256;
-    const int grid = beside_stream ? st.sms
+    const int threads = beside_stream ? SPEC_SELECT_BESIDE_THREADS : 256;
+    const int grid = beside_stream ? st.sms * SPEC_SELECT_BESIDE_BLOCKS
                                    : static_cast<int>(std::min(static_cast<int64_t>(st.sms) * SPEC_SELECT_BLOCKS_PER_SM,
                                                                (static_cast<int64_t>(B) * kMaxK + 7) / 8));
     // the call's first kernel: launched early behind the stream's previous
