@@ -446,7 +446,7 @@ def measure_vocab_shard(torch, sv, dev, reps, warmup, Gs):
     del d
     return {"workload": w.name, "by_ranks": out,
             "calls": "per rank, replayed as one CUDA graph (rank_ms_*; issued from Python: rank_ms_max_eager): "
-                     "spec_shard_stats (ticket reset + stats_kernel shard mode + shard_row_kernel), "
+                     "spec_shard_stats (stats_kernel shard mode + shard_row_kernel), "
                      "spec_shard_decide (shard_decide_kernel), spec_shard_draw (shard_draw_kernel); exchanges not timed"}
 
 
