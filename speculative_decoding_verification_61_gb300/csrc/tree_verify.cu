@@ -110,8 +110,12 @@ __global__ void __launch_bounds__(256) tree_setup_kernel(const int *__restrict__
 #define SPEC_TREE_CTAS 2
 #endif
 constexpr int kTreeCtas = SPEC_TREE_CTAS;
-static_assert(kTreeCtas == 1 || kTreeCtas == 2, "one or two CTAs per tree");
-constexpr int kWalkThreads = 512;
+static_assert(kTreeCtas == 1 || kTreeCtas == 2 || kTreeCtas == 4, "one, two or four CTAs per tree");
+// four CTAs per tree: 256 threads each, two per SM (a tree's quarter-pass
+// shares its SM with another tree's CTA, and has it to itself while that
+// tree tests, draws or has finished)
+constexpr int kWalkThreads = kTreeCtas == 4 ? 256 : 512;
+constexpr int kWalkMinBlocks = kTreeCtas == 4 ? 2 : 1;
 constexpr int kWalkWarps = kWalkThreads / 32;
 
 struct TreeWalkSmem {
@@ -135,6 +139,7 @@ struct TreeWalkSmem {
     int next;                   // accepted child (local index) or -1
     int zpos;                   // the last residual mass was > 0
     int token;                  // the drawn token
+    DrawSmem ds;                // block-level draws (CTA 0)
 };
 
 // The residual chain in closed form.  With a = p and b = q of the node,
@@ -317,7 +322,7 @@ __device__ bool tree_meet_sum(int *cnt, int target, float2 *ptot, int cr, const 
 // or an invalid needed row) make the whole sequence -1, as in the chain
 // verify; an invalid node_offsets array fails the whole call.
 template <int DT>
-__global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
+__global__ void __launch_bounds__(kWalkThreads, kWalkMinBlocks) tree_walk_kernel(
     const void *__restrict__ target, const void *__restrict__ draft, const int *__restrict__ node_offsets,
     const int *__restrict__ parent, const int32_t *__restrict__ tokens, const float *__restrict__ u_accept,
     const float *__restrict__ u_resample, const float *__restrict__ temperature, int B, int N, Geometry g,
@@ -401,6 +406,20 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
                                    counters + kStatus, S0);
     };
     const int64_t rb = static_cast<int64_t>(V) * E::kBytes;
+    // this CTA's share of a node's two rows to L2 in 32 KB bulk prefetches
+    // (one warp; sub-chunk bounds are 16-byte aligned), so that the passes
+    // over them wait on L2, not on DRAM
+    auto prefetch_rows = [&](const unsigned char *prt, const unsigned char *prd) {
+        if (!SPEC_RESID_PREFETCH || sc0 >= sc1) return;
+        int e_lo, e_hi, unused;
+        sub_range(g, sc0, &e_lo, &unused);
+        sub_range(g, sc1 - 1, &unused, &e_hi);
+        const int64_t lo = static_cast<int64_t>(e_lo) * E::kBytes, hi = static_cast<int64_t>(e_hi) * E::kBytes;
+        constexpr int64_t kPiece = 32768;
+        const unsigned char *r0 = (lane & 1) ? prd : prt;
+        for (int64_t off = lo + static_cast<int64_t>(lane >> 1) * kPiece; off < hi; off += 16 * kPiece)
+            bulk_prefetch_l2(r0 + off, static_cast<uint32_t>(min(kPiece, hi - off)));
+    };
 
     // --- prologue: the statistics of every node's rows (the n target rows,
     // then the internal nodes' draft rows; each warp takes two rows at a
@@ -414,11 +433,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
             bool internal = false;
             for (int i = tid + 1; i < n; ++i) internal |= sm.par[i] == tid;
             if (!internal) sm.okd[tid] = 1;
-            if (!greedy && tid > 0) {
-                const int64_t prow = g0 + sm.par[tid];
-                sm.zt[tid] = E::load1(target, prow * V + sm.tok[tid]);
-                sm.zd[tid] = E::load1(draft, prow * V + sm.tok[tid]);
-            }
+        }
+        // every child's logits at its token (two loads from HBM each): issued
+        // now, stored to shared memory after the rows' combine below
+        float zt_own = 0.0f, zd_own = 0.0f;
+        if (tid < n && tid > 0 && !greedy) {
+            const int64_t prow = g0 + sm.par[tid];
+            zt_own = E::load1(target, prow * V + sm.tok[tid]);
+            zd_own = E::load1(draft, prow * V + sm.tok[tid]);
         }
         const int items = n + (greedy ? 0 : nint[b]);
         // partials of item k: target row of node k, or the draft row of the
@@ -475,6 +497,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
                 }
             }
         }
+        if (tid < n && tid > 0 && !greedy) {
+            sm.zt[tid] = zt_own;
+            sm.zd[tid] = zd_own;
+        }
         __syncthreads();
     }
 
@@ -508,13 +534,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
             continue;
         }
         if (leaf) {
-            // bonus token from p_u, as the chain's bonus draw
-            if (warp == 0 && cr == 0) {
-                const float2 *pr = part + urow * g.n_sub;
-                float2 pc[kPartCache];
-                load_parts(pr, g.n_sub, pc);
-                const int tk = warp_draw_row<DT>(target, urow, pr, pc, g, c, sm.M[u], u_resample[urow]);
-                if (lane == 0) sm.token = tk;
+            // bonus token from p_u, as the chain's bonus draw (the whole of CTA 0)
+            if (cr == 0) {
+                const int tk = block_draw_row<DT>(target, urow, part + urow * g.n_sub, g, c, sm.M[u],
+                                                  u_resample[urow], sm.ds);
+                if (tid == 0) sm.token = tk;
             }
             __syncthreads();
             final_token = sm.token;
@@ -567,18 +591,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
             }
             // rejected: the next level t' = t + S(t), and one pass over u's
             // rows for S(t') and its per-sub-chunk masses
-            if (j == 0 && warp == 0 && SPEC_RESID_PREFETCH && sc0 < sc1) {
-                // this CTA's half of both rows to L2 in 32 KB bulk prefetches
-                // (sub-chunk bounds are 16-byte aligned): the later passes hit L2
-                int e_lo, e_hi, unused;
-                sub_range(g, sc0, &e_lo, &unused);
-                sub_range(g, sc1 - 1, &unused, &e_hi);
-                const int64_t lo = static_cast<int64_t>(e_lo) * E::kBytes, hi = static_cast<int64_t>(e_hi) * E::kBytes;
-                constexpr int64_t kPiece = 32768;
-                const unsigned char *r0 = (lane & 1) ? rd : rt;
-                for (int64_t off = lo + static_cast<int64_t>(lane >> 1) * kPiece; off < hi; off += 16 * kPiece)
-                    bulk_prefetch_l2(r0 + off, static_cast<uint32_t>(min(kPiece, hi - off)));
-            }
+            if (j == 0 && warp == 0) prefetch_rows(rt, rd);  // at a node's first pass: the later ones hit L2
             const double tn = sm.t + static_cast<double>(sm.S);
             TreeWeight W = base;
             W.t = static_cast<float>(tn);
@@ -628,27 +641,36 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(
                 break;
             }
         }
-        if (warp == 0 && cr == 0) {
+        // the draw, by the whole of CTA 0: warp 0 locates the sub-chunk, the
+        // block scans its elements
+        if (cr == 0) {
             int tk = -1;
             if (from_partials) {
-                const float2 *pr = part + urow * g.n_sub;
-                float2 pc[kPartCache];
-                load_parts(pr, g.n_sub, pc);
-                tk = warp_draw_row<DT>(target, urow, pr, pc, g, c, sm.M[u], u_resample[urow]);
+                tk = block_draw_row<DT>(target, urow, part + urow * g.n_sub, g, c, sm.M[u], u_resample[urow], sm.ds);
             } else {
-                float w[kPartCache];
+                if (warp == 0) {
+                    float w[kPartCache];
 #pragma unroll
-                for (int q = 0; q < kPartCache; ++q) w[q] = (lane + 32 * q < g.n_sub) ? __ldcg(rm + lane + 32 * q) : 0.0f;
-                auto wfar = [&](int i) -> float { return __ldcg(rm + i); };
-                F2 before, Z, tgt;
-                const int sc = warp_locate(g.n_sub, w, wfar, u_resample[urow], &before, &Z, &tgt);
+                    for (int q = 0; q < kPartCache; ++q)
+                        w[q] = (lane + 32 * q < g.n_sub) ? __ldcg(rm + lane + 32 * q) : 0.0f;
+                    auto wfar = [&](int i) -> float { return __ldcg(rm + i); };
+                    F2 before, Z, tgt;
+                    const int sc = warp_locate(g.n_sub, w, wfar, u_resample[urow], &before, &Z, &tgt);
+                    if (lane == 0) {
+                        sm.ds.sc = sc;
+                        sm.ds.before = before;
+                        sm.ds.target = tgt;
+                    }
+                }
+                __syncthreads();
+                const int sc = sm.ds.sc;
                 if (sc >= 0) {
                     int a, e1;
                     sub_range(g, sc, &a, &e1);
-                    tk = warp_scan_elems<DT>(rt, rd, a, e1, W, before, tgt);
+                    tk = block_scan_elems<DT>(rt, rd, a, e1, W, sm.ds.before, sm.ds.target, sm.ds);
                 }
             }
-            if (lane == 0) sm.token = tk;
+            if (tid == 0) sm.token = tk;
         }
         __syncthreads();
         final_token = sm.token;
