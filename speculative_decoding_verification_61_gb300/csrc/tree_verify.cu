@@ -262,11 +262,9 @@ __device__ __noinline__ void tree_pass(const unsigned char *rt, const unsigned c
         nc = nn;
         sc = sn;
     }
-    if (lane == 0) {
-        wpart[warp_id()] = make_float2(wacc.hi, wacc.lo);
-        // this warp's masses visible to the other CTA of the tree before the meeting
-        if (kTreeCtas > 1) __threadfence();
-    }
+    // (the masses reach the other CTAs of the tree through the meeting's
+    // release: the CTA barrier before it, then thread 0's release-add)
+    if (lane == 0) wpart[warp_id()] = make_float2(wacc.hi, wacc.lo);
 }
 
 __device__ __forceinline__ unsigned cluster_ctarank() {
@@ -296,8 +294,9 @@ __device__ bool tree_meet_sum(int *cnt, int target, float2 *ptot, int cr, const 
     }
     const float2 mine = make_float2(part.hi, part.lo);
     ptot[cr] = mine;
-    __threadfence();
-    atomicAdd(cnt, 1);
+    // release: this CTA's masses (written before the caller's barrier) and
+    // its partial, to whoever acquires the count
+    red_add_release_gpu(cnt, 1);
     const uint64_t t0 = global_timer_ns();
     while (ld_acquire_gpu(cnt) < target) {
         if (global_timer_ns() - t0 > kWaitLimitNs) {
