@@ -481,12 +481,14 @@ int spec_workspace_status(const void *workspace, int *status_out, int clear);
 /*
  * Self-check of the device-side bounded waits (for tests): one kernel waits
  * on an mbarrier that nothing arrives at, then on a meeting counter that
- * nothing completes, as the streaming kernel and the tree walk would when a
- * copy or a peer CTA never comes.  Each wait gives up after its limit (2 s
- * each) and SPEC_ERR_TIMEOUT is recorded in the status word of `workspace`
- * (device, >= 256 bytes, 16-byte aligned, zero-filled; word 8 gets 3 when
- * both waits gave up).  Nothing traps or faults; the context stays usable.
- * Asynchronous on `stream`; takes about 4 s on the device.
+ * nothing completes, then for a residual pair that is never listed, as the
+ * streaming kernels, the tree walk and the deferred epilogue would when a
+ * copy, a peer CTA or a deciding CTA never comes.  Each wait gives up after
+ * its limit (2 s each) and SPEC_ERR_TIMEOUT is recorded in the status word
+ * of `workspace` (device, >= 256 bytes, 16-byte aligned, zero-filled; word 8
+ * gets 7 when all three waits gave up).  Nothing traps or faults; the
+ * context stays usable.  Asynchronous on `stream`; takes about 6 s on the
+ * device.
  */
 int spec_selfcheck_wait_timeout(void *workspace, size_t workspace_bytes, void *stream);
 

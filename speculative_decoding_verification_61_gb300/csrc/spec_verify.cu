@@ -708,27 +708,9 @@ __global__ void __launch_bounds__(kThreads, 2) decide_stream_kernel(
                 const int tn = atomicAdd(counters + kTicket, 1);  // the next ticket, in flight meanwhile
                 if (p != cur) {
                     // wait for pair p: listed and ready, or never listed
-                    bool listed = false;
-                    const uint64_t t0 = global_timer_ns();
-                    for (;;) {
-                        int np = ld_acquire_gpu(counters + kPairs);
-                        if (p < np && ld_acquire_gpu(&ws.pairs[p].ready)) {
-                            listed = true;
-                            break;
-                        }
-                        if (p >= np && ld_acquire_gpu(counters + kDecided) >= B) {
-                            // every listing precedes its sequence's count
-                            np = ld_acquire_gpu(counters + kPairs);
-                            if (p >= np) break;
-                            continue;
-                        }
-                        if (global_timer_ns() - t0 > kWaitLimitNs) {
-                            ok = false;
-                            break;
-                        }
-                        __nanosleep(64);
-                    }
-                    if (!listed) break;
+                    const int listed = wait_pair(counters, ws.pairs, p, B);
+                    if (listed < 0) ok = false;
+                    if (listed <= 0) break;
                     r = ws.pairs[p];
                     cur = p;
                 }

@@ -692,8 +692,11 @@ __global__ void __launch_bounds__(kWalkThreads, kWalkMinBlocks) tree_walk_kernel
 // The bounded device-side waits, made to run out on purpose: one thread
 // waits on an mbarrier that nothing arrives at (as a ring slot whose copy
 // never lands), then meets on a counter that no other CTA completes (as a
-// tree whose other CTA never arrives).  Each wait gives up after its limit
-// and the status word gets SPEC_ERR_TIMEOUT; the kernel then returns.
+// tree whose other CTA never arrives), then waits for an entry of the
+// deferred epilogue's pair list that nobody lists while the decided count
+// stays short (as a residual stream whose deciding CTA never runs).  Each
+// wait gives up after its limit and the status word gets SPEC_ERR_TIMEOUT;
+// the kernel then returns.
 __global__ void selfcheck_wait_kernel(int *counters, int *never) {
     __shared__ uint64_t bar;
     if (threadIdx.x != 0) return;
@@ -707,7 +710,11 @@ __global__ void selfcheck_wait_kernel(int *counters, int *never) {
     float S;
     // a count the single arrival of this CTA never reaches
     const bool meet_ok = tree_meet_sum(never, 2 * kTreeCtas, ptot, 0, wpart, counters + kStatus, &S);
-    counters[8] = (mbar_ok ? 0 : 1) | (meet_ok ? 0 : 2);  // which waits gave up
+    // the list and the decided count of a zero-filled block stay at 0; one
+    // sequence is owed (the list's entries are never read)
+    const bool pair_ok = wait_pair(counters, nullptr, 0, 1) >= 0;
+    if (!pair_ok) set_status(counters + kStatus, SPEC_ERR_TIMEOUT);
+    counters[8] = (mbar_ok ? 0 : 1) | (meet_ok ? 0 : 2) | (pair_ok ? 0 : 4);  // which waits gave up
     *never = 0;
 }
 

@@ -63,6 +63,26 @@ struct __align__(16) PairRec {
     int t0, k;       // the sequence's first target row and its draft length
 };
 
+// Wait (bounded, 2 s) for entry p of the deferred epilogue's pair list:
+// 1 once it is listed and its ready flag is set (acquire: its fields are
+// then visible), 0 once every one of the B sequences is decided and p lies
+// past the list (every listing precedes its sequence's count), -1 on a
+// time-out (the caller records it).
+__device__ __forceinline__ int wait_pair(const int *counters, const PairRec *pairs, int p, int B) {
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        int np = ld_acquire_gpu(counters + kPairs);
+        if (p < np && ld_acquire_gpu(&pairs[p].ready)) return 1;
+        if (p >= np && ld_acquire_gpu(counters + kDecided) >= B) {
+            np = ld_acquire_gpu(counters + kPairs);
+            if (p >= np) return 0;
+            continue;
+        }
+        if (global_timer_ns() - t0 > kWaitLimitNs) return -1;
+        __nanosleep(64);
+    }
+}
+
 struct WsPtrs {
     float2 *part;        // [rows_cap * n_sub] sub-chunk partials
     int *counters;       // CounterWord: status, unit tickets and CTAs done, pairs
