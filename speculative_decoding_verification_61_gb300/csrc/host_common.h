@@ -46,6 +46,12 @@ bool cuda_ok(cudaError_t e, const char *what);
 bool make_geometry(int V, int dtype, Geometry *g);
 // Per-device state of the chain kernels (attributes set once per device).
 DeviceState *device_state(int *dev_out);
+
+// The streaming kernel copies its rows evict-first in L2 (chain and tree
+// passes; the vocab-sharded pass measured no better with it).
+#ifndef SPEC_STREAM_EVICT_FIRST
+#define SPEC_STREAM_EVICT_FIRST 1
+#endif
 // Ring depth, dynamic shared memory and CTAs per SM of stats_kernel for a
 // call with B sequences (ns = 0 if nothing fits).
 void pick_ring(const DeviceState &st, int B, int *ns, size_t *smem, int *ctas_per_sm);

@@ -763,7 +763,7 @@ int launch_shard_stats(const void *target, const void *draft, const int32_t *tok
     if (!cuda_ok(launch_k(true, stats_kernel<DT, kModeShard>, dim3(st.sms * per_sm), dim3(kThreads), smem, stream,
                           target, draft, temperature, k_offsets, B, g, ns, w.part, w.counters,
                           static_cast<int *>(nullptr), static_cast<const int *>(nullptr),
-                          static_cast<const int *>(nullptr), 0, 1, static_cast<PairRec *>(nullptr)),
+                          static_cast<const int *>(nullptr), 0, 1, static_cast<PairRec *>(nullptr), 0),
                  "launch stats_kernel (shard)") ||
         !cuda_ok(launch_k(true, shard_row_kernel<DT>, dim3(B), dim3(256), 0, stream, target,
                           draft, tokens, temperature, k_offsets, B, g, sp.v0, static_cast<const float2 *>(w.part),

@@ -982,6 +982,7 @@ DeviceState *device_state(int *dev_out) {
     return &st;
 }
 
+
 // Dynamic shared memory of stats_kernel with ns ring slots.
 size_t stats_smem(int ns, int B) {
     size_t s = static_cast<size_t>(ns) * kSlotBytes;
@@ -1122,10 +1123,10 @@ int launch_verify(const void *target, const void *draft, const double *draft_lse
     const cudaError_t e1 =
         draft_lse2 ? launch_k(!after_event, stats_kernel<DT, kModeTarget>, dim3(grid), dim3(kThreads), smem, stream,
                               target, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, w.seqcnt,
-                              nullptr, nullptr, 0, pdl_first ? 2 : 1, w.pairs)
+                              nullptr, nullptr, 0, pdl_first ? 2 : 1, w.pairs, SPEC_STREAM_EVICT_FIRST)
                    : launch_k(!after_event, stats_kernel<DT, kModeVerify>, dim3(grid), dim3(kThreads), smem, stream,
                               target, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, w.seqcnt,
-                              nullptr, nullptr, 0, pdl_first ? 2 : 1, w.pairs);
+                              nullptr, nullptr, 0, pdl_first ? 2 : 1, w.pairs, SPEC_STREAM_EVICT_FIRST);
     if (!cuda_ok(e1, "launch stats_kernel")) return SPEC_ERR_CUDA;
     const int fgrid = defer ? fuse_grid<DT>(st, B) : 0;
     if (fgrid > 0) {
@@ -1185,7 +1186,7 @@ int launch_draft(const void *draft, const float *temperature, const float *u_dra
     // kernel, it waits for it before reading the inputs (wait_first)
     if (!cuda_ok(launch_k(true, stats_kernel<DT, kModeDraft>, dim3(st.sms * per_sm), dim3(kThreads), smem, stream,
                           draft, draft, temperature, k_offsets, B, g, ns, w.part, w.counters, nullptr, nullptr,
-                          nullptr, 0, 1, static_cast<PairRec *>(nullptr)),
+                          nullptr, 0, 1, static_cast<PairRec *>(nullptr), SPEC_STREAM_EVICT_FIRST),
                  "launch stats_kernel") ||
         !cuda_ok(launch_k(true, draft_select_kernel<DT>, dim3(std::max(grid, 1)), dim3(threads),
                           (B + 1) * sizeof(int), stream, draft, temperature, u_draft, k_offsets, B, g,

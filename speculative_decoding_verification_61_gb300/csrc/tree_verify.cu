@@ -872,11 +872,11 @@ int launch_tree(const void *target, const void *draft, const int32_t *node_offse
         VERIFY ? launch_k(false, stats_kernel<DT, kModeTree>, dim3(st.sms * per_sm), dim3(kThreads), smem, stream,
                           target, draft, temperature, node_offsets, B, g, ns, part, counters,
                           static_cast<int *>(nullptr), static_cast<const int *>(nint), static_cast<const int *>(tint), N, 0,
-                          static_cast<PairRec *>(nullptr))
+                          static_cast<PairRec *>(nullptr), SPEC_STREAM_EVICT_FIRST)
                : launch_k(false, stats_kernel<DT, kModeTreeDraft>, dim3(st.sms * per_sm), dim3(kThreads), smem,
                           stream, draft, draft, temperature, node_offsets, B, g, ns, part, counters,
                           static_cast<int *>(nullptr), static_cast<const int *>(nint), static_cast<const int *>(tint), N, 0,
-                          static_cast<PairRec *>(nullptr));
+                          static_cast<PairRec *>(nullptr), SPEC_STREAM_EVICT_FIRST);
     if (!cuda_ok(e, "launch stats_kernel (tree)")) return SPEC_ERR_CUDA;
     if (VERIFY) {
         // kTreeCtas CTAs per tree as one cluster (co-scheduled), launched

@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
     const float *__restrict__ temperature, const int *__restrict__ k_offsets, int B, Geometry g, int ns,
     float2 *__restrict__ part, int *__restrict__ counters, int *__restrict__ seqcnt,
     const int *__restrict__ tree_nint, const int *__restrict__ tree_int, int tree_nodes, int wait_first,
-    PairRec *__restrict__ pairs) {
+    PairRec *__restrict__ pairs, int evict_first_rows) {
     using E = Elem<DT>;
     constexpr bool DRAFT = MODE == kModeDraft;
     constexpr bool TREE = MODE == kModeTree || MODE == kModeTreeDraft;
@@ -324,6 +324,12 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
             int b = 0;
             int islot = 0;
             uint32_t iphase = 0;  // slot and use parity of the next issue
+            // evict_first_rows: the rows pass through L2 as its first
+            // victims, so that the stream does not push out what the
+            // epilogue reads back from L2 (the partials of every row, the
+            // pair list, the offsets)
+            const bool hints = evict_first_rows != 0;
+            const uint64_t evict_first = hints ? l2_policy_evict_first() : 0ull;
             int t = atomicAdd(tickets, 1);
             while (ok) {
                 int64_t u0;
@@ -384,7 +390,11 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
                     const unsigned char *src = static_cast<const unsigned char *>(base_ptr) +
                                                (row * g.V + e0) * static_cast<int64_t>(E::kBytes);
                     mbar_arrive_expect_tx(&full[islot], d.nbytes);
-                    bulk_g2s(ring + static_cast<size_t>(islot) * kSlotBytes, src, d.nbytes, &full[islot]);
+                    if (hints)
+                        bulk_g2s_hint(ring + static_cast<size_t>(islot) * kSlotBytes, src, d.nbytes, &full[islot],
+                                      evict_first);
+                    else
+                        bulk_g2s(ring + static_cast<size_t>(islot) * kSlotBytes, src, d.nbytes, &full[islot]);
                     ++issued;
                     if (++islot == ns) {
                         islot = 0;
