@@ -71,6 +71,30 @@ def test_spec_round_and_verify_under_capture(sv):
     assert torch.equal(vt, out_t) and torch.equal(vn, out_n)
 
 
+@pytest.mark.parametrize("B", [160, 640])
+def test_deferred_epilogue_under_capture(sv, B):
+    """Batches of 128 sequences or more take the deferred epilogue: one launch
+    for decisions and residual stream up to two sequences per resident CTA
+    (B = 160), two launches beyond (B = 640).  Both replay bit for bit."""
+    w = workloads.make_case(B=B, k="ragged_1_10", V=8192, dtype="bf16", temperature="odd_greedy", seed=23 + B,
+                            sigma_d=1.5)
+    d = to_device(w)
+    toks = torch.empty(w.rows_draft, dtype=torch.int32, device="cuda")
+    out_t = torch.empty(w.rows_target, dtype=torch.int32, device="cuda")
+    out_n = torch.empty(w.B, dtype=torch.int32, device="cuda")
+    args = (d["target_logits"], d["draft_logits"], d["u_draft"], d["u_accept"], d["u_resample"], d["temperature"],
+            d["k_offsets"])
+    replay_equals_eager(lambda: sv.spec_round(*args, out_draft_tokens=toks, out_tokens=out_t, out_num_accepted=out_n),
+                        [toks, out_t, out_n])
+    vt = torch.empty_like(out_t)
+    vn = torch.empty_like(out_n)
+    replay_equals_eager(lambda: sv.spec_verify(d["target_logits"], d["draft_logits"], toks, d["u_accept"],
+                                               d["u_resample"], d["temperature"], d["k_offsets"], out_tokens=vt,
+                                               out_num_accepted=vn), [vt, vn])
+    assert torch.equal(vt, out_t) and torch.equal(vn, out_n)
+    assert int((vn.cpu() < torch.from_numpy(np.diff(w.k_offsets))).sum()) > B // 4  # residual draws happened
+
+
 def test_tree_verify_under_capture(sv):
     w = workloads.make_tree_case(B=20, shape=[3, 2], V=8192, dtype="bf16", temperature=1.0, seed=31)
     t = lambda a: (torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16)  # noqa: E731
