@@ -36,6 +36,8 @@ CASES = [
     dict(B=128, k=6, V=3000, dtype="f32", temperature=1.0, sigma_d=0.0),          # q = p: all accepted, no pair
     dict(B=200, k=[i % 11 for i in range(200)], V=16000, dtype="bf16", temperature=0.8),  # ragged, k = 0 included
     dict(B=256, k="ragged_1_10", V=40008, dtype="bf16", temperature="odd_greedy", sigma_d="uniform_0.2_1.5"),
+    dict(B=300, k=[i % 33 for i in range(300)], V=2056, dtype="bf16", temperature=1.0, sigma_d=0.0),  # k 0..32, all accepted
+    dict(B=300, k=[32 - i % 33 for i in range(300)], V=2056, dtype="f32", temperature="odd_greedy", sigma_d=2.5),
 ]
 
 
@@ -45,6 +47,10 @@ def test_deferred_epilogue_matches_the_oracle(sv, case):
     rep = run_and_compare(w)
     if case == 2:
         assert rep["mean_accepted"] == 6.0  # q = p accepts every drafted token
+    if case == 5:
+        # q = p: every sequence accepts all k drafts and draws its bonus
+        # token at position k (up to 32, the last u_resample slot)
+        assert rep["mean_accepted"] == float(np.mean([i % 33 for i in range(300)]))
 
 
 def test_deferred_data_errors_mark_only_their_sequence(sv):
