@@ -119,9 +119,10 @@ static __device__ __forceinline__ bool shard_combine_soft(const float2 *p, int n
 // ============================================================ row records
 // One block per sequence; warp w takes rows w, w + 8, ... of the sequence
 // (its k + 1 target rows, then its k draft rows), so that every record of
-// the call is written.  The k_offsets check and the drafted tokens are read
-// before the wait on stats_kernel; each row's partials and its drafted
-// token's logit are then loaded together.  Partials are at slot r for
+// the call is written.  The k_offsets check, the drafted tokens and their
+// logits in this rank's columns (the call's inputs, complete once
+// stats_kernel has passed its own wait) are read before the wait on
+// stats_kernel; after it, only each row's partials.  Partials are at slot r for
 // target row r and R_t + d for draft row d (the record index), as
 // stats_kernel writes them in verify mode.
 template <int DT>
@@ -131,6 +132,7 @@ __global__ void __launch_bounds__(256) shard_row_kernel(
     const float2 *__restrict__ part, spec_shard_stat_t *__restrict__ out, int *__restrict__ counters) {
     using E = Elem<DT>;
     __shared__ int s_x[kMaxK];
+    __shared__ float s_zx[2 * kMaxK];  // the drafted token's logit in row rr (rr < k: target, else draft)
     const int b = blockIdx.x;
     const bool bad = block_bad_offsets(k_offsets, B);
     int k0 = 0, k = 0, R_t = 0;
@@ -141,6 +143,21 @@ __global__ void __launch_bounds__(256) shard_row_kernel(
         R_t = k_offsets[B] + B;
         c = temp_scale(temperature[b]);
         if (static_cast<int>(threadIdx.x) < k) s_x[threadIdx.x] = tokens[k0 + threadIdx.x];
+    }
+    __syncthreads();
+    if (!bad && c == c && c != 0.0f) {
+        // thread j < 2k: the token's logit in target row j (j < k) or draft
+        // row j - k, if this rank holds its column
+        const int j = threadIdx.x;
+        if (j < 2 * k) {
+            const bool is_t = j < k;
+            const int i = is_t ? j : j - k;
+            const int x = s_x[i];
+            const int64_t row = is_t ? static_cast<int64_t>(k0) + b + i : static_cast<int64_t>(k0) + i;
+            float zx = 0.0f;
+            if (x >= v0 && x - v0 < g.V) zx = E::load1(is_t ? target : draft, row * g.V + (x - v0));
+            s_zx[j] = zx;
+        }
     }
     __syncthreads();
     grid_dependency_wait();
@@ -156,7 +173,6 @@ __global__ void __launch_bounds__(256) shard_row_kernel(
         const bool is_t = rr <= k;
         const int i = is_t ? rr : rr - k - 1;
         const int64_t r = is_t ? static_cast<int64_t>(ot) + i : static_cast<int64_t>(R_t) + k0 + i;
-        const int64_t row = is_t ? static_cast<int64_t>(ot) + i : static_cast<int64_t>(k0) + i;
         const float2 *p = part + r * g.n_sub;
         spec_shard_stat_t rec{-INFINITY, __int_as_float(0x7fc00000), 0.0f, -1};
         if (valid && greedy && is_t) {
@@ -168,11 +184,7 @@ __global__ void __launch_bounds__(256) shard_row_kernel(
             a = warp_arg(a);
             rec = spec_shard_stat_t{a.v, 0.0f, 0.0f, (a.i == -1 || a.i == INT_MAX) ? -1 : a.i + v0};
         } else if (valid && !greedy) {
-            float zx = 0.0f;
-            if (i < k) {
-                const int x = s_x[i];
-                if (x >= v0 && x - v0 < g.V) zx = E::load1(is_t ? target : draft, row * g.V + (x - v0));
-            }
+            const float zx = i < k ? s_zx[is_t ? i : k + i] : 0.0f;
             float M, S;
             if (shard_combine_soft(p, g.n_sub, &M, &S)) {
                 rec = spec_shard_stat_t{M, S, zx, 0};
