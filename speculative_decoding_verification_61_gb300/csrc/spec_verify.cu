@@ -653,9 +653,10 @@ __global__ void __launch_bounds__(kThreads, 2) resid_stream_kernel(
 
 // Units (consecutive chunks of one pair) per ticket of decide_stream_kernel:
 // one ticket, and one check of the pair's flag, per SPEC_FUSE_UNITS copies.
-// Measured on B=256: 1 unit 176.3 µs, 2-4 units 173.2-174.1 µs per verify.
+// Measured (three CTAs per SM, two slots): 1 unit per ticket 4-8 µs slower
+// per B=512 verify or round than 2 units; 4 units 1-2 µs slower on B=256.
 #ifndef SPEC_FUSE_UNITS
-#define SPEC_FUSE_UNITS 3
+#define SPEC_FUSE_UNITS 2
 #endif
 // The deferred epilogue's decisions and residual stream in one launch (for
 // B at most twice the grid).  Each CTA first decides its sequences
@@ -672,7 +673,17 @@ __global__ void __launch_bounds__(kThreads, 2) resid_stream_kernel(
 // occupancy the host queries); should another kernel hold SMs for longer
 // than the bounded wait (2 s), the call reports a time-out, not a hang.
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 2) decide_stream_kernel(
+// Resident decide_stream_kernel CTAs per SM and 32 KB ring slots per CTA:
+// three CTAs of two slots decide more sequences at once than two of three
+// (B=512: 1.1 sequences per CTA instead of 1.7) with the same bytes in flight
+// per SM; measured 3-4 µs faster per B=512 verify, the same on B=256.
+#ifndef SPEC_FUSE_CTAS_PER_SM
+#define SPEC_FUSE_CTAS_PER_SM 3
+#endif
+#ifndef SPEC_FUSE_SLOTS
+#define SPEC_FUSE_SLOTS 2
+#endif
+__global__ void __launch_bounds__(kThreads, SPEC_FUSE_CTAS_PER_SM) decide_stream_kernel(
     const void *__restrict__ target, const void *__restrict__ draft,
     const int32_t *__restrict__ tokens, const float *__restrict__ u_accept,
     const float *__restrict__ u_resample, const float *__restrict__ temperature,
@@ -954,10 +965,12 @@ bool set_stats_attrs_all(DeviceState &st) {
            set_stats_attrs<DT, kModeTarget>(st.smem_optin) &&
            cuda_ok(cudaFuncSetAttribute(resid_stream_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, rs),
                    "cudaFuncSetAttribute(resid_stream_kernel)") &&
-           cuda_ok(cudaFuncSetAttribute(decide_stream_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, rs),
+           cuda_ok(cudaFuncSetAttribute(decide_stream_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(resid_smem(SPEC_FUSE_SLOTS))),
                    "cudaFuncSetAttribute(decide_stream_kernel)") &&
            cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&st.fuse_per_sm[DT == SPEC_F32 ? 0 : 1],
-                                                                 decide_stream_kernel<DT>, kThreads, rs),
+                                                                 decide_stream_kernel<DT>, kThreads,
+                                                                 resid_smem(SPEC_FUSE_SLOTS)),
                    "cudaOccupancyMaxActiveBlocksPerMultiprocessor(decide_stream_kernel)");
 }
 
@@ -1085,7 +1098,7 @@ bool defer_residual(const DeviceState &, int B) { return B >= SPEC_DEFER_MIN_B; 
 #endif
 template <int DT>
 int fuse_grid(const DeviceState &st, int B) {
-    const int g = st.sms * std::min(2, st.fuse_per_sm[DT == SPEC_F32 ? 0 : 1]);
+    const int g = st.sms * std::min(SPEC_FUSE_CTAS_PER_SM, st.fuse_per_sm[DT == SPEC_F32 ? 0 : 1]);
     return (g > 0 && B <= SPEC_FUSE_PER_CTA * g) ? g : 0;
 }
 
@@ -1130,9 +1143,9 @@ int launch_verify(const void *target, const void *draft, const double *draft_lse
     if (!cuda_ok(e1, "launch stats_kernel")) return SPEC_ERR_CUDA;
     const int fgrid = defer ? fuse_grid<DT>(st, B) : 0;
     if (fgrid > 0) {
-        if (!cuda_ok(launch_k(true, decide_stream_kernel<DT>, dim3(fgrid), dim3(kThreads), resid_smem(kResidSlots), stream,
+        if (!cuda_ok(launch_k(true, decide_stream_kernel<DT>, dim3(fgrid), dim3(kThreads), resid_smem(SPEC_FUSE_SLOTS), stream,
                               target, draft, tokens, u_accept, u_resample, temperature, k_offsets, draft_lse2, B, g, w,
-                              out_tokens, out_num, aux, pdl_first ? 0 : 1, kResidSlots),
+                              out_tokens, out_num, aux, pdl_first ? 0 : 1, SPEC_FUSE_SLOTS),
                      "launch decide_stream_kernel"))
             return SPEC_ERR_CUDA;
     } else if (!cuda_ok(launch_k(true, resolve_kernel<DT>, dim3(B * nsplit), dim3(SPEC_RESOLVE_THREADS), 0, stream, target, draft, tokens,

@@ -1,5 +1,5 @@
 """GPU parity of the deferred epilogue (batches of 128 sequences or more).
-Up to two sequences per resident streaming CTA (608 on a 152-SM GPU),
+Up to two sequences per resident streaming CTA (912 on a 152-SM GPU),
 decide_stream_kernel decides and lists the rejected positions and streams
 the listed row pairs in one launch; larger batches take resolve_kernel, then
 resid_stream_kernel; resid_draw_kernel draws in both.  Against the fp64
@@ -7,7 +7,7 @@ oracle on shapes the full-size workloads do not cover: fp32 rows, a batch
 with no rejection at all (all greedy; all accepted), many rejections, ragged
 k with k = 0, data errors, the fused round and a caller workspace.  The
 thresholds are checked by verifying the same sequences as a 127- and a
-128-sequence batch, and as a 600- and a 700-sequence batch."""
+128-sequence batch, and as a 900- and a 1000-sequence batch."""
 from __future__ import annotations
 
 import numpy as np
@@ -123,30 +123,30 @@ def test_deferred_round_and_caller_workspace(sv):
 
 
 def test_large_batch_forms_agree(sv):
-    """The first 600 sequences verified as their own batch (one launch for
-    decisions and residual stream) and inside a 700-sequence batch (decisions,
-    then the residual stream, as two launches) give the oracle's outputs;
-    tokens and accept counts agree exactly between the two."""
-    w = workloads.make_case(B=700, k="ragged_1_10", V=4104, dtype="bf16", seed=513, temperature="odd_greedy",
+    """The first 900 sequences verified as their own batch (one launch for
+    decisions and residual stream) and inside a 1000-sequence batch
+    (decisions, then the residual stream, as two launches) give the oracle's
+    outputs; tokens and accept counts agree exactly between the two."""
+    w = workloads.make_case(B=1000, k="ragged_1_10", V=4104, dtype="bf16", seed=513, temperature="odd_greedy",
                             sigma_d=1.5)
     ods = oracle.draft_sample(w.draft_logits, w.temperature, w.u_draft, w.k_offsets)
     ora = oracle.verify(w.target_logits, w.draft_logits, ods.tokens, w.u_accept, w.u_resample, w.temperature,
                         w.k_offsets)
     d = to_device(w)
     toks = torch.from_numpy(ods.tokens).cuda()
-    t700, n700 = sv.spec_verify(d["target_logits"], d["draft_logits"], toks, d["u_accept"], d["u_resample"],
+    tbig, nbig = sv.spec_verify(d["target_logits"], d["draft_logits"], toks, d["u_accept"], d["u_resample"],
                                 d["temperature"], d["k_offsets"])
-    B1 = 600
+    B1 = 900
     R_d, R_t = int(w.k_offsets[B1]), int(w.k_offsets[B1]) + B1
-    t600, n600 = sv.spec_verify(d["target_logits"][:R_t], d["draft_logits"][:R_d], toks[:R_d],
+    tpre, npre = sv.spec_verify(d["target_logits"][:R_t], d["draft_logits"][:R_d], toks[:R_d],
                                 d["u_accept"][:R_d], d["u_resample"][:R_t], d["temperature"][:B1],
                                 d["k_offsets"][:B1 + 1].contiguous())
     torch.cuda.synchronize()
-    compare_verify(w, t700.cpu().numpy(), n700.cpu().numpy(), None, ora)
-    assert torch.equal(n700[:B1], n600) and torch.equal(t700[:R_t], t600)
+    compare_verify(w, tbig.cpu().numpy(), nbig.cpu().numpy(), None, ora)
+    assert torch.equal(nbig[:B1], npre) and torch.equal(tbig[:R_t], tpre)
     kb = np.diff(w.k_offsets)[:B1]
-    pairs = (n600.cpu().numpy() < kb) & (w.temperature[:B1] > 0)  # sampled sequences with a rejection
+    pairs = (npre.cpu().numpy() < kb) & (w.temperature[:B1] > 0)  # sampled sequences with a rejection
     assert int(pairs.sum()) > 100
     sub = workloads.Workload(**{**w.__dict__, "B": B1, "k_offsets": w.k_offsets[:B1 + 1],
                                 "temperature": w.temperature[:B1]})
-    compare_verify(sub, t600.cpu().numpy(), n600.cpu().numpy(), None, ora, seq_list=range(B1))
+    compare_verify(sub, tpre.cpu().numpy(), npre.cpu().numpy(), None, ora, seq_list=range(B1))
