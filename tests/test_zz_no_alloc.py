@@ -65,6 +65,8 @@ def _noalloc_call(sv, d, toks, V, dtype):
     dict(B=48, k="ragged_1_10", V=32000, dtype="bf16", temperature="odd_greedy", seed=31),
     dict(B=20, k=[0, 1, 2, 3, 5, 8, 13, 21, 32, 4, 7, 1, 2, 2, 6, 9, 10, 3, 1, 1], V=16000,
          dtype="f32", temperature=0.9, seed=32),
+    # a batch of the deferred epilogue (decisions and residual stream in one launch)
+    dict(B=200, k="ragged_1_10", V=8192, dtype="bf16", temperature="odd_greedy", sigma_d=1.5, seed=34),
 ])
 def test_noalloc_matches_spec_verify_twice(sv, case):
     w = workloads.make_case(**case)
