@@ -343,28 +343,38 @@ __global__ void __launch_bounds__(256) shard_decide_kernel(
     __syncthreads();
 
     // --- 1. rows over all ranks -------------------------------------------
+    // A row's G records are combined by a group of gs lanes (the power of
+    // two at or above G, one lane per rank), so that a warp takes 32 / gs
+    // rows at once; with more than 32 ranks, lane l holds ranks l and l + 32.
+    // The group's reductions are the whole warp's with the other groups'
+    // steps left out, which only ever added zeros: the same bits.
     if (!err0) {
         const int nrows = greedy ? k + 1 : 2 * k + 1;
-        for (int rr = warp; rr < nrows; rr += blockDim.x >> 5) {
+        const int nw = blockDim.x >> 5;
+        const int gs = G <= 32 ? (G <= 1 ? 1 : 1 << (32 - __clz(G - 1))) : 32;
+        const int rpw = 32 / gs;  // rows per warp and round
+        const int grp = lane / gs, gl = lane - grp * gs;
+        for (int r0 = warp * rpw; r0 < nrows; r0 += nw * rpw) {
+            const int rr = r0 + grp;
+            const bool active = rr < nrows;
             const bool is_t = rr <= k;
             const int i = is_t ? rr : rr - k - 1;
             const int si = is_t ? i : kMaxK + 1 + i;
             const int64_t rec = is_t ? static_cast<int64_t>(ot) + i : static_cast<int64_t>(R_t) + od + i;
-            // lane l holds the records of ranks l and l + 32 (G <= 64),
-            // each one 16-byte load (m, s, zx, arg)
+            // each lane's records (m, s, zx, arg): rank gl (and gl + 32 when G > 32)
             int4 st[2];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const int h = lane + 32 * j;
-                st[j] = h < G ? __ldg(reinterpret_cast<const int4 *>(all_stats + h * per_rank + rec))
-                              : make_int4(__float_as_int(-INFINITY), 0, 0, INT_MAX);
+                const int h = gl + 32 * j;
+                st[j] = (active && h < G) ? __ldg(reinterpret_cast<const int4 *>(all_stats + h * per_rank + rec))
+                                          : make_int4(__float_as_int(-INFINITY), 0, 0, INT_MAX);
             }
             if (greedy) {
                 ArgPart a{-INFINITY, INT_MAX};
 #pragma unroll
                 for (int j = 0; j < 2; ++j) a = arg_merge(a, ArgPart{__int_as_float(st[j].x), st[j].w});
-                a = warp_arg(a);
-                if (lane == 0) {
+                for (int off = gs >> 1; off > 0; off >>= 1) a = arg_merge(a, shfl_arg(a, off));
+                if (active && gl == 0) {
                     sm.arg[si] = a.i;
                     sm.ok[si] = a.i >= 0 && a.i != INT_MAX;
                 }
@@ -379,22 +389,21 @@ __global__ void __launch_bounds__(256) shard_decide_kernel(
                     nan |= (sh[j] != sh[j]);
                     M = fmaxf(M, mh[j]);
                 }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-                nan = __any_sync(0xffffffffu, nan);
+                for (int off = gs >> 1; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+                const unsigned gmask = (gs == 32 ? 0xffffffffu : ((1u << gs) - 1u)) << (grp * gs);
+                nan = (__ballot_sync(0xffffffffu, nan) & gmask) != 0u;
                 Acc2 acc;
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
                     if (mh[j] > -INFINITY) acc.add(sh[j] * ex2(mh[j] - M));
-                const float S = warp_sum_f(acc.value());
+                float S = acc.value();
+                for (int off = gs >> 1; off > 0; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
                 const bool ok = !nan && M > -INFINITY && M < INFINITY && S > 0.0f && S < INFINITY;
-                // the drafted token's logit, from the lane holding its rank
-                float z = 0.0f;
-                if (i < k) {
-                    const int h = sm.xr[i];
-                    z = __shfl_sync(0xffffffffu, __int_as_float(h < 32 ? st[0].z : st[1].z), h & 31);
-                }
-                if (lane == 0) {
+                // the drafted token's logit, from the group's lane holding its rank
+                const int h = (active && i < k) ? sm.xr[i] : 0;
+                const float z = __shfl_sync(0xffffffffu, __int_as_float(h < 32 ? st[0].z : st[1].z),
+                                            grp * gs + (h & 31) % gs);
+                if (active && gl == 0) {
                     if (is_t) {
                         sm.M[i] = M;
                         sm.S[i] = S;
