@@ -65,6 +65,9 @@
  *     that word holds it every verify or draft-sampling call on the
  *     workspace reports all its sequences (rows) as data errors (-1) rather
  *     than outputs that look valid; clear it with spec_workspace_status.
+ *     Some kernels' CTAs wait on one another (they are launched no wider
+ *     than the GPU holds at once); another workload that keeps SMs busy for
+ *     longer than the limit can therefore make a call time out.
  *   - Temperature: every row of sequence b, target and draft, is divided by
  *     T_b before the softmax.
  *   - Randomness is never drawn inside the library: all uniforms are inputs,
