@@ -78,15 +78,42 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "spec_round_traffic_B512_ragged_k1
 VERIFY_SOURCES = ("spec_verify.cu", "device_utils.cuh", "verify_common.cuh", "host_common.h")
 
 
+def strip_comments(src: str) -> str:
+    """C++ source without its // and /* */ comments and without blank lines
+    (string and character literals kept as they are), so that an edit of a
+    comment leaves the code's hash alone."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = ("".join(out)).split("\n")
+    return "\n".join(ln.rstrip() for ln in lines if ln.strip())
+
+
 def kernel_source_hash() -> str:
-    """sha256 over the sources of spec_verify's kernels (names and contents)."""
+    """sha256 over the code of spec_verify's kernels (file names and their
+    sources without comments)."""
     import hashlib
     d = os.path.join(ROOT, "speculative_decoding_verification_61_gb300", "csrc")
     h = hashlib.sha256()
     for name in VERIFY_SOURCES:
         h.update(name.encode())
-        with open(os.path.join(d, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(d, name), encoding="utf-8") as f:
+            h.update(strip_comments(f.read()).encode())
     return h.hexdigest()
 
 

@@ -17,17 +17,26 @@
 //                      softmax partial (max m, sum 2^(x c - m)) or, for
 //                      greedy rows, an arg-max partial.  Each row is read
 //                      from HBM once.
-//   2. resolve_kernel  kSub blocks per sequence: each combines the partials
-//                      of the sequence's rows, forms alpha_i and finds the
-//                      first rejection with a warp ballot; on a rejection the
-//                      blocks share the residual mass max(0, p - q) of the two
-//                      rows at that position, and the last warp to finish
-//                      locates the sub-chunk where the cumulative mass crosses
-//                      u * Z, re-reads only that piece and finds the token
-//                      with a warp scan.  The bonus draw uses the partials of
-//                      row k the same way.
+//   2. the epilogue, by batch size:
+//      B < 128         resolve_kernel, up to kSub blocks per sequence: each
+//                      combines the partials of the sequence's rows, forms
+//                      alpha_i and finds the first rejection with a warp
+//                      ballot; on a rejection the blocks share the residual
+//                      mass max(0, p - q) of the two rows at that position,
+//                      and the last block to finish locates the sub-chunk
+//                      where the cumulative mass crosses u * Z, re-reads only
+//                      that piece and finds the token with a block scan.
+//                      The bonus draw uses the partials of row k the same way.
+//      B >= 128        decide_stream_kernel (up to two sequences per
+//                      resident CTA) decides every sequence and streams the
+//                      rejected positions' row pairs into residual masses in
+//                      one launch; beyond that, resolve_kernel decides and
+//                      resid_stream_kernel streams.  resid_draw_kernel then
+//                      draws each residual token (block per pair).
 // spec_draft_sample runs stats_kernel over the draft rows, then
 // draft_select_kernel (arg-max, or the same locate + scan per row).
+// spec_round chains both passes in one call: the target pass streams while
+// the draft tokens are still being drawn.
 
 #include <algorithm>
 #include <climits>
