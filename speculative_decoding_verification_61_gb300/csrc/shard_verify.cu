@@ -80,9 +80,9 @@ __device__ __forceinline__ bool block_bad_offsets(const int *__restrict__ k_offs
 // A row's combine over this shard's sub-chunk partials: M = the largest
 // partial maximum (-inf when no column is finite), S = sum s_i 2^(m_i - M)
 // (0 then).  False when a partial carries NaN (a NaN or +inf column).
-static __device__ __forceinline__ bool shard_combine_soft(const float2 *p, int n, float *M_out, float *S_out) {
-    float2 cache[kPartCache];
-    load_parts(p, n, cache);
+// cache: the row's first 32 * kPartCache partials (load_parts).
+static __device__ __forceinline__ bool shard_combine_soft(const float2 (&cache)[kPartCache], const float2 *p, int n,
+                                                          float *M_out, float *S_out) {
     const int lane = lane_id();
     float M = -INFINITY;
     bool nan = false;
@@ -125,8 +125,9 @@ static __device__ __forceinline__ bool shard_combine_soft(const float2 *p, int n
 // stats_kernel; after it, only each row's partials.  Partials are at slot r for
 // target row r and R_t + d for draft row d (the record index), as
 // stats_kernel writes them in verify mode.
+// (four blocks per SM: a 512-sequence batch is resident at once)
 template <int DT>
-__global__ void __launch_bounds__(256) shard_row_kernel(
+__global__ void __launch_bounds__(256, 4) shard_row_kernel(
     const void *__restrict__ target, const void *__restrict__ draft, const int32_t *__restrict__ tokens,
     const float *__restrict__ temperature, const int *__restrict__ k_offsets, int B, Geometry g, int v0,
     const float2 *__restrict__ part, spec_shard_stat_t *__restrict__ out, int *__restrict__ counters) {
@@ -169,15 +170,46 @@ __global__ void __launch_bounds__(256) shard_row_kernel(
     const int lane = lane_id();
     const int ot = k0 + b;
     const bool greedy = c == 0.0f, valid = c == c;
-    for (int rr = warp_id(); rr < 2 * k + 1; rr += blockDim.x >> 5) {
+    const int nrows = 2 * k + 1, nw = blockDim.x >> 5;
+    // record index of row rr (target rows first) and whether it is combined
+    auto rec_of = [&](int rr) -> int64_t {
+        return rr <= k ? static_cast<int64_t>(ot) + rr : static_cast<int64_t>(R_t) + k0 + (rr - k - 1);
+    };
+    auto combined = [&](int rr) -> bool { return valid && (!greedy || rr <= k); };
+    // the first 32 partials of a warp's next kAhead rows are requested
+    // together (whole rows when a shard has at most 32 sub-chunks), so that
+    // its rows wait on L2 once rather than one after another
+    constexpr int kAhead = 3;
+    auto first_part = [&](int rr) -> float2 {
+        return (rr < nrows && combined(rr) && lane < g.n_sub) ? __ldcg(part + rec_of(rr) * g.n_sub + lane)
+                                                               : make_float2(-INFINITY, 0.0f);
+    };
+    float2 ahead[kAhead];
+#pragma unroll
+    for (int q = 0; q < kAhead; ++q) ahead[q] = first_part(warp_id() + q * nw);
+    for (int rr = warp_id(); rr < nrows; rr += nw) {
         const bool is_t = rr <= k;
         const int i = is_t ? rr : rr - k - 1;
-        const int64_t r = is_t ? static_cast<int64_t>(ot) + i : static_cast<int64_t>(R_t) + k0 + i;
+        const int64_t r = rec_of(rr);
         const float2 *p = part + r * g.n_sub;
+        // the row's cache as load_parts fills it, its first entry requested earlier
+        float2 cur[kPartCache];
+        cur[0] = ahead[0];
+#pragma unroll
+        for (int q = 0; q + 1 < kAhead; ++q) ahead[q] = ahead[q + 1];
+        ahead[kAhead - 1] = first_part(rr + kAhead * nw);
+#pragma unroll
+        for (int j = 1; j < kPartCache; ++j) {
+            const int e = lane + 32 * j;
+            cur[j] = (combined(rr) && e < g.n_sub) ? __ldcg(p + e) : make_float2(-INFINITY, 0.0f);
+        }
         spec_shard_stat_t rec{-INFINITY, __int_as_float(0x7fc00000), 0.0f, -1};
         if (valid && greedy && is_t) {
             ArgPart a{-INFINITY, INT_MAX};
-            for (int j = lane; j < g.n_sub; j += 32) {
+#pragma unroll
+            for (int j = 0; j < kPartCache; ++j)
+                if (lane + 32 * j < g.n_sub) a = arg_merge(a, ArgPart{cur[j].x, __float_as_int(cur[j].y)});
+            for (int j = lane + 32 * kPartCache; j < g.n_sub; j += 32) {
                 const float2 v = __ldcg(p + j);
                 a = arg_merge(a, ArgPart{v.x, __float_as_int(v.y)});
             }
@@ -186,7 +218,7 @@ __global__ void __launch_bounds__(256) shard_row_kernel(
         } else if (valid && !greedy) {
             const float zx = i < k ? s_zx[is_t ? i : k + i] : 0.0f;
             float M, S;
-            if (shard_combine_soft(p, g.n_sub, &M, &S)) {
+            if (shard_combine_soft(cur, p, g.n_sub, &M, &S)) {
                 rec = spec_shard_stat_t{M, S, zx, 0};
             } else {
                 rec = spec_shard_stat_t{-INFINITY, __int_as_float(0x7fc00000), zx, 0};
@@ -199,10 +231,13 @@ __global__ void __launch_bounds__(256) shard_row_kernel(
 // ================================================================ decide
 // This rank's residual masses max(0, p - q) of one (target, draft) row pair,
 // per sub-chunk of its columns, by all warps of the block; warp 0 first
-// moves both rows to L2 in bulk so that the loads wait on L2.
+// moves both rows to L2 in bulk so that the loads wait on L2.  The masses
+// go to rp, and the first 32 * kPartCache also to rp_s (shared memory) for
+// the block's own total.
 template <int DT>
 __device__ void shard_resid_pass(const void *target, const void *draft, int64_t trow, int64_t drow,
-                                 const Geometry &g, float c, float lth, float ltl, float ldh, float ldl, float *rp) {
+                                 const Geometry &g, float c, float lth, float ltl, float ldh, float ldl, float *rp,
+                                 float *rp_s) {
     using E = Elem<DT>;
     const int lane = lane_id(), warp = warp_id(), nwarps = blockDim.x >> 5;
     const unsigned char *t0 = static_cast<const unsigned char *>(target) + trow * g.V * static_cast<int64_t>(E::kBytes);
@@ -243,7 +278,10 @@ __device__ void shard_resid_pass(const void *target, const void *draft, int64_t 
             }
         }
         const float sum = warp_sum_f((acc0.x + acc0.y) + (acc1.x + acc1.y));
-        if (lane == 0) rp[sc] = sum;
+        if (lane == 0) {
+            rp[sc] = sum;
+            if (sc < 32 * kPartCache) rp_s[sc] = sum;
+        }
     }
 }
 
@@ -276,6 +314,13 @@ __device__ __forceinline__ void r_weights_cached(const float *r, int n, float (&
     for (int j = 0; j < kPartCache; ++j) w[j] = (lane + 32 * j < n) ? __ldcg(r + lane + 32 * j) : 0.0f;
 }
 
+// the same from the block's shared copy of its first masses
+__device__ __forceinline__ void r_weights_shared(const float *r_s, int n, float (&w)[kPartCache]) {
+    const int lane = lane_id();
+#pragma unroll
+    for (int j = 0; j < kPartCache; ++j) w[j] = (lane + 32 * j < n) ? r_s[lane + 32 * j] : 0.0f;
+}
+
 struct DecideSmem {
     float M[kMaxK + 1];        // target rows: global max of z c
     float S[kMaxK + 1];        // target rows: sum of 2^(z c - M) over all ranks
@@ -289,6 +334,7 @@ struct DecideSmem {
     int bound[kMaxShards + 1];
     int n, kind;
     float lth, ltl, ldh, ldl, Mn;
+    float rp[32 * kPartCache];  // this rank's first residual masses (shard_resid_pass)
 };
 
 // One block per sequence.  Phase 1: the gathered records of each needed row
@@ -331,6 +377,35 @@ __global__ void __launch_bounds__(256) shard_decide_kernel(
     const int G = sp.G;
     for (int i = threadIdx.x; i <= G; i += blockDim.x) sm.bound[i] = sp.bound[i];
     const int V = sp.bound[G];
+
+    // A row's G records are combined by a group of gs lanes (the power of
+    // two at or above G, one lane per rank), so that a warp takes 32 / gs
+    // rows at once; with more than 32 ranks, lane l holds ranks l and l + 32.
+    const int nrows = greedy ? k + 1 : 2 * k + 1;
+    const int nw = blockDim.x >> 5;
+    const int gs = G <= 32 ? (G <= 1 ? 1 : 1 << (32 - __clz(G - 1))) : 32;
+    const int rpw = 32 / gs;  // rows per warp and round
+    const int grp = lane / gs, gl = lane - grp * gs;
+    // each lane's records (m, s, zx, arg) of row r0 + grp: rank gl (and gl + 32);
+    // a greedy sequence's draft records are loaded too, unused (so that the
+    // loads need k_offsets alone, not the temperature)
+    auto load_recs = [&](int r0, int4 (&st)[2]) {
+        const int rr = r0 + grp;
+        const bool active = rr < 2 * k + 1;
+        const bool is_t = rr <= k;
+        const int i = is_t ? rr : rr - k - 1;
+        const int64_t rec = is_t ? static_cast<int64_t>(ot) + i : static_cast<int64_t>(R_t) + od + i;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int h = gl + 32 * j;
+            st[j] = (active && h < G) ? __ldg(reinterpret_cast<const int4 *>(all_stats + h * per_rank + rec))
+                                      : make_int4(__float_as_int(-INFINITY), 0, 0, INT_MAX);
+        }
+    };
+    // the first round's records are requested before the drafted tokens, so
+    // that both wait on memory together
+    int4 st0[2];
+    load_recs(warp * rpw, st0);
     int xbad = 0;
     if (static_cast<int>(threadIdx.x) < k) {
         const int x = tokens[od + threadIdx.x];
@@ -343,31 +418,21 @@ __global__ void __launch_bounds__(256) shard_decide_kernel(
     __syncthreads();
 
     // --- 1. rows over all ranks -------------------------------------------
-    // A row's G records are combined by a group of gs lanes (the power of
-    // two at or above G, one lane per rank), so that a warp takes 32 / gs
-    // rows at once; with more than 32 ranks, lane l holds ranks l and l + 32.
     // The group's reductions are the whole warp's with the other groups'
     // steps left out, which only ever added zeros: the same bits.
     if (!err0) {
-        const int nrows = greedy ? k + 1 : 2 * k + 1;
-        const int nw = blockDim.x >> 5;
-        const int gs = G <= 32 ? (G <= 1 ? 1 : 1 << (32 - __clz(G - 1))) : 32;
-        const int rpw = 32 / gs;  // rows per warp and round
-        const int grp = lane / gs, gl = lane - grp * gs;
         for (int r0 = warp * rpw; r0 < nrows; r0 += nw * rpw) {
             const int rr = r0 + grp;
             const bool active = rr < nrows;
             const bool is_t = rr <= k;
             const int i = is_t ? rr : rr - k - 1;
             const int si = is_t ? i : kMaxK + 1 + i;
-            const int64_t rec = is_t ? static_cast<int64_t>(ot) + i : static_cast<int64_t>(R_t) + od + i;
-            // each lane's records (m, s, zx, arg): rank gl (and gl + 32 when G > 32)
             int4 st[2];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int h = gl + 32 * j;
-                st[j] = (active && h < G) ? __ldg(reinterpret_cast<const int4 *>(all_stats + h * per_rank + rec))
-                                          : make_int4(__float_as_int(-INFINITY), 0, 0, INT_MAX);
+            if (r0 == warp * rpw) {
+                st[0] = st0[0];
+                st[1] = st0[1];
+            } else {
+                load_recs(r0, st);
             }
             if (greedy) {
                 ArgPart a{-INFINITY, INT_MAX};
@@ -523,14 +588,14 @@ __global__ void __launch_bounds__(256) shard_decide_kernel(
     if (warp == 0) p_weights_cached(pw, g.n_sub, w);  // p of row n: the bonus, or a zero residual's fallback
     if (kind == kJobResid) {
         shard_resid_pass<DT>(target, draft, trow, static_cast<int64_t>(od) + n, g, c, sm.lth, sm.ltl, sm.ldh, sm.ldl,
-                             rp);
+                             rp, sm.rp);
         __syncthreads();  // every warp's masses, before warp 0 sums them
     }
     if (warp != 0) return;
     const F2 Zp = warp_total(g.n_sub, w, pw);
     F2 Z = Zp;
     if (kind == kJobResid) {
-        r_weights_cached(rp, g.n_sub, w);
+        r_weights_shared(sm.rp, g.n_sub, w);
         Z = warp_total(g.n_sub, w, RWeights{rp});
     }
     if (lane == 0) {

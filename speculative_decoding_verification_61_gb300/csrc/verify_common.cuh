@@ -140,13 +140,13 @@ static __device__ int block_excl_scan(int v, int *s_warp, int *total) {
 // kStatsTailBatch, which keeps the finishing times within a fraction of a
 // microsecond without an atomic per unit.
 #ifndef SPEC_STATS_BATCH
-#define SPEC_STATS_BATCH 4
+#define SPEC_STATS_BATCH 2
 #endif
 #ifndef SPEC_STATS_TAIL_BATCH
 #define SPEC_STATS_TAIL_BATCH 1
 #endif
 #ifndef SPEC_STATS_TAIL_PER_CTA
-#define SPEC_STATS_TAIL_PER_CTA 8
+#define SPEC_STATS_TAIL_PER_CTA 2
 #endif
 constexpr int kStatsBatch = SPEC_STATS_BATCH;
 constexpr int kStatsTailBatch = SPEC_STATS_TAIL_BATCH;
@@ -340,6 +340,15 @@ __global__ void __launch_bounds__(kThreads, 5) stats_kernel(
                 cnt = static_cast<int>(min(static_cast<int64_t>(cnt), total_units - u0));
                 int r = static_cast<int>(u0 / g.n_chunks);
                 int ch = static_cast<int>(u0 - static_cast<int64_t>(r) * g.n_chunks);
+                if (s_rowpre[b + 1] <= r) {
+                    // a new batch can lie many sequences ahead (short rows):
+                    // the last b with s_rowpre[b] <= r (s_rowpre is
+                    // non-decreasing and s_rowpre[b] <= r already), by
+                    // binary lifting; within the batch b moves on one
+                    // sequence at a time
+                    for (int step = 1 << (31 - __clz(B)); step > 0; step >>= 1)
+                        if (b + step < B && s_rowpre[b + step] <= r) b += step;
+                }
                 for (int q = 0; q < cnt; ++q) {
                     if (issued >= ns && !mbar_wait_bounded(&empty[islot], iphase ^ 1u)) {
                         ok = false;
