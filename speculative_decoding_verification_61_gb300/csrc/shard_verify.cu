@@ -356,6 +356,10 @@ __global__ void __launch_bounds__(256) shard_decide_kernel(
     const int lane = lane_id(), warp = warp_id();
     grid_dependency_wait();
     grid_launch_dependents();
+    // the sequence's own offsets and temperature (in bounds whatever the
+    // offsets hold) are requested with the check's loads
+    const int kb0 = k_offsets[b], kb1 = k_offsets[b + 1], kbB = k_offsets[B];
+    const float temp_b = temperature[b];
     if (block_bad_offsets(k_offsets, B)) {
         // the whole call fails; outputs of unknown size stay untouched
         if (threadIdx.x == 0) {
@@ -367,12 +371,12 @@ __global__ void __launch_bounds__(256) shard_decide_kernel(
         }
         return;
     }
-    const int k0 = k_offsets[b];
-    const int k = k_offsets[b + 1] - k0;
+    const int k0 = kb0;
+    const int k = kb1 - k0;
     const int ot = k0 + b, od = k0;
-    const int R_t = k_offsets[B] + B;
-    const int64_t per_rank = static_cast<int64_t>(R_t) + k_offsets[B];  // records per rank
-    const float c = temp_scale(temperature[b]);
+    const int R_t = kbB + B;
+    const int64_t per_rank = static_cast<int64_t>(R_t) + kbB;  // records per rank
+    const float c = temp_scale(temp_b);
     const bool greedy = c == 0.0f;
     const int G = sp.G;
     for (int i = threadIdx.x; i <= G; i += blockDim.x) sm.bound[i] = sp.bound[i];
