@@ -159,6 +159,32 @@ def test_data_errors_mark_only_their_sequence():
     compare_verify(w2, gt.cpu().numpy(), gn, {k: v.cpu().numpy() for k, v in ga.items()}, ora)
 
 
+@pytest.mark.parametrize("B", [100, 600, 1000])
+def test_runs_of_rowless_sequences_between_short_rows(B):
+    """A sequence with a bad temperature streams no rows.  Runs of 40 such
+    sequences (one at the batch's end) between sequences that do stream, in
+    rows of one 8 KB chunk, so that one ticket of a streaming pass lies many
+    sequences ahead and the producer's search for a row's sequence must step
+    over the row-less ones: the draft draws and the verify outputs equal the
+    oracle's, and every row-less sequence is a data error.  The three batch
+    sizes take the one-kernel epilogue, the one-launch deferred epilogue and
+    the two-launch one."""
+    w = workloads.make_case(B=B, k="ragged_1_10", V=4096, dtype="bf16", seed=60 + B, temperature="odd_greedy")
+    temp = w.temperature.copy()
+    bad = np.zeros(B, dtype=bool)
+    for start in range(3, B, 97):
+        bad[start:start + 40] = True
+    bad[B - 40:] = True
+    temp[bad] = -1.0
+    w2 = workloads.Workload(**{**w.__dict__, "temperature": temp})
+    rep = run_and_compare(w2)
+    assert rep["sequences"] == B
+    ora = oracle.verify(w2.target_logits, w2.draft_logits,
+                        oracle.draft_sample(w2.draft_logits, temp, w2.u_draft, w2.k_offsets).tokens,
+                        w2.u_accept, w2.u_resample, temp, w2.k_offsets)
+    assert (ora.num_accepted[bad] == -1).all() and (ora.num_accepted[~bad] >= 0).all()
+
+
 def test_invalid_k_offsets_fail_the_call_on_device():
     import speculative_decoding_verification_61_gb300 as sv
     w = workloads.make_case(B=4, k=2, V=1000, seed=2)

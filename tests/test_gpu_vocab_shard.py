@@ -180,6 +180,22 @@ def test_vocab_shard_data_errors(sv):
         assert (per_rank[:, k0 + b:k1 + b + 1] == -1).all(), b
 
 
+def test_vocab_shard_runs_of_rowless_sequences(sv):
+    """Runs of sequences with a bad temperature (no rows streamed) between
+    rows of one chunk per rank (G = 8 ranks of 1024 columns): every rank's
+    streaming pass steps over them, the rest equal the oracle's outputs."""
+    w = workloads.make_case(B=300, k="ragged_1_10", V=8192, dtype="bf16", temperature="odd_greedy", seed=93)
+    temp = w.temperature.copy()
+    bad = np.zeros(w.B, dtype=bool)
+    for start in range(2, w.B, 61):
+        bad[start:start + 30] = True
+    bad[w.B - 20:] = True
+    temp[bad] = -1.0
+    w2 = workloads.Workload(**{**w.__dict__, "temperature": temp})
+    got, num = run_case(sv, w2, even(w2.V, 8))
+    assert (num[bad] == -1).all() and (num[~bad] >= 0).all()
+
+
 def test_vocab_shard_invalid_offsets_fail_on_device(sv):
     from speculative_decoding_verification_61_gb300.vocab_shard import VocabShardVerifier
     w = workloads.make_case(B=4, k=3, V=2048, dtype="bf16", seed=5)
