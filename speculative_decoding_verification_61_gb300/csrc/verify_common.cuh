@@ -146,7 +146,7 @@ static __device__ int block_excl_scan(int v, int *s_warp, int *total) {
 #define SPEC_STATS_TAIL_BATCH 1
 #endif
 #ifndef SPEC_STATS_TAIL_PER_CTA
-#define SPEC_STATS_TAIL_PER_CTA 2
+#define SPEC_STATS_TAIL_PER_CTA 1
 #endif
 constexpr int kStatsBatch = SPEC_STATS_BATCH;
 constexpr int kStatsTailBatch = SPEC_STATS_TAIL_BATCH;
