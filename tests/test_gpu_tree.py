@@ -117,6 +117,31 @@ def test_tree_draft_sample_parity(sv):
     assert (gd[w.parent < 0] == -1).all()
 
 
+def test_tree_runs_of_rowless_trees(sv):
+    """Runs of trees with a bad temperature (no rows streamed; one run at the
+    batch's end) between trees whose rows are one chunk, so that a ticket of
+    the streaming passes lies many trees ahead: the drafting and the verify
+    equal the oracle's outputs, and every row-less tree is -1."""
+    w = workloads.make_tree_case(B=300, shape=[2, 2], V=4096, dtype="bf16", temperature=1.0, sigma_d=1.0,
+                                 seed=590)
+    temp = w.temperature.copy()
+    bad = np.zeros(w.B, dtype=bool)
+    for start in range(1, w.B, 53):
+        bad[start:start + 25] = True
+    bad[w.B - 15:] = True
+    temp[bad] = -1.0
+    w2 = workloads.TreeWorkload(**{**w.__dict__, "temperature": temp})
+    d = tree_inputs(w2)
+    gd = sv.spec_tree_draft_sample(d["draft_logits"], d["node_offsets"], d["parent"], d["temperature"],
+                                   d["u_draft"]).cpu().numpy()
+    od = oracle.tree_draft_sample(w2.draft_logits, w2.node_offsets, w2.parent, temp, w2.u_draft)
+    ok = od.margin > FLAG_MARGIN
+    assert (gd[ok] == od.tokens[ok]).all()
+    got, ora = run_tree_parity(sv, w2)
+    n = got[1].cpu().numpy()
+    assert (n[bad] == -1).all() and (ora.num_accepted[bad] == -1).all() and (n[~bad] >= 0).all()
+
+
 def test_tree_data_errors(sv):
     w = workloads.make_tree_case(B=6, shape=[2, 1], V=4096, dtype="f32", seed=88)
     tl = w.target_logits.copy()
