@@ -134,6 +134,9 @@ struct TreeWalkSmem {
     int ok[kMaxTreeNodes];      // i's target row is valid
     int okd[kMaxTreeNodes];     // i's draft row is valid (or not needed)
     int path[kMaxTreeNodes];    // accepted tokens
+    int isint[kMaxTreeNodes];   // i has a child (an internal node)
+    int ilist[kMaxTreeNodes];   // the internal nodes in ascending order
+    int nil;                    // their count
     double t;                   // residual level of the current p at the node (0: p itself)
     float S;                    // its mass S(t)
     int next;                   // accepted child (local index) or -1
@@ -369,18 +372,39 @@ __global__ void __launch_bounds__(kWalkThreads, kWalkMinBlocks) tree_walk_kernel
     // a greedy walk makes no pass: CTA 0 does it alone
     if (greedy && cr != 0) return;
     const int V = g.V;
-    bool tokbad = false;
+    bool tokbad = false, parbad = false;
+    if (tid < kMaxTreeNodes) sm.isint[tid] = 0;
     if (tid < n) {
         const int pa = parent[g0 + tid];
-        sm.par[tid] = pa < 0 ? -1 : pa - g0;
+        const int lp = pa < 0 ? -1 : pa - g0;
+        sm.par[tid] = lp;
+        // the setup kernel's rule: the root first (parent -1), every other
+        // node's parent an earlier node of the tree
+        parbad = tid == 0 ? lp != -1 : (lp < 0 || lp >= tid);
         const int x = tokens[g0 + tid];
         sm.tok[tid] = x;
         tokbad = tid > 0 && (x < 0 || x >= V);
     }
     tokbad = __syncthreads_or(tokbad);
+    // the internal nodes (those with a child) in ascending order, as the
+    // setup kernel lists them for the streaming pass, found here from the
+    // parents so that the prologue's loads wait on nothing the setup kernel
+    // wrote (its count, read below, still marks a tree it found invalid)
+    if (tid > 0 && tid < n && !parbad) sm.isint[sm.par[tid]] = 1;
+    parbad = __syncthreads_or(parbad);
+    if (warp == 0) {
+        const bool f0 = lane < n && sm.isint[lane] != 0, f1 = lane + 32 < n && sm.isint[lane + 32] != 0;
+        const unsigned m0 = __ballot_sync(0xffffffffu, f0), m1 = __ballot_sync(0xffffffffu, f1);
+        const unsigned below = (1u << lane) - 1u;
+        if (f0) sm.ilist[__popc(m0 & below)] = lane;
+        if (f1) sm.ilist[__popc(m0) + __popc(m1 & below)] = lane + 32;
+        if (lane == 0) sm.nil = __popc(m0) + __popc(m1);
+    }
+    __syncthreads();
     grid_dependency_wait();
+    const int nint_b = nint[b];  // -1: the setup kernel found the tree invalid
 
-    bool err = (c != c) || tokbad || nint[b] < 0;
+    bool err = (c != c) || tokbad || parbad;
     int u = 0, nacc = 0, final_token = -1;
     // per-sub-chunk masses, two buffers used in turn by successive passes
     // (a CTA may start the next pass while the other still reads the last)
@@ -429,9 +453,7 @@ __global__ void __launch_bounds__(kWalkThreads, kWalkMinBlocks) tree_walk_kernel
             sm.ua[tid] = u_accept[g0 + tid];
             // a leaf's draft row is not needed; an internal node's okd is
             // written by its row's combine below (no other write, no race)
-            bool internal = false;
-            for (int i = tid + 1; i < n; ++i) internal |= sm.par[i] == tid;
-            if (!internal) sm.okd[tid] = 1;
+            if (!sm.isint[tid]) sm.okd[tid] = 1;
         }
         // every child's logits at its token (two loads from HBM each): issued
         // now, stored to shared memory after the rows' combine below
@@ -441,12 +463,12 @@ __global__ void __launch_bounds__(kWalkThreads, kWalkMinBlocks) tree_walk_kernel
             zt_own = E::load1(target, prow * V + sm.tok[tid]);
             zd_own = E::load1(draft, prow * V + sm.tok[tid]);
         }
-        const int items = n + (greedy ? 0 : nint[b]);
+        const int items = n + (greedy ? 0 : sm.nil);
         // partials of item k: target row of node k, or the draft row of the
         // (k - n)-th internal node
         auto item_part = [&](int k) -> const float2 * {
             const int64_t slot = k < n ? static_cast<int64_t>(g0) + k
-                                       : static_cast<int64_t>(N) + tint[b * kMaxTreeNodes + (k - n)];
+                                       : static_cast<int64_t>(N) + g0 + sm.ilist[k - n];
             return part + slot * g.n_sub;
         };
         auto store_soft = [&](int k, bool ok, float M, float S) {
@@ -461,7 +483,7 @@ __global__ void __launch_bounds__(kWalkThreads, kWalkMinBlocks) tree_walk_kernel
                     sm.ltl[k] = static_cast<float>(Lt - static_cast<double>(sm.lth[k]));
                 }
             } else {
-                const int i = tint[b * kMaxTreeNodes + (k - n)] - g0;
+                const int i = sm.ilist[k - n];
                 sm.okd[i] = ok;
                 if (ok) {
                     const double Ld = lse2(M, S);
@@ -502,6 +524,8 @@ __global__ void __launch_bounds__(kWalkThreads, kWalkMinBlocks) tree_walk_kernel
         }
         __syncthreads();
     }
+    // the setup kernel's verdict on the parent array (the rule of parbad)
+    err = err || nint_b < 0;
 
     for (int step = 0; !err && step < n; ++step) {
         const int64_t urow = g0 + u;
