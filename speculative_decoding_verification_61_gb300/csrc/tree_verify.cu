@@ -747,6 +747,24 @@ __global__ void selfcheck_wait_kernel(int *counters, int *never) {
 // draft row (partials at slot parent, stats_kernel tree-draft mode):
 // arg-max at T = 0, else the inverse-CDF draw at u_draft[node].  Roots,
 // invalid sequences and invalid rows give -1.
+// A node's sequence (by bisection of the node offsets in shared memory),
+// parent, temperature scale and drafting uniform.
+struct TreeNodeIn {
+    int lo, pa;
+    float c, ud;
+};
+
+__device__ __forceinline__ TreeNodeIn tree_node_inputs(const int *s_no, int B, const int *__restrict__ parent,
+                                                       const float *__restrict__ temperature,
+                                                       const float *__restrict__ u_draft, int node) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_no[mid] <= node) lo = mid; else hi = mid - 1;
+    }
+    return TreeNodeIn{lo, parent[node], temp_scale(temperature[lo]), u_draft[node]};
+}
+
 template <int DT>
 __global__ void __launch_bounds__(256) tree_draft_select_kernel(
     const void *__restrict__ draft, const int *__restrict__ node_offsets, const int *__restrict__ parent,
@@ -768,32 +786,39 @@ __global__ void __launch_bounds__(256) tree_draft_select_kernel(
         if (i == B && v != N) s_bad = 1;
     }
     __syncthreads();
+    const int lane = lane_id();
+    const int nw = (gridDim.x * blockDim.x) >> 5;
+    const int node0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    // a node's sequence, parent, temperature and uniform: the caller's
+    // inputs, complete once the call's first kernel passed its wait, so the
+    // first node's are read before this kernel's wait
+    TreeNodeIn in{0, -1, 0.0f, 0.0f};
+    if (!s_bad && node0 < N) in = tree_node_inputs(s_no, B, parent, temperature, u_draft, node0);
     grid_dependency_wait();
     grid_launch_dependents();
     if (s_bad) {
         if (blockIdx.x == 0 && threadIdx.x == 0) set_status(counters + kStatus, SPEC_ERR_INVALID_ARG);
         return;
     }
-    const int lane = lane_id();
-    const int nw = (gridDim.x * blockDim.x) >> 5;
-    for (int node = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; node < N; node += nw) {
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (s_no[mid] <= node) lo = mid; else hi = mid - 1;
-        }
-        const int pa = parent[node];
-        const float c = temp_scale(temperature[lo]);
+    for (int node = node0; node < N; node += nw) {
+        if (node != node0) in = tree_node_inputs(s_no, B, parent, temperature, u_draft, node);
+        const int lo = in.lo, pa = in.pa;
+        const float c = in.c;
         int token = -1;
-        if (pa >= s_no[lo] && pa < node && nint[lo] >= 0 && c == c) {
+        // the partials of the parent's draft row (in the tree's range) are
+        // requested with the setup kernel's verdict on the tree, not after it
+        if (pa >= s_no[lo] && pa < node && c == c) {
+            const int ni = nint[lo];
             const float2 *pr = part + static_cast<int64_t>(pa) * g.n_sub;
             if (c == 0.0f) {
-                token = warp_combine_arg(pr, g.n_sub);
+                const int am = warp_combine_arg(pr, g.n_sub);
+                if (ni >= 0) token = am;
             } else {
                 float M, S;
                 float2 pc[kPartCache];
                 load_parts(pr, g.n_sub, pc);
-                if (combine_soft(pc, pr, g.n_sub, &M, &S)) token = warp_draw_row<DT>(draft, pa, pr, pc, g, c, M, u_draft[node]);
+                if (ni >= 0 && combine_soft(pc, pr, g.n_sub, &M, &S))
+                    token = warp_draw_row<DT>(draft, pa, pr, pc, g, c, M, in.ud);
             }
         }
         if (lane == 0) out[node] = token;
