@@ -822,6 +822,22 @@ __global__ void __launch_bounds__(kDrawThreads) resid_draw_kernel(
 // out_lse2 given, each row's log2-domain log-sum-exp (the value
 // resolve_kernel would combine from the same partials) is written too: NaN
 // for greedy and invalid rows.
+// A draft row's temperature scale (its sequence by bisection of the
+// offsets in shared memory) and drafting uniform.
+struct DraftRowIn {
+    float c, ud;
+};
+
+__device__ __forceinline__ DraftRowIn draft_row_inputs(const int *s_kofs, int B, const float *__restrict__ temperature,
+                                                       const float *__restrict__ u_draft, int r) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_kofs[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    return DraftRowIn{temp_scale(temperature[lo]), u_draft[r]};
+}
+
 template <int DT>
 __global__ void __launch_bounds__(256) draft_select_kernel(
     const void *__restrict__ draft, const float *__restrict__ temperature, const float *__restrict__ u_draft,
@@ -845,6 +861,16 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
         }
     }
     __syncthreads();
+    const int R = s_kofs[B];
+    const int lane = lane_id();
+    const int nw = (gridDim.x * blockDim.x) >> 5;
+    const int r0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    // a row's temperature scale and uniform: the caller's inputs, complete
+    // once the call's first kernel passed its wait, so the first row's are
+    // read before this kernel's wait (with valid offsets only: then r < R
+    // stays inside the caller's arrays)
+    DraftRowIn in{0.0f, 0.0f};
+    if (!s_bad && r0 < R) in = draft_row_inputs(s_kofs, B, temperature, u_draft, r0);
     grid_dependency_wait();
     grid_launch_dependents();
     if (s_bad) {
@@ -854,29 +880,24 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
     // the streaming pass timed out: its partials are of unknown age, so every
     // row gets -1 (and no normaliser) instead of a token that looks valid
     const bool timed_out = __ldcg(counters + kStatus) == SPEC_ERR_TIMEOUT;
-    const int R = s_kofs[B];
-    const int lane = lane_id();
-    const int nw = (gridDim.x * blockDim.x) >> 5;
-    for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < R; r += nw) {
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (s_kofs[mid] <= r) lo = mid; else hi = mid - 1;
-        }
-        const float c = timed_out ? __int_as_float(0x7fc00000) : temp_scale(temperature[lo]);
-        // (draft row r's partials are at slot R_t + r, R_t = R + B)
+    for (int r = r0; r < R; r += nw) {
+        if (r != r0) in = draft_row_inputs(s_kofs, B, temperature, u_draft, r);
+        const float c = timed_out ? __int_as_float(0x7fc00000) : in.c;
+        // (draft row r's partials are at slot R_t + r, R_t = R + B); they are
+        // requested with the status word, whatever the row's temperature (a
+        // row of a bad temperature has a slot too, its contents unused)
         const float2 *pr = part + (static_cast<int64_t>(R) + B + r) * g.n_sub;
+        float2 pc[kPartCache];
+        load_parts(pr, g.n_sub, pc);  // one round trip serves the combine and the draw
         int token = -1;
         double L = NAN;
         if (c == 0.0f) {
-            token = warp_combine_arg(pr, g.n_sub);
+            token = warp_combine_arg_cached(pc, pr, g.n_sub);
         } else if (c == c) {
             float M, S;
-            float2 pc[kPartCache];
-            load_parts(pr, g.n_sub, pc);  // one round trip serves the combine and the draw
             if (combine_soft(pc, pr, g.n_sub, &M, &S)) {
                 L = lse2(M, S);
-                token = warp_draw_row<DT>(draft, r, pr, pc, g, c, M, u_draft[r]);
+                token = warp_draw_row<DT>(draft, r, pr, pc, g, c, M, in.ud);
             }
         }
         if (lane == 0) {

@@ -678,24 +678,37 @@ static __device__ bool warp_combine_soft(const float2 *p, int n, float *M_out, f
 // Arg-max over the n sub-chunk partials of one row; -1 if a NaN was seen.
 // The first 32 * kPartCache partials arrive in one round trip (load_parts);
 // the merge is order-free (largest value, lowest index, NaN wins).
-static __device__ int warp_combine_arg(const float2 *p, int n) {
+// The same from the row's first 32 * kPartCache partials already loaded
+// (load_parts), the rest read here.
+static __device__ int warp_combine_arg_cached(const float2 (&c)[kPartCache], const float2 *p, int n) {
     const int lane = lane_id();
     ArgPart a{-INFINITY, INT_MAX};
-#if SPEC_ARG_BATCH
-    float2 c[kPartCache];
-    load_parts(p, n, c);
 #pragma unroll
     for (int j = 0; j < kPartCache; ++j)
         if (lane + 32 * j < n) a = arg_merge(a, ArgPart{c[j].x, __float_as_int(c[j].y)});
     for (int i = lane + 32 * kPartCache; i < n; i += 32) {
-#else
-    for (int i = lane; i < n; i += 32) {
-#endif
         const float2 v = __ldcg(p + i);
         a = arg_merge(a, ArgPart{v.x, __float_as_int(v.y)});
     }
     a = warp_arg(a);
     return a.i == INT_MAX ? -1 : a.i;
+}
+
+static __device__ int warp_combine_arg(const float2 *p, int n) {
+#if SPEC_ARG_BATCH
+    float2 c[kPartCache];
+    load_parts(p, n, c);
+    return warp_combine_arg_cached(c, p, n);
+#else
+    const int lane = lane_id();
+    ArgPart a{-INFINITY, INT_MAX};
+    for (int i = lane; i < n; i += 32) {
+        const float2 v = __ldcg(p + i);
+        a = arg_merge(a, ArgPart{v.x, __float_as_int(v.y)});
+    }
+    a = warp_arg(a);
+    return a.i == INT_MAX ? -1 : a.i;
+#endif
 }
 
 // warp_locate: warp-level locate over n non-negative weights (sub-chunk
