@@ -22,13 +22,18 @@
 //   2. stats_kernel       (tree mode) streams every node's target row and
 //                         the internal nodes' draft rows once, to sub-chunk
 //                         partials, as in the chain verify;
-//   3. tree_walk_kernel   block per sequence: walks the tree from the root.
-//                         At a node it combines the node's partials, tests
-//                         the children in order and, after each rejection,
+//   3. tree_walk_kernel   a cluster of two CTAs per sequence: a prologue
+//                         (the parent array checked and the internal nodes
+//                         listed again in the walk itself) combines every
+//                         node's partials and loads each child's logits;
+//                         the walk from the root then tests a node's
+//                         children in order and, after each rejection,
 //                         makes one pass over the node's two rows for the
-//                         residual mass (the rows are prefetched into L2 at
-//                         the first rejection, so later passes hit L2); the
-//                         last draw locates the sub-chunk from the pass's
+//                         residual mass, each CTA over half the sub-chunks
+//                         (the rows are prefetched into L2 at the first
+//                         rejection, so later passes hit L2), the halves'
+//                         sums meeting through a counter; the last draw
+//                         locates the sub-chunk from the pass's
 //                         per-sub-chunk masses and scans it.
 // spec_tree_draft_sample runs the setup, stats_kernel over the internal
 // nodes' draft rows, and tree_draft_select_kernel (warp per node: its token
