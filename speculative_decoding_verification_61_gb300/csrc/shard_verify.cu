@@ -13,10 +13,11 @@
 //                     decisions; then the rank's share of the mass to draw
 //                     from (a residual pass over its columns, or the bonus
 //                     row's mass from its partials);
-//   spec_shard_draw   shard_draw_kernel, one warp per sequence: the gathered
-//                     masses locate the rank holding the crossing of the
-//                     cumulative mass, and that rank alone draws inside its
-//                     columns.
+//   spec_shard_draw   shard_draw_kernel, one block per sequence: the
+//                     gathered masses locate the rank holding the crossing
+//                     of the cumulative mass, and that rank alone draws
+//                     inside its columns (its warp 0 locates the sub-chunk,
+//                     the block scans it).
 // The accept rule, residual and bonus are those of the chain verify
 // (docs.ifdog.com "投机解码", 投机解码的三步流程 step 3; bbs.huaweicloud.com
 // "大模型推理无损加速:投机采样(Speculative Decoding)数学原理与工业级落地实践",
