@@ -818,10 +818,6 @@ __global__ void __launch_bounds__(kDrawThreads) resid_draw_kernel(
     }
 }
 
-// Draft-side draw: one warp per draft row (grid-stride over rows).  With
-// out_lse2 given, each row's log2-domain log-sum-exp (the value
-// resolve_kernel would combine from the same partials) is written too: NaN
-// for greedy and invalid rows.
 // A draft row's temperature scale (its sequence by bisection of the
 // offsets in shared memory) and drafting uniform.
 struct DraftRowIn {
@@ -838,6 +834,10 @@ __device__ __forceinline__ DraftRowIn draft_row_inputs(const int *s_kofs, int B,
     return DraftRowIn{temp_scale(temperature[lo]), u_draft[r]};
 }
 
+// Draft-side draw: one warp per draft row (grid-stride over rows).  With
+// out_lse2 given, each row's log2-domain log-sum-exp (the value
+// resolve_kernel would combine from the same partials) is written too: NaN
+// for greedy and invalid rows.
 template <int DT>
 __global__ void __launch_bounds__(256) draft_select_kernel(
     const void *__restrict__ draft, const float *__restrict__ temperature, const float *__restrict__ u_draft,

@@ -748,10 +748,6 @@ __global__ void selfcheck_wait_kernel(int *counters, int *never) {
 }
 
 // ================================================================== drafting
-// Warp per node (grid-stride): a non-root node's token from its parent's
-// draft row (partials at slot parent, stats_kernel tree-draft mode):
-// arg-max at T = 0, else the inverse-CDF draw at u_draft[node].  Roots,
-// invalid sequences and invalid rows give -1.
 // A node's sequence (by bisection of the node offsets in shared memory),
 // parent, temperature scale and drafting uniform.
 struct TreeNodeIn {
@@ -770,6 +766,10 @@ __device__ __forceinline__ TreeNodeIn tree_node_inputs(const int *s_no, int B, c
     return TreeNodeIn{lo, parent[node], temp_scale(temperature[lo]), u_draft[node]};
 }
 
+// Warp per node (grid-stride): a non-root node's token from its parent's
+// draft row (partials at slot parent, stats_kernel tree-draft mode):
+// arg-max at T = 0, else the inverse-CDF draw at u_draft[node].  Roots,
+// invalid sequences and invalid rows give -1.
 template <int DT>
 __global__ void __launch_bounds__(256) tree_draft_select_kernel(
     const void *__restrict__ draft, const int *__restrict__ node_offsets, const int *__restrict__ parent,
